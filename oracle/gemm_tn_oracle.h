@@ -1,0 +1,77 @@
+/*
+ * CPU oracle for the half-precision TN GEMM — TEST INFRASTRUCTURE ONLY.
+ *
+ * Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference
+ * legs may load this code.  The product path (the CUDA library) never calls it
+ * and shares no code, header, table or helper with it.
+ *
+ * What it computes (one definition, written out plainly):
+ *
+ *   D[b][m][n] = RNE_fp16( alpha * sum_{k<K} A[b][m][k] * B[b][n][k]
+ *                          + beta * C[b][m][n] )
+ *
+ *   - the TN contraction of "CuTe C++ 简介01 … gemm_device", section 3
+ *     (appendix code: the SIMT loop tCrC(m,n) += tCsA(m,k) * tCsB(n,k));
+ *   - the epilogue C = alpha*A*B + beta*C of the same page (axpby, and the
+ *     kernel signature in section 1);
+ *   - A (M,K) and B (N,K) both K-contiguous, D (M,N) N-contiguous, as in
+ *     "cute(8) smem_gemm", section "代码实现" (make_stride(K, Int<1>)).
+ *
+ * Readings taken where the pages are silent:
+ *   - every fp16 operand is decoded exactly to fp64; products and the k-ordered
+ *     sum are done in fp64; alpha and beta are fp32 values widened to fp64;
+ *   - exactly one rounding to fp16 at the end, IEEE round-to-nearest-even,
+ *     subnormals kept, overflow to +-inf, NaN stays NaN;
+ *   - beta == 0 drops the C term entirely (C is not read, may be NULL);
+ *   - K == 0 gives D = RNE(beta*C); M == 0 or N == 0 does nothing.
+ *
+ * Parity pins (tests/test_oracle_pins.py): exhaustive fp16 decode and encode
+ * against numpy's IEEE conversions, exact rational brute force on tiny shapes,
+ * identity / permutation matrices, the all-ones closed form, the transpose
+ * invariant D(A,B)^T = D(B,A), small-integer exactness against integer matmul.
+ */
+#ifndef GEMM_TN_ORACLE_H
+#define GEMM_TN_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exact binary16 -> binary64 decode (IEEE 754 binary16 bit layout). */
+double gto_half_to_double(uint16_t h);
+
+/* binary64 -> binary16, round to nearest, ties to even. */
+uint16_t gto_double_to_half(double x);
+
+/*
+ * Batched TN GEMM over flattened output rows r in [r_begin, r_end), where
+ * r = b*M + m.  Matrices are arrays of binary16 bit patterns; strides and
+ * leading dimensions are in elements.  C may be NULL when beta == 0.
+ */
+void gto_gemm_tn_f16(const uint16_t* A, int64_t lda, int64_t strideA,
+                     const uint16_t* B, int64_t ldb, int64_t strideB,
+                     const uint16_t* C, int64_t ldc, int64_t strideC,
+                     uint16_t* D, int64_t ldd, int64_t strideD,
+                     int64_t M, int64_t N, int64_t K,
+                     float alpha, float beta,
+                     int64_t r_begin, int64_t r_end);
+
+/*
+ * The same definition evaluated at `count` chosen output positions
+ * (b_idx[i], m_idx[i], n_idx[i]); results go to out[i].
+ */
+void gto_gemm_tn_f16_entries(const uint16_t* A, int64_t lda, int64_t strideA,
+                             const uint16_t* B, int64_t ldb, int64_t strideB,
+                             const uint16_t* C, int64_t ldc, int64_t strideC,
+                             int64_t K, float alpha, float beta,
+                             const int64_t* b_idx, const int64_t* m_idx,
+                             const int64_t* n_idx, int64_t count,
+                             uint16_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_TN_ORACLE_H */

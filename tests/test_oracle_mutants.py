@@ -1,0 +1,48 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and check that
+the pins catch every one of them."""
+import os
+
+import pytest
+
+import oracle
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "gemm_tn_oracle.c")
+
+# (name, text in the oracle source, replacement)
+MUTANTS = [
+    ("drop_beta_term", "v = v + beta * g_decode[*c_elem];", "v = v;"),
+    ("drop_alpha", "double v = alpha * acc;", "double v = acc;"),
+    ("wrong_operand", "g_decode[a_row[k]] * g_decode[b_row[k]]", "g_decode[a_row[k]] * g_decode[a_row[k]]"),
+    ("skip_last_k", "for (int64_t k = 0; k < K; ++k) {\n        acc +=", "for (int64_t k = 0; k + 1 < K; ++k) {\n        acc +="),
+    ("b_uses_lda", "B + b * strideB + n * ldb;", "B + b * strideB + n * lda;"),
+    ("c_transposed", "(C + b * strideC + m * ldc + n) : NULL;\n            D[", "(C + b * strideC + n * ldc + m) : NULL;\n            D["),
+    ("batch_stride_mixup", "const uint16_t* a_row = A + b * strideA + m * lda;\n        for", "const uint16_t* a_row = A + b * strideB + m * lda;\n        for"),
+    ("truncate_not_rne", "rint(ldexp(a, -q))", "trunc(ldexp(a, -q))"),
+    ("ties_away", "rint(ldexp(a, -q))", "round(ldexp(a, -q))"),
+    ("saturate_not_inf", "if (bits >= 0x7c00) bits = 0x7c00;", "if (bits >= 0x7c00) bits = 0x7bff;"),
+    ("subnormal_scale", "v = ldexp((double)frac, -24);", "v = ldexp((double)frac, -25);"),
+    ("exponent_bias", "expo - 25);", "expo - 24);"),
+    ("lost_sign", "return sign ? -v : v;", "return v;"),
+    ("flush_subnormals", "const int q = (E < -14) ? -24 : E - 10;", "const int q = (E < -14) ? 99 : E - 10;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    mutated = src.replace(old, new, 1)
+    path = tmp_path / f"{name}.c"
+    path.write_text(mutated)
+    lib = oracle.compile_source(str(path), str(tmp_path / f"lib_{name}.so"))
+    o = oracle.Oracle.from_path(lib)
+    failures = []
+    for check in pins.CONVERSION_CHECKS[:3] + pins.GEMM_CHECKS:
+        try:
+            check(o)
+        except AssertionError:
+            failures.append(check.__name__)
+        except Exception as e:  # noqa: BLE001 - a crash in a check also counts as caught
+            failures.append(f"{check.__name__}:{type(e).__name__}")
+    assert failures, f"mutant {name} passed every pin"
