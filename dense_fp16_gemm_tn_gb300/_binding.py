@@ -1,0 +1,176 @@
+"""ctypes binding to ``libgemm_tn_f16.so`` — argument marshalling only.
+
+Each function has the name and argument order of the C function it calls
+(see ``include/gemm_tn_f16.h``).  Pointer arguments accept an integer
+address, ``None`` (NULL) or any object with ``data_ptr()`` (a torch tensor);
+``stream`` accepts an integer handle, ``None`` (the legacy default stream) or
+an object with a ``cuda_stream`` attribute (a torch stream).  All arithmetic
+happens in the library's CUDA kernels; there is no fallback: if the library
+is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+GEMM_OK = 0
+GEMM_ERR_INVALID_VALUE = 1
+GEMM_ERR_MISALIGNED = 2
+GEMM_ERR_UNSUPPORTED = 3
+GEMM_ERR_CUDA = 4
+GEMM_ERR_TIMEOUT = 5
+GEMM_ERR_WORKSPACE = 6
+
+GEMM_TN_OPT_WAIT_TIMEOUT_NS = 1
+GEMM_TN_OPT_SKIP_FIRST_LOAD = 2
+GEMM_TN_OPT_FORCE_BN = 3
+GEMM_TN_OPT_FORCE_PAIR = 4
+GEMM_TN_OPT_FORCE_SPLITS = 5
+GEMM_TN_OPT_FORCE_SWAP = 6
+GEMM_TN_OPT_FORCE_GENERIC_EPI = 7
+GEMM_TN_OPT_FORCE_PACK = 8
+
+EXPORTED = ["gemm_tn_f16", "gemm_tn_f16_batched", "gemm_status_string", "gemm_tn_f16_last_device_error",
+            "gemm_tn_f16_last_cuda_error", "gemm_tn_f16_shutdown", "gemm_tn_f16_version", "gemm_tn_f16_plan",
+            "gemm_tn_f16_set_option", "gemm_tn_f16_get_option"]
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {gemm_status_string(status)} (status {status})")
+
+
+class gemm_tn_plan_t(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("cta_pair", ctypes.c_int32), ("swap_ab", ctypes.c_int32), ("splits", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("epi_tma", ctypes.c_int32), ("pack_a", ctypes.c_int32),
+                ("pack_b", ctypes.c_int32), ("units", ctypes.c_int64), ("grid", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load_library(build_if_missing: bool = True):
+    """Load (building first if needed) the shared library.  Raises if it cannot."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB_PATH
+        if not os.path.exists(path) or not _build.up_to_date():
+            if not build_if_missing:
+                raise RuntimeError(f"{path} is missing; run dense_fp16_gemm_tn_gb300.build.build()")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        vp, i64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
+        lib.gemm_tn_f16.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, f32, f32, vp]
+        lib.gemm_tn_f16.restype = ctypes.c_int
+        lib.gemm_tn_f16_batched.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, i64, vp, i64, i64,
+                                            i64, i64, i64, i64, f32, f32, vp]
+        lib.gemm_tn_f16_batched.restype = ctypes.c_int
+        lib.gemm_status_string.argtypes = [ctypes.c_int]
+        lib.gemm_status_string.restype = ctypes.c_char_p
+        lib.gemm_tn_f16_last_device_error.argtypes = []
+        lib.gemm_tn_f16_last_device_error.restype = ctypes.c_int
+        lib.gemm_tn_f16_last_cuda_error.argtypes = []
+        lib.gemm_tn_f16_last_cuda_error.restype = ctypes.c_int
+        lib.gemm_tn_f16_shutdown.argtypes = []
+        lib.gemm_tn_f16_shutdown.restype = None
+        lib.gemm_tn_f16_version.argtypes = []
+        lib.gemm_tn_f16_version.restype = ctypes.c_int
+        lib.gemm_tn_f16_plan.argtypes = [i64] * 12 + [f32, ctypes.c_uint32, ctypes.c_int32,
+                                                       ctypes.POINTER(gemm_tn_plan_t)]
+        lib.gemm_tn_f16_plan.restype = ctypes.c_int
+        lib.gemm_tn_f16_set_option.argtypes = [ctypes.c_int32, i64]
+        lib.gemm_tn_f16_set_option.restype = ctypes.c_int
+        lib.gemm_tn_f16_get_option.argtypes = [ctypes.c_int32]
+        lib.gemm_tn_f16_get_option.restype = ctypes.c_int64
+        _lib = lib
+        return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if hasattr(s, "cuda_stream"):
+        return s.cuda_stream
+    return int(s)
+
+
+def _check(status, where, check):
+    if check and status != GEMM_OK:
+        raise GemmError(status, where)
+    return status
+
+
+def gemm_tn_f16(A, lda, B, ldb, C, ldc, D, ldd, M, N, K, alpha, beta, stream=None, *, check=True):
+    st = load_library().gemm_tn_f16(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _ptr(D), ldd, M, N, K,
+                                    float(alpha), float(beta), _stream(stream))
+    return _check(st, "gemm_tn_f16", check)
+
+
+def gemm_tn_f16_batched(A, lda, strideA, B, ldb, strideB, C, ldc, strideC, D, ldd, strideD,
+                        M, N, K, batch, alpha, beta, stream=None, *, check=True):
+    st = load_library().gemm_tn_f16_batched(_ptr(A), lda, strideA, _ptr(B), ldb, strideB, _ptr(C), ldc, strideC,
+                                            _ptr(D), ldd, strideD, M, N, K, batch, float(alpha), float(beta),
+                                            _stream(stream))
+    return _check(st, "gemm_tn_f16_batched", check)
+
+
+def gemm_status_string(status: int) -> str:
+    return load_library().gemm_status_string(int(status)).decode()
+
+
+def gemm_tn_f16_last_device_error() -> int:
+    return load_library().gemm_tn_f16_last_device_error()
+
+
+def gemm_tn_f16_last_cuda_error() -> int:
+    return load_library().gemm_tn_f16_last_cuda_error()
+
+
+def gemm_tn_f16_shutdown() -> None:
+    load_library().gemm_tn_f16_shutdown()
+
+
+def gemm_tn_f16_version() -> int:
+    return load_library().gemm_tn_f16_version()
+
+
+def gemm_tn_f16_plan(M, N, K, batch, lda, ldb, ldc, ldd, strideA, strideB, strideC, strideD,
+                     beta, align_flags, num_sms):
+    plan = gemm_tn_plan_t()
+    st = load_library().gemm_tn_f16_plan(M, N, K, batch, lda, ldb, ldc, ldd, strideA, strideB, strideC, strideD,
+                                         float(beta), align_flags, num_sms, ctypes.byref(plan))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_tn_f16_plan")
+    return plan.as_dict()
+
+
+def gemm_tn_f16_set_option(option: int, value: int) -> None:
+    _check(load_library().gemm_tn_f16_set_option(int(option), int(value)), "gemm_tn_f16_set_option", True)
+
+
+def gemm_tn_f16_get_option(option: int) -> int:
+    return load_library().gemm_tn_f16_get_option(int(option))

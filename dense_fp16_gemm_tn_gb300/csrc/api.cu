@@ -1,0 +1,568 @@
+// Host side of the C ABI declared in include/gemm_tn_f16.h: argument checks,
+// kernel planning, scratch memory, TMA tensor maps and launches.
+//
+// The operation is the TN GEMM D = alpha * A . B^T + beta * C of the
+// "gemm_device 逐行解析" page (section 1, the kernel signature with alpha and
+// beta; section 3, the axpby epilogue), with the (M,K)/(N,K) K-contiguous
+// operand views of "cute(8) smem_gemm" (section 代码实现).  Unlike the pages'
+// host code (torch::Tensor arguments, CUDA_CHECK calling exit() on failure),
+// this layer takes plain pointers, never exits, and reports every failure as
+// a gemm_status_t.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_tn_f16.h"
+#include "internal.h"
+
+namespace gtn {
+
+// Device error word written by timed-out waits (see tc_gemm.cuh).
+__device__ uint32_t g_error_word = 0;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+std::atomic<int64_t> g_opt_timeout_ns{2000000000ll};
+std::atomic<int64_t> g_opt_skip_first_load{0};
+std::atomic<int64_t> g_opt_force_bn{0};
+std::atomic<int64_t> g_opt_force_pair{0};
+std::atomic<int64_t> g_opt_force_splits{0};
+std::atomic<int64_t> g_opt_force_swap{0};
+std::atomic<int64_t> g_opt_force_generic{0};
+std::atomic<int64_t> g_opt_force_pack{0};
+
+gemm_status_t cuda_fail(cudaError_t e) {
+    t_last_cuda_error = static_cast<int>(e);
+    return GEMM_ERR_CUDA;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
+
+// ------------------------------------------------------------------ per-device state
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int major = 0, minor = 0;
+    uint32_t* err = nullptr;
+    cudaMemPool_t pool = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_devices[kMaxDevices];
+std::mutex g_dev_mu;
+
+gemm_status_t device_state(DeviceState** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return GEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceState& d = g_devices[dev];
+    if (!d.ready) {
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return cuda_fail(e);
+        if (!(d.major == 10 && d.minor == 3)) return GEMM_ERR_UNSUPPORTED;  // kernels are built for sm_103a only
+        void* p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_error_word)) != cudaSuccess) return cuda_fail(e);
+        d.err = static_cast<uint32_t*>(p);
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if ((e = cudaMemPoolCreate(&d.pool, &props)) != cudaSuccess) return cuda_fail(e);
+        uint64_t keep = UINT64_MAX;  // keep freed scratch cached in the pool
+        if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
+            return cuda_fail(e);
+        d.ready = true;
+    }
+    *out = &d;
+    return GEMM_OK;
+}
+
+// ------------------------------------------------------------------ tensor maps
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D fp16 tensor map over (inner, rows, batch) with a box of (box_inner, box_rows, 1)
+// and 128-byte swizzle.  `batched` false maps a single matrix (batch extent 1).
+bool encode_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t batch, int64_t ld,
+                int64_t stride, bool batched, uint32_t box_inner, uint32_t box_rows) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
+                          static_cast<cuuint64_t>(batched ? batch : 1)};
+    const int64_t st = batched ? stride : ld * rows;
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2u, static_cast<cuuint64_t>(st) * 2u};
+    cuuint32_t box[3] = {box_inner, box_rows, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ problem + plan
+
+struct Problem {
+    int64_t M, N, K, batch;
+    int64_t lda, ldb, ldc, ldd;
+    int64_t sA, sB, sC, sD;
+    float beta;
+    uint32_t align;  // bit i: operand i (A,B,C,D) base is 16-byte aligned
+};
+
+struct Plan {
+    gemm_tn_plan_t pub;
+    TcVariant var;
+    int32_t epi;
+    int64_t rows_a, rows_b;
+    int64_t tiles_m, tiles_n;
+    int64_t ldo_a, ldo_b;        // leading dims of the packed copies
+    int64_t pack_a_bytes, pack_b_bytes, partial_bytes;
+    int group_m;
+};
+
+bool operand_tma_ok(bool aligned16, int64_t ld, int64_t stride, int64_t batch) {
+    return aligned16 && ld % 8 == 0 && (batch == 1 || stride % 8 == 0);
+}
+
+gemm_status_t validate(const Problem& p) {
+    if (p.M < 0 || p.N < 0 || p.K < 0 || p.batch < 0) return GEMM_ERR_INVALID_VALUE;
+    const int64_t lim = int64_t(1) << 31;
+    if (p.M >= lim || p.N >= lim || p.K >= lim || p.batch >= lim) return GEMM_ERR_UNSUPPORTED;
+    if (p.M == 0 || p.N == 0 || p.batch == 0) return GEMM_OK;
+    if (p.ldd < std::max<int64_t>(p.N, 1)) return GEMM_ERR_INVALID_VALUE;
+    if (p.K > 0 && (p.lda < p.K || p.ldb < p.K)) return GEMM_ERR_INVALID_VALUE;
+    if (p.beta != 0.0f && p.ldc < std::max<int64_t>(p.N, 1)) return GEMM_ERR_INVALID_VALUE;
+    if (p.batch > 1) {
+        if (p.sA < 0 || p.sB < 0 || p.sC < 0 || p.sD < 0) return GEMM_ERR_INVALID_VALUE;
+        if (p.sD < (p.M - 1) * p.ldd + p.N) return GEMM_ERR_INVALID_VALUE;  // output entries must be disjoint
+    }
+    return GEMM_OK;
+}
+
+// Tensor-core tile plan; pure host arithmetic, no CUDA calls.
+void make_plan(const Problem& pr, int sms, Plan& pl) {
+    std::memset(&pl, 0, sizeof(pl));
+    gemm_tn_plan_t& pub = pl.pub;
+    pub.splits = 1;
+    if (pr.M == 0 || pr.N == 0 || pr.batch == 0) {
+        pub.kernel = 0;
+        return;
+    }
+    if (pr.K == 0) {
+        pub.kernel = 1;
+        pub.units = pr.batch;
+        return;
+    }
+    const bool force_pack = g_opt_force_pack.load() != 0;
+    pub.pack_a = (force_pack || !operand_tma_ok(pr.align & 1u, pr.lda, pr.sA, pr.batch)) ? 1 : 0;
+    pub.pack_b = (force_pack || !operand_tma_ok(pr.align & 2u, pr.ldb, pr.sB, pr.batch)) ? 1 : 0;
+    const bool d_ok = operand_tma_ok(pr.align & 8u, pr.ldd, pr.sD, pr.batch);
+
+    // Small M: swap operands so that the long N side fills the 128 tensor-memory lanes.
+    bool swap = pr.M <= 64 && pr.N >= 128 && pr.N >= 2 * pr.M;
+    const int64_t fs = g_opt_force_swap.load();
+    if (fs > 0 && pr.M <= 64) swap = true;
+    if (fs < 0) swap = false;
+
+    int bn, pair;
+    const int64_t slots = std::max(sms, 1);
+    if (swap) {
+        bn = pr.M <= 16 ? 16 : pr.M <= 32 ? 32 : 64;
+        pair = 1;
+    } else {
+        const int64_t t_pair = ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.batch;
+        const int64_t t_256 = ceil_div(pr.M, 128) * ceil_div(pr.N, 256) * pr.batch;
+        if (pr.K >= 512 && 2 * t_pair >= slots) {
+            pair = 2;
+            bn = 256;
+        } else if (t_256 >= slots || pr.N > 128 * 8) {
+            pair = 1;
+            bn = 256;
+        } else {
+            pair = 1;
+            bn = 128;
+        }
+        const int64_t fbn = g_opt_force_bn.load(), fpair = g_opt_force_pair.load();
+        if (fbn == 128 || fbn == 256) bn = static_cast<int>(fbn);
+        if (fpair == 1 || fpair == 2) pair = static_cast<int>(fpair);
+    }
+    const int64_t rows_a = swap ? pr.N : pr.M;
+    const int64_t rows_b = swap ? pr.M : pr.N;
+    const int64_t kb = ceil_div(pr.K, 64);
+
+    // Split K when the tiles alone cannot fill the machine.
+    int splits = 1;
+    const int64_t tiles_1 = ceil_div(rows_a, 128) * ceil_div(rows_b, swap ? bn : 128) * pr.batch;
+    if (pair == 1 && kb >= 8 && tiles_1 * 2 <= slots) {
+        int64_t best = INT64_MAX;
+        const int64_t max_s = std::min<int64_t>(64, kb / 4);
+        for (int64_t s = 1; s <= max_s; ++s) {
+            const int64_t cost = ceil_div(tiles_1 * s, slots) * (ceil_div(kb, s) + 2);
+            if (cost < best) {
+                best = cost;
+                splits = static_cast<int>(s);
+            }
+        }
+    }
+    const int64_t fsplit = g_opt_force_splits.load();
+    if (fsplit >= 1 && pair == 1) splits = static_cast<int>(std::min<int64_t>(fsplit, kb));
+    if (splits > 1 && !swap) bn = 128;  // the partial-sum variant exists at 128 columns
+
+    int epi;
+    if (splits > 1) epi = swap ? EPI_PARTIAL_SWAP : EPI_PARTIAL;
+    else if (swap) epi = EPI_SWAP;
+    else if (pr.beta == 0.0f && d_ok && g_opt_force_generic.load() == 0) epi = EPI_TMA;
+    else epi = EPI_GENERIC;
+
+    TcVariant v;
+    if (!find_tc_variant(bn, pair, epi, &v)) {
+        // Fall back to the single-CTA variant of the same epilogue.
+        pair = 1;
+        if (!find_tc_variant(bn, pair, epi, &v)) {
+            bn = 128;
+            find_tc_variant(bn, pair, epi, &v);
+        }
+    }
+    pl.var = v;
+    pl.epi = epi;
+    pl.rows_a = rows_a;
+    pl.rows_b = rows_b;
+    pl.tiles_m = ceil_div(rows_a, 128 * pair);
+    pl.tiles_n = ceil_div(rows_b, bn);
+    pl.group_m = pair == 2 ? 8 : 16;
+
+    pub.kernel = splits > 1 ? 3 : 2;
+    pub.tile_m = 128 * pair;
+    pub.tile_n = bn;
+    pub.cta_pair = pair;
+    pub.swap_ab = swap ? 1 : 0;
+    pub.splits = splits;
+    pub.stages = v.stages;
+    pub.epi_tma = epi == EPI_TMA ? 1 : 0;
+    pub.units = pl.tiles_m * pl.tiles_n * pr.batch * splits;
+    pub.grid = std::min<int64_t>(pub.units * pair, (slots / pair) * pair);
+
+    pl.ldo_a = round_up(pr.K, 8);
+    pl.ldo_b = round_up(pr.K, 8);
+    const int64_t nba = (pr.batch > 1 && pr.sA != 0) ? pr.batch : 1;
+    const int64_t nbb = (pr.batch > 1 && pr.sB != 0) ? pr.batch : 1;
+    pl.pack_a_bytes = pub.pack_a ? round_up(nba * pr.M * pl.ldo_a * 2, 256) : 0;
+    pl.pack_b_bytes = pub.pack_b ? round_up(nbb * pr.N * pl.ldo_b * 2, 256) : 0;
+    pl.partial_bytes = splits > 1 ? round_up(pr.batch * splits * pr.M * pr.N * 4, 256) : 0;
+    pub.workspace_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool ranges_overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(b_bytes) && b0 < a0 + static_cast<uintptr_t>(a_bytes);
+}
+
+int64_t extent_bytes(int64_t rows, int64_t cols, int64_t ld, int64_t stride, int64_t batch) {
+    return 2 * ((batch - 1) * stride + (rows - 1) * ld + cols);
+}
+
+gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Problem& pr, float alpha,
+                  cudaStream_t stream) {
+    gemm_status_t st = validate(pr);
+    if (st != GEMM_OK) return st;
+    if (pr.M == 0 || pr.N == 0 || pr.batch == 0) return GEMM_OK;
+    if (!D) return GEMM_ERR_INVALID_VALUE;
+    if (pr.K > 0 && (!A || !B)) return GEMM_ERR_INVALID_VALUE;
+    if (pr.beta != 0.0f && !C) return GEMM_ERR_INVALID_VALUE;
+    auto odd = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) != 0; };
+    if (odd(D) || (pr.K > 0 && (odd(A) || odd(B))) || (pr.beta != 0.0f && odd(C))) return GEMM_ERR_MISALIGNED;
+
+    // D must not overlap any input, except C exactly.
+    const int64_t d_bytes = extent_bytes(pr.M, pr.N, pr.ldd, pr.sD, pr.batch);
+    if (pr.K > 0) {
+        if (ranges_overlap(D, d_bytes, A, extent_bytes(pr.M, pr.K, pr.lda, pr.sA, pr.batch)) ||
+            ranges_overlap(D, d_bytes, B, extent_bytes(pr.N, pr.K, pr.ldb, pr.sB, pr.batch)))
+            return GEMM_ERR_INVALID_VALUE;
+    }
+    if (pr.beta != 0.0f) {
+        if (C == D) {
+            if (pr.ldc != pr.ldd || (pr.batch > 1 && pr.sC != pr.sD)) return GEMM_ERR_INVALID_VALUE;
+        } else if (ranges_overlap(D, d_bytes, C, extent_bytes(pr.M, pr.N, pr.ldc, pr.sC, pr.batch))) {
+            return GEMM_ERR_INVALID_VALUE;
+        }
+    }
+
+    DeviceState* dev = nullptr;
+    if ((st = device_state(&dev)) != GEMM_OK) return st;
+
+    cudaError_t e;
+    if (pr.K == 0) {
+        e = launch_scale(pr.M, pr.N, pr.batch, pr.beta, C, pr.ldc, pr.sC, D, pr.ldd, pr.sD, dev->sms, stream);
+        return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+    }
+
+    Problem p = pr;
+    p.align = (aligned16(A) ? 1u : 0u) | (aligned16(B) ? 2u : 0u) | (aligned16(C) ? 4u : 0u) |
+              (aligned16(D) ? 8u : 0u);
+    Plan pl;
+    make_plan(p, dev->sms, pl);
+
+    // Tensor maps first: an operand whose map the driver rejects is repacked instead.
+    const bool swap = pl.pub.swap_ab != 0;
+    const uint32_t box_rows_b = static_cast<uint32_t>(pl.var.bn / pl.var.pair);
+    CUtensorMap mapA_op, mapB_op, mapD;
+    std::memset(&mapD, 0, sizeof(mapD));
+    // Problem operand A is the MMA's B operand when swapped, else its A operand.
+    const uint32_t boxA = swap ? box_rows_b : 128u;
+    const uint32_t boxB = swap ? 128u : box_rows_b;
+    CUtensorMap mapPA, mapPB;
+    if (!pl.pub.pack_a && !encode_map(&mapPA, A, p.K, p.M, p.batch, p.lda, p.sA, p.batch > 1 && p.sA != 0, 64, boxA))
+        pl.pub.pack_a = 1, pl.pack_a_bytes = round_up(((p.batch > 1 && p.sA != 0) ? p.batch : 1) * p.M * pl.ldo_a * 2, 256);
+    if (!pl.pub.pack_b && !encode_map(&mapPB, B, p.K, p.N, p.batch, p.ldb, p.sB, p.batch > 1 && p.sB != 0, 64, boxB))
+        pl.pub.pack_b = 1, pl.pack_b_bytes = round_up(((p.batch > 1 && p.sB != 0) ? p.batch : 1) * p.N * pl.ldo_b * 2, 256);
+    if (pl.epi == EPI_TMA &&
+        !encode_map(&mapD, D, p.N, p.M, p.batch, p.ldd, p.sD, p.batch > 1, 64, 32)) {
+        TcVariant v;
+        if (find_tc_variant(pl.var.bn, pl.var.pair, EPI_GENERIC, &v)) {
+            pl.var = v;
+            pl.epi = EPI_GENERIC;
+            pl.pub.epi_tma = 0;
+        } else {
+            return GEMM_ERR_UNSUPPORTED;
+        }
+    }
+
+    const int64_t ws_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes;
+    uint8_t* ws = nullptr;
+    if (ws_bytes > 0) {
+        e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), static_cast<size_t>(ws_bytes), dev->pool, stream);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_WORKSPACE;
+        }
+    }
+    auto release = [&]() {
+        if (ws) cudaFreeAsync(ws, stream);
+    };
+
+    const bool a_batched = p.batch > 1 && p.sA != 0;
+    const bool b_batched = p.batch > 1 && p.sB != 0;
+    if (pl.pub.pack_a) {
+        void* dst = ws;
+        e = launch_repack(A, p.lda, p.sA, dst, pl.ldo_a, p.M, p.K, a_batched ? p.batch : 1, dev->sms, stream);
+        if (e != cudaSuccess) { release(); return cuda_fail(e); }
+        if (!encode_map(&mapPA, dst, p.K, p.M, p.batch, pl.ldo_a, p.M * pl.ldo_a, a_batched, 64, boxA)) {
+            release();
+            return GEMM_ERR_UNSUPPORTED;
+        }
+    }
+    if (pl.pub.pack_b) {
+        void* dst = ws + pl.pack_a_bytes;
+        e = launch_repack(B, p.ldb, p.sB, dst, pl.ldo_b, p.N, p.K, b_batched ? p.batch : 1, dev->sms, stream);
+        if (e != cudaSuccess) { release(); return cuda_fail(e); }
+        if (!encode_map(&mapPB, dst, p.K, p.N, p.batch, pl.ldo_b, p.N * pl.ldo_b, b_batched, 64, boxB)) {
+            release();
+            return GEMM_ERR_UNSUPPORTED;
+        }
+    }
+    mapA_op = swap ? mapPB : mapPA;
+    mapB_op = swap ? mapPA : mapPB;
+    if (pl.epi != EPI_TMA) mapD = mapA_op;  // unused by the kernel; any valid map
+
+    KParams kp;
+    std::memset(&kp, 0, sizeof(kp));
+    kp.rows_a = static_cast<int32_t>(pl.rows_a);
+    kp.rows_b = static_cast<int32_t>(pl.rows_b);
+    kp.K = static_cast<int32_t>(p.K);
+    kp.batch = static_cast<int32_t>(p.batch);
+    kp.tiles_m = static_cast<int32_t>(pl.tiles_m);
+    kp.tiles_n = static_cast<int32_t>(pl.tiles_n);
+    kp.splits = pl.pub.splits;
+    kp.kb_total = static_cast<int32_t>(ceil_div(p.K, 64));
+    kp.group_m = pl.group_m;
+    kp.zA = swap ? (b_batched ? 1 : 0) : (a_batched ? 1 : 0);
+    kp.zB = swap ? (a_batched ? 1 : 0) : (b_batched ? 1 : 0);
+    kp.zD = p.batch > 1 ? 1 : 0;
+    kp.num_units = pl.tiles_m * pl.tiles_n * p.batch * pl.pub.splits;
+    kp.M = static_cast<int32_t>(p.M);
+    kp.N = static_cast<int32_t>(p.N);
+    kp.alpha = alpha;
+    kp.beta = p.beta;
+    kp.D = D;
+    kp.ldd = p.ldd;
+    kp.strideD = p.sD;
+    kp.C = C;
+    kp.ldc = p.ldc;
+    kp.strideC = p.sC;
+    kp.W = pl.pub.splits > 1 ? reinterpret_cast<float*>(ws + pl.pack_a_bytes + pl.pack_b_bytes) : nullptr;
+    kp.err = dev->err;
+    kp.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
+    kp.debug_skip_first_load = g_opt_skip_first_load.load() != 0 ? 1 : 0;
+
+    const int64_t cap = tc_variant_capacity(pl.var, dev->sms);
+    int64_t grid = 0;
+    e = launch_tc_variant(pl.var, mapA_op, mapB_op, mapD, kp, cap > 0 ? cap : dev->sms, stream, &grid);
+    if (e != cudaSuccess) { release(); return cuda_fail(e); }
+    if (pl.pub.splits > 1) {
+        e = launch_splitk_reduce(kp.W, pl.pub.splits, p.M, p.N, p.batch, alpha, p.beta, C, p.ldc, p.sC, D, p.ldd,
+                                 p.sD, dev->sms, stream);
+        if (e != cudaSuccess) { release(); return cuda_fail(e); }
+    }
+    release();
+    return GEMM_OK;
+}
+
+}  // namespace
+}  // namespace gtn
+
+using namespace gtn;
+
+extern "C" {
+
+gemm_status_t gemm_tn_f16(const void* A, int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc,
+                          void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                          gemm_stream_t stream) {
+    Problem p = {M, N, K, 1, lda, ldb, ldc, ldd, 0, 0, 0, 0, beta, 0};
+    return run(A, B, C, D, p, alpha, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_tn_f16_batched(const void* A, int64_t lda, int64_t strideA, const void* B, int64_t ldb,
+                                  int64_t strideB, const void* C, int64_t ldc, int64_t strideC, void* D, int64_t ldd,
+                                  int64_t strideD, int64_t M, int64_t N, int64_t K, int64_t batch, float alpha,
+                                  float beta, gemm_stream_t stream) {
+    Problem p = {M, N, K, batch, lda, ldb, ldc, ldd, strideA, strideB, strideC, strideD, beta, 0};
+    return run(A, B, C, D, p, alpha, reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* gemm_status_string(gemm_status_t s) {
+    switch (s) {
+        case GEMM_OK: return "success";
+        case GEMM_ERR_INVALID_VALUE: return "invalid value (size, leading dimension, stride, overlap or NULL pointer)";
+        case GEMM_ERR_MISALIGNED: return "pointer not 2-byte aligned";
+        case GEMM_ERR_UNSUPPORTED: return "unsupported device or problem size";
+        case GEMM_ERR_CUDA: return "CUDA runtime or driver error";
+        case GEMM_ERR_TIMEOUT: return "device-side wait timed out";
+        case GEMM_ERR_WORKSPACE: return "scratch memory unavailable";
+    }
+    return "unknown status";
+}
+
+gemm_status_t gemm_tn_f16_last_device_error(void) {
+    DeviceState* dev = nullptr;
+    gemm_status_t st = device_state(&dev);
+    if (st != GEMM_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    uint32_t word = 0;
+    if ((e = cudaMemcpy(&word, dev->err, sizeof(word), cudaMemcpyDeviceToHost)) != cudaSuccess) return cuda_fail(e);
+    if (word != 0) {
+        const uint32_t zero = 0;
+        if ((e = cudaMemcpy(dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess) return cuda_fail(e);
+        return (word >> 8) == 5u ? GEMM_ERR_TIMEOUT : GEMM_ERR_CUDA;
+    }
+    return GEMM_OK;
+}
+
+int gemm_tn_f16_last_cuda_error(void) { return t_last_cuda_error; }
+
+void gemm_tn_f16_shutdown(void) {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    int cur = 0;
+    const bool have_cur = cudaGetDevice(&cur) == cudaSuccess;
+    for (int i = 0; i < kMaxDevices; ++i) {
+        DeviceState& d = g_devices[i];
+        if (d.ready && d.pool) {
+            cudaSetDevice(i);
+            cudaDeviceSynchronize();
+            cudaMemPoolDestroy(d.pool);
+            d.pool = nullptr;
+            d.ready = false;
+        }
+    }
+    if (have_cur) cudaSetDevice(cur);
+}
+
+int gemm_tn_f16_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t lda, int64_t ldb, int64_t ldc,
+                               int64_t ldd, int64_t strideA, int64_t strideB, int64_t strideC, int64_t strideD,
+                               float beta, uint32_t align_flags, int32_t num_sms, gemm_tn_plan_t* plan) {
+    if (!plan || num_sms <= 0) return GEMM_ERR_INVALID_VALUE;
+    Problem p = {M, N, K, batch, lda, ldb, ldc, ldd, strideA, strideB, strideC, strideD, beta, align_flags};
+    gemm_status_t st = validate(p);
+    if (st != GEMM_OK) return st;
+    Plan pl;
+    make_plan(p, num_sms, pl);
+    *plan = pl.pub;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value) {
+    switch (option) {
+        case GEMM_TN_OPT_WAIT_TIMEOUT_NS:
+            if (value < 1000000 || value > 60000000000ll) return GEMM_ERR_INVALID_VALUE;
+            g_opt_timeout_ns = value;
+            return GEMM_OK;
+        case GEMM_TN_OPT_SKIP_FIRST_LOAD: g_opt_skip_first_load = value ? 1 : 0; return GEMM_OK;
+        case GEMM_TN_OPT_FORCE_BN:
+            if (value != 0 && value != 128 && value != 256) return GEMM_ERR_INVALID_VALUE;
+            g_opt_force_bn = value;
+            return GEMM_OK;
+        case GEMM_TN_OPT_FORCE_PAIR:
+            if (value < 0 || value > 2) return GEMM_ERR_INVALID_VALUE;
+            g_opt_force_pair = value;
+            return GEMM_OK;
+        case GEMM_TN_OPT_FORCE_SPLITS:
+            if (value < 0 || value > 64) return GEMM_ERR_INVALID_VALUE;
+            g_opt_force_splits = value;
+            return GEMM_OK;
+        case GEMM_TN_OPT_FORCE_SWAP:
+            if (value < -1 || value > 1) return GEMM_ERR_INVALID_VALUE;
+            g_opt_force_swap = value;
+            return GEMM_OK;
+        case GEMM_TN_OPT_FORCE_GENERIC_EPI: g_opt_force_generic = value ? 1 : 0; return GEMM_OK;
+        case GEMM_TN_OPT_FORCE_PACK: g_opt_force_pack = value ? 1 : 0; return GEMM_OK;
+    }
+    return GEMM_ERR_INVALID_VALUE;
+}
+
+int64_t gemm_tn_f16_get_option(int32_t option) {
+    switch (option) {
+        case GEMM_TN_OPT_WAIT_TIMEOUT_NS: return g_opt_timeout_ns.load();
+        case GEMM_TN_OPT_SKIP_FIRST_LOAD: return g_opt_skip_first_load.load();
+        case GEMM_TN_OPT_FORCE_BN: return g_opt_force_bn.load();
+        case GEMM_TN_OPT_FORCE_PAIR: return g_opt_force_pair.load();
+        case GEMM_TN_OPT_FORCE_SPLITS: return g_opt_force_splits.load();
+        case GEMM_TN_OPT_FORCE_SWAP: return g_opt_force_swap.load();
+        case GEMM_TN_OPT_FORCE_GENERIC_EPI: return g_opt_force_generic.load();
+        case GEMM_TN_OPT_FORCE_PACK: return g_opt_force_pack.load();
+    }
+    return -1;
+}
+
+}  // extern "C"

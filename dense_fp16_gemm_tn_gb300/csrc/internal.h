@@ -1,0 +1,41 @@
+// Declarations shared between the host API and the kernel translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "kparams.h"
+
+namespace gtn {
+
+// One compiled tensor-core kernel variant.
+struct TcVariant {
+    int bn;      // MMA N (columns of the accumulator tile)
+    int pair;    // 1 = one CTA per 128-row tile, 2 = CTA pair per 256-row tile
+    int stages;  // shared-memory ring depth
+    int epi;     // EpiMode
+};
+
+// Looks up the compiled variant for (bn, pair, epi); returns false if none exists.
+bool find_tc_variant(int bn, int pair, int epi, TcVariant* out);
+
+// Launches a tensor-core variant with a persistent grid of at most `max_ctas`
+// CTAs (rounded to whole CTA pairs).  *grid_out receives the grid used.
+cudaError_t launch_tc_variant(const TcVariant& v, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const CUtensorMap& tmD, const KParams& p, int64_t max_ctas, cudaStream_t stream,
+                              int64_t* grid_out);
+
+// Largest number of CTAs of variant v that can be resident at once on the current device.
+int64_t tc_variant_capacity(const TcVariant& v, int sms);
+
+cudaError_t launch_repack(const void* src, int64_t ld_src, int64_t stride_src, void* dst, int64_t ldo, int64_t rows,
+                          int64_t K, int64_t batch, int sms, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float* W, int32_t splits, int64_t M, int64_t N, int64_t batch, float alpha,
+                                 float beta, const void* C, int64_t ldc, int64_t strideC, void* D, int64_t ldd,
+                                 int64_t strideD, int sms, cudaStream_t stream);
+cudaError_t launch_scale(int64_t M, int64_t N, int64_t batch, float beta, const void* C, int64_t ldc,
+                         int64_t strideC, void* D, int64_t ldd, int64_t strideD, int sms, cudaStream_t stream);
+
+}  // namespace gtn

@@ -1,0 +1,40 @@
+// Variants for small M: operands swapped so the tensor core computes D^T = B . A^T.
+#include "tc_launch.cuh"
+
+namespace gtn {
+
+bool launch_family_swap(const TcVariant& v, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
+                          const KParams& p, int64_t max_ctas, cudaStream_t stream, int64_t* grid_out,
+                          cudaError_t* err) {
+#define GTN_CASE(BN, PAIR, ST, EPI)                                                                    \
+    if (v.bn == BN && v.pair == PAIR && v.stages == ST && v.epi == EPI) {                             \
+        *err = TcLauncher<BN, PAIR, ST, EPI>::launch(tmA, tmB, tmD, p, max_ctas, stream, grid_out);   \
+        return true;                                                                                  \
+    }
+    GTN_CASE(16, 1, 8, EPI_SWAP)
+    GTN_CASE(32, 1, 8, EPI_SWAP)
+    GTN_CASE(64, 1, 8, EPI_SWAP)
+    GTN_CASE(16, 1, 8, EPI_PARTIAL_SWAP)
+    GTN_CASE(32, 1, 8, EPI_PARTIAL_SWAP)
+    GTN_CASE(64, 1, 8, EPI_PARTIAL_SWAP)
+#undef GTN_CASE
+    return false;
+}
+
+bool capacity_family_swap(const TcVariant& v, int sms, int64_t* cap) {
+#define GTN_CASE(BN, PAIR, ST, EPI)                                          \
+    if (v.bn == BN && v.pair == PAIR && v.stages == ST && v.epi == EPI) {   \
+        *cap = TcLauncher<BN, PAIR, ST, EPI>::capacity(sms);                \
+        return true;                                                        \
+    }
+    GTN_CASE(16, 1, 8, EPI_SWAP)
+    GTN_CASE(32, 1, 8, EPI_SWAP)
+    GTN_CASE(64, 1, 8, EPI_SWAP)
+    GTN_CASE(16, 1, 8, EPI_PARTIAL_SWAP)
+    GTN_CASE(32, 1, 8, EPI_PARTIAL_SWAP)
+    GTN_CASE(64, 1, 8, EPI_PARTIAL_SWAP)
+#undef GTN_CASE
+    return false;
+}
+
+}  // namespace gtn

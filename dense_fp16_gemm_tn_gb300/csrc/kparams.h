@@ -1,0 +1,38 @@
+// Parameters shared by the host launcher and the tensor-core GEMM kernel.
+#pragma once
+
+#include <cstdint>
+
+namespace gtn {
+
+enum EpiMode : int {
+    EPI_TMA = 0,           // D = alpha*acc via TMA stores (beta == 0, aligned D)
+    EPI_GENERIC = 1,       // D = alpha*acc + beta*C, predicated element stores
+    EPI_SWAP = 2,          // same, accumulator holds D^T (swapped operands)
+    EPI_PARTIAL = 3,       // fp32 partial sums of one K slice -> workspace
+    EPI_PARTIAL_SWAP = 4,  // same, accumulator holds D^T
+};
+
+struct KParams {
+    // Tensor-core view: the MMA's A operand has rows_a rows, its B operand rows_b rows.
+    int32_t rows_a, rows_b, K, batch;
+    int32_t tiles_m, tiles_n;  // tiles of (128*PAIR) x BN in that view
+    int32_t splits;            // K slices per tile
+    int32_t kb_total;          // number of 64-wide k-blocks, ceil(K/64)
+    int32_t group_m;           // rasterisation group size along the tile rows
+    int32_t zA, zB, zD;        // batch coordinate multipliers (0 = operand not batched)
+    int64_t num_units;
+    // Problem view, for the epilogue.
+    int32_t M, N;
+    float alpha, beta;
+    void* D;
+    int64_t ldd, strideD;
+    const void* C;
+    int64_t ldc, strideC;
+    float* W;  // split-K partials, [batch][splits][M][N] fp32
+    uint32_t* err;
+    uint64_t timeout_ns;
+    int32_t debug_skip_first_load;  // test hook: CTA 0 never issues its first load
+};
+
+}  // namespace gtn

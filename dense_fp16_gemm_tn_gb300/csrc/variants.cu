@@ -1,0 +1,62 @@
+// Table of the compiled tensor-core kernel variants and dispatch to the
+// translation unit that holds each one.
+#include "internal.h"
+
+namespace gtn {
+
+bool launch_family_tma(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KParams&,
+                       int64_t, cudaStream_t, int64_t*, cudaError_t*);
+bool launch_family_generic(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                           const KParams&, int64_t, cudaStream_t, int64_t*, cudaError_t*);
+bool launch_family_swap(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KParams&,
+                        int64_t, cudaStream_t, int64_t*, cudaError_t*);
+bool capacity_family_tma(const TcVariant&, int, int64_t*);
+bool capacity_family_generic(const TcVariant&, int, int64_t*);
+bool capacity_family_swap(const TcVariant&, int, int64_t*);
+
+static const TcVariant kVariants[] = {
+    {256, 1, 4, EPI_TMA},
+    {256, 2, 6, EPI_TMA},
+    {128, 1, 6, EPI_TMA},
+    {128, 2, 8, EPI_TMA},
+    {256, 1, 4, EPI_GENERIC},
+    {256, 2, 6, EPI_GENERIC},
+    {128, 1, 6, EPI_GENERIC},
+    {128, 1, 6, EPI_PARTIAL},
+    {16, 1, 8, EPI_SWAP},
+    {32, 1, 8, EPI_SWAP},
+    {64, 1, 8, EPI_SWAP},
+    {16, 1, 8, EPI_PARTIAL_SWAP},
+    {32, 1, 8, EPI_PARTIAL_SWAP},
+    {64, 1, 8, EPI_PARTIAL_SWAP},
+};
+
+bool find_tc_variant(int bn, int pair, int epi, TcVariant* out) {
+    for (const TcVariant& v : kVariants) {
+        if (v.bn == bn && v.pair == pair && v.epi == epi) {
+            if (out) *out = v;
+            return true;
+        }
+    }
+    return false;
+}
+
+cudaError_t launch_tc_variant(const TcVariant& v, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                              const CUtensorMap& tmD, const KParams& p, int64_t max_ctas, cudaStream_t stream,
+                              int64_t* grid_out) {
+    cudaError_t e = cudaErrorInvalidValue;
+    if (launch_family_tma(v, tmA, tmB, tmD, p, max_ctas, stream, grid_out, &e)) return e;
+    if (launch_family_generic(v, tmA, tmB, tmD, p, max_ctas, stream, grid_out, &e)) return e;
+    if (launch_family_swap(v, tmA, tmB, tmD, p, max_ctas, stream, grid_out, &e)) return e;
+    return cudaErrorInvalidValue;
+}
+
+int64_t tc_variant_capacity(const TcVariant& v, int sms) {
+    int64_t cap = 0;
+    if (capacity_family_tma(v, sms, &cap) || capacity_family_generic(v, sms, &cap) ||
+        capacity_family_swap(v, sms, &cap))
+        return cap;
+    return 0;
+}
+
+}  // namespace gtn

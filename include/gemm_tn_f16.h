@@ -1,0 +1,193 @@
+/*
+ * gemm_tn_f16 — half-precision TN GEMM for one NVIDIA GB300 (sm_103a) GPU.
+ *
+ *     D[m][n] = alpha * sum_k A[m][k] * B[n][k] + beta * C[m][n]
+ *
+ * The operation is the GEMM of the "CuTe C++ 简介01 / gemm_device 逐行解析"
+ * page: the TN inner product tCrC(m,n) += tCsA(m,k) * tCsB(n,k) and the
+ * axpby epilogue C = alpha*A*B + beta*C (section 1, kernel signature;
+ * section 3, appendix code), with A (M,K) and B (N,K) both K-contiguous and
+ * D (M,N) N-contiguous as in "cute(8) smem_gemm", section "代码实现"
+ * (make_stride(K, Int<1>) for A and B, make_stride(N, Int<1>) for D).
+ * The batched form is the attention-score contraction score = Q . K^T of the
+ * "为什么要用 retile_D" page (sections 1 and 3: Q is the A operand, K the B
+ * operand, head_dim 64), one GEMM per batch entry.
+ *
+ * Numerics: A, B, C, D are IEEE binary16.  Products are accumulated in fp32
+ * on the tensor cores (summation order unspecified); alpha*acc + beta*C is
+ * formed in fp32 and rounded once to binary16, round-to-nearest-even,
+ * subnormals kept, overflow to +-inf.
+ *
+ * Layout (all sizes and leading dimensions count ELEMENTS, not bytes):
+ *   A: M rows of K halves, row m at A + m*lda,   lda >= max(K,1)
+ *   B: N rows of K halves, row n at B + n*ldb,   ldb >= max(K,1)
+ *   C: M rows of N halves, row m at C + m*ldc,   ldc >= max(N,1)  (if beta != 0)
+ *   D: M rows of N halves, row m at D + m*ldd,   ldd >= max(N,1)
+ *   batched: entry b of X starts at X + b*strideX (strides >= 0; a stride of
+ *   0 broadcasts that operand; D's stride must keep entries disjoint).
+ *
+ * Ownership and memory: every pointer is DEVICE memory owned by the caller
+ * and must stay valid until the work queued on `stream` has finished.  The
+ * library keeps, per device, a small stream-ordered memory pool for its own
+ * scratch (split-K partial sums, repacked copies of operands whose leading
+ * dimension is not a multiple of 8); scratch is allocated and freed in stream
+ * order, so concurrent calls on different streams never share it.
+ * gemm_tn_f16_shutdown() returns the pool's memory.
+ *
+ * Alignment: every pointer must be 2-byte aligned.  Any leading dimension
+ * and any 2-byte-aligned address is accepted; 16-byte aligned pointers with
+ * leading dimensions (and batch strides) that are multiples of 8 take the
+ * direct tensor-memory-accelerator path, other operands are first repacked.
+ *
+ * Special cases: M == 0, N == 0 or batch == 0 does nothing and returns
+ * GEMM_OK.  K == 0 gives D = beta*C (D = 0 when beta == 0).  When beta == 0,
+ * C is never read and may be NULL (NaNs in C do not propagate).  D may alias
+ * C exactly (same pointer, ldc == ldd, same batch stride); any other overlap
+ * between D and A, B or C is undefined.
+ *
+ * Asynchrony and errors: calls enqueue work on `stream` and return without
+ * waiting.  The returned status covers argument checks and the launch.  No
+ * function ever exits or aborts the process.  Device-side waits are bounded:
+ * a kernel whose pipeline stalls past its limit records GEMM_ERR_TIMEOUT in a
+ * device error word and returns; read it with gemm_tn_f16_last_device_error().
+ */
+#ifndef GEMM_TN_F16_H
+#define GEMM_TN_F16_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define GEMM_TN_API __attribute__((visibility("default")))
+#else
+#define GEMM_TN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t is a pointer to this opaque type; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st* gemm_stream_t;
+
+typedef enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_VALUE = 1, /* bad size, leading dimension, stride or NULL pointer */
+    GEMM_ERR_MISALIGNED = 2,    /* a pointer is not 2-byte aligned */
+    GEMM_ERR_UNSUPPORTED = 3,   /* device is not sm_103 / sm_100 class, or sizes beyond limits */
+    GEMM_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (see gemm_tn_f16_last_cuda_error) */
+    GEMM_ERR_TIMEOUT = 5,       /* a device-side wait ran past its limit (device error word) */
+    GEMM_ERR_WORKSPACE = 6      /* scratch memory could not be obtained */
+} gemm_status_t;
+
+/*
+ * D = alpha * A . B^T + beta * C for one problem.
+ * A: const half[M][lda]; B: const half[N][ldb]; C: const half[M][ldc] or NULL
+ * when beta == 0; D: half[M][ldd].  Sizes must be >= 0 and M, N, K < 2^31.
+ * Returns GEMM_OK once the work is queued on `stream`.
+ */
+GEMM_TN_API gemm_status_t gemm_tn_f16(const void* A, int64_t lda,
+                          const void* B, int64_t ldb,
+                          const void* C, int64_t ldc,
+                          void* D, int64_t ldd,
+                          int64_t M, int64_t N, int64_t K,
+                          float alpha, float beta,
+                          gemm_stream_t stream);
+
+/*
+ * The same for `batch` independent problems of one shape:
+ *   D_b = alpha * A_b . B_b^T + beta * C_b,  X_b = X + b*strideX (elements).
+ * For the attention score S = Q . K^T: A = Q (seq_q x head_dim, lda = head_dim),
+ * B = K (seq_k x head_dim), D = S (seq_q x seq_k), batch = batch*heads.
+ */
+GEMM_TN_API gemm_status_t gemm_tn_f16_batched(const void* A, int64_t lda, int64_t strideA,
+                                  const void* B, int64_t ldb, int64_t strideB,
+                                  const void* C, int64_t ldc, int64_t strideC,
+                                  void* D, int64_t ldd, int64_t strideD,
+                                  int64_t M, int64_t N, int64_t K, int64_t batch,
+                                  float alpha, float beta,
+                                  gemm_stream_t stream);
+
+/* Static English text for a status code; never NULL. */
+GEMM_TN_API const char* gemm_status_string(gemm_status_t status);
+
+/*
+ * Synchronises the current device, then reads and clears the device error
+ * word that bounded device-side waits write.  GEMM_OK when no kernel of this
+ * library has reported a stall since the last call, GEMM_ERR_TIMEOUT if one
+ * has, GEMM_ERR_CUDA if the synchronisation itself failed.
+ */
+GEMM_TN_API gemm_status_t gemm_tn_f16_last_device_error(void);
+
+/* The CUDA error code (cudaError_t value) behind the last GEMM_ERR_CUDA of this thread. */
+GEMM_TN_API int gemm_tn_f16_last_cuda_error(void);
+
+/* Returns the library pool's memory to the driver for every device it was used on. */
+GEMM_TN_API void gemm_tn_f16_shutdown(void);
+
+/* Library version, major*10000 + minor*100 + patch. */
+GEMM_TN_API int gemm_tn_f16_version(void);
+
+/*
+ * Host-only planning (no CUDA call; safe without a GPU).  Describes the
+ * kernel the library would launch for a problem on a device with `num_sms`
+ * streaming multiprocessors.  `align_flags` bit i set means operand i
+ * (0=A, 1=B, 2=C, 3=D) has a 16-byte aligned base pointer.
+ */
+typedef struct {
+    int32_t kernel;          /* 0 none (empty problem), 1 scale-only (K == 0),
+                                2 tensor-core tile kernel, 3 split-K (+ reduction) */
+    int32_t tile_m;          /* output rows per tile as seen by the tensor core (128 or 256) */
+    int32_t tile_n;          /* output columns per tile as seen by the tensor core */
+    int32_t cta_pair;        /* 1: one CTA per tile; 2: CTA pair sharing one 256-row tile */
+    int32_t swap_ab;         /* 1: computes D^T = B . A^T (small M) */
+    int32_t splits;          /* K slices (1 = no split) */
+    int32_t stages;          /* shared-memory pipeline depth */
+    int32_t epi_tma;         /* 1: D written by tensor stores; 0: plain predicated stores */
+    int32_t pack_a;          /* 1: A is first repacked to an aligned scratch copy */
+    int32_t pack_b;          /* 1: B is first repacked */
+    int64_t units;           /* work units (tiles x splits x batch) */
+    int64_t grid;            /* CTAs launched */
+    int64_t workspace_bytes; /* scratch taken from the pool for this call */
+} gemm_tn_plan_t;
+
+GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int64_t batch,
+                               int64_t lda, int64_t ldb, int64_t ldc, int64_t ldd,
+                               int64_t strideA, int64_t strideB, int64_t strideC, int64_t strideD,
+                               float beta, uint32_t align_flags, int32_t num_sms,
+                               gemm_tn_plan_t* plan);
+
+/*
+ * Process-wide tuning and test options (host only; take effect on the next call).
+ *   GEMM_TN_OPT_WAIT_TIMEOUT_NS   limit of every device-side wait, in ns (default 2e9).
+ *   GEMM_TN_OPT_SKIP_FIRST_LOAD   1: CTA 0 of each tensor-core launch skips its first operand
+ *                                 load, so its MMA wait runs out and the kernel reports
+ *                                 GEMM_ERR_TIMEOUT -- exercises the stall path without any
+ *                                 fault.  Testing only; 0 restores normal operation.
+ *   GEMM_TN_OPT_FORCE_BN          force the accumulator tile width (16..256), 0 = automatic.
+ *   GEMM_TN_OPT_FORCE_PAIR        force 1 (single CTA) or 2 (CTA pair), 0 = automatic.
+ *   GEMM_TN_OPT_FORCE_SPLITS      force the number of K slices, 0 = automatic.
+ *   GEMM_TN_OPT_FORCE_SWAP        force operand swapping off (-1) or on (1), 0 = automatic.
+ *   GEMM_TN_OPT_FORCE_GENERIC_EPI 1: never use the TMA-store epilogue.
+ *   GEMM_TN_OPT_FORCE_PACK        1: repack A and B through scratch even when aligned.
+ * A forced setting that no compiled kernel supports for a problem is ignored.
+ * Returns GEMM_ERR_INVALID_VALUE for an unknown option or an out-of-range value.
+ */
+enum {
+    GEMM_TN_OPT_WAIT_TIMEOUT_NS = 1,
+    GEMM_TN_OPT_SKIP_FIRST_LOAD = 2,
+    GEMM_TN_OPT_FORCE_BN = 3,
+    GEMM_TN_OPT_FORCE_PAIR = 4,
+    GEMM_TN_OPT_FORCE_SPLITS = 5,
+    GEMM_TN_OPT_FORCE_SWAP = 6,
+    GEMM_TN_OPT_FORCE_GENERIC_EPI = 7,
+    GEMM_TN_OPT_FORCE_PACK = 8
+};
+GEMM_TN_API gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value);
+GEMM_TN_API int64_t gemm_tn_f16_get_option(int32_t option);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GEMM_TN_F16_H */

@@ -1,0 +1,161 @@
+"""The C-ABI library without a GPU: it loads, exports every function the
+header declares, and its host-only logic (argument checks, planning, options)
+behaves as documented.  No compute call is made here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import dense_fp16_gemm_tn_gb300 as G
+from dense_fp16_gemm_tn_gb300 import build as B
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gemm_tn_f16.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"GEMM_TN_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+def test_library_builds_and_loads():
+    G.load_library()
+    assert os.path.exists(G.library_path())
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(G.library_path())
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(G.EXPORTED)
+    out = subprocess.run(["nm", "-D", "--defined-only", G.library_path()], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported == set(names), exported ^ set(names)
+
+
+def test_built_for_sm103a_only():
+    assert B.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings_and_version():
+    for s in range(7):
+        assert G.gemm_status_string(s)
+    assert "unknown" in G.gemm_status_string(99)
+    assert G.gemm_tn_f16_version() >= 10000
+
+
+@pytest.mark.parametrize("args", [
+    dict(M=-1, N=8, K=8, lda=8, ldb=8, ldd=8),
+    dict(M=8, N=8, K=8, lda=7, ldb=8, ldd=8),     # lda < K
+    dict(M=8, N=8, K=8, lda=8, ldb=7, ldd=8),     # ldb < K
+    dict(M=8, N=8, K=8, lda=8, ldb=8, ldd=7),     # ldd < N
+])
+def test_invalid_sizes_rejected_before_any_cuda_call(args):
+    a = dict(A=0x1000, B=0x2000, C=None, ldc=8, D=0x3000, alpha=1.0, beta=0.0)
+    a.update(args)
+    st = G.gemm_tn_f16(a["A"], a["lda"], a["B"], a["ldb"], a["C"], a["ldc"], a["D"], a["ldd"],
+                       a["M"], a["N"], a["K"], a["alpha"], a["beta"], check=False)
+    assert st == G.GEMM_ERR_INVALID_VALUE
+
+
+def test_null_and_misaligned_pointers_rejected():
+    assert G.gemm_tn_f16(None, 8, 0x2000, 8, None, 8, 0x3000, 8, 8, 8, 8, 1.0, 0.0, check=False) == \
+        G.GEMM_ERR_INVALID_VALUE
+    assert G.gemm_tn_f16(0x1000, 8, 0x2000, 8, None, 8, 0x3000, 8, 8, 8, 8, 1.0, 1.0, check=False) == \
+        G.GEMM_ERR_INVALID_VALUE  # beta != 0 needs C
+    assert G.gemm_tn_f16(0x1001, 8, 0x2000, 8, None, 8, 0x3000, 8, 8, 8, 8, 1.0, 0.0, check=False) == \
+        G.GEMM_ERR_MISALIGNED
+    # D overlapping A, and C overlapping D without being identical
+    assert G.gemm_tn_f16(0x1000, 8, 0x2000, 8, None, 8, 0x1010, 8, 8, 8, 8, 1.0, 0.0, check=False) == \
+        G.GEMM_ERR_INVALID_VALUE
+    assert G.gemm_tn_f16(0x1000, 8, 0x2000, 8, 0x3010, 8, 0x3000, 8, 8, 8, 8, 1.0, 1.0, check=False) == \
+        G.GEMM_ERR_INVALID_VALUE
+    assert G.gemm_tn_f16(0x1000, 8, 0x2000, 8, 0x3000, 16, 0x3000, 8, 8, 8, 8, 1.0, 1.0, check=False) == \
+        G.GEMM_ERR_INVALID_VALUE  # C == D but different leading dimensions
+
+
+def test_batched_output_entries_must_be_disjoint():
+    st = G.gemm_tn_f16_batched(0x100000, 8, 64, 0x200000, 8, 64, None, 8, 0, 0x300000, 8, 32,
+                               8, 8, 8, 2, 1.0, 0.0, check=False)
+    assert st == G.GEMM_ERR_INVALID_VALUE
+    st = G.gemm_tn_f16_batched(0x100000, 8, -64, 0x200000, 8, 64, None, 8, 0, 0x300000, 8, 64,
+                               8, 8, 8, 2, 1.0, 0.0, check=False)
+    assert st == G.GEMM_ERR_INVALID_VALUE
+
+
+def test_empty_problems_are_no_ops_without_touching_cuda():
+    assert G.gemm_tn_f16(None, 1, None, 1, None, 1, None, 1, 0, 5, 5, 1.0, 0.0, check=False) == G.GEMM_OK
+    assert G.gemm_tn_f16_batched(None, 1, 0, None, 1, 0, None, 1, 0, None, 1, 0, 4, 4, 4, 0, 1.0, 0.0,
+                                 check=False) == G.GEMM_OK
+
+
+def test_sizes_beyond_int32_unsupported():
+    st = G.gemm_tn_f16(0x1000, 1 << 31, 0x2000, 1 << 31, None, 8, 0x3000, 8, 8, 8, 1 << 31, 1.0, 0.0, check=False)
+    assert st == G.GEMM_ERR_UNSUPPORTED
+
+
+def plan(M, N, K, batch=1, lda=None, ldb=None, ldc=None, ldd=None, sA=0, sB=0, sC=0, sD=0, beta=0.0,
+         align=15, sms=148):
+    return G.gemm_tn_f16_plan(M, N, K, batch, lda or K, ldb or K, ldc or N, ldd or N, sA, sB, sC, sD,
+                              beta, align, sms)
+
+
+def test_plan_large_square_uses_cta_pairs_and_tma_store():
+    p = plan(8192, 8192, 8192)
+    assert p["kernel"] == 2 and p["cta_pair"] == 2 and p["tile_m"] == 256 and p["tile_n"] == 256
+    assert p["epi_tma"] == 1 and p["splits"] == 1 and p["pack_a"] == 0 and p["pack_b"] == 0
+    assert p["units"] == 32 * 32 and p["grid"] == 148
+    assert p["workspace_bytes"] == 0
+
+
+def test_plan_skinny_m_swaps_and_splits_k():
+    p = plan(16, 8192, 8192)
+    assert p["kernel"] == 3 and p["swap_ab"] == 1 and p["tile_n"] == 16 and p["splits"] >= 2
+    assert p["units"] == 64 * p["splits"]
+    assert p["workspace_bytes"] >= p["splits"] * 16 * 8192 * 4
+
+
+def test_plan_ragged_packed_ld_repacks_operands():
+    p = plan(4095, 3073, 2047, lda=2047, ldb=2047, ldc=3073, ldd=3073, beta=1.5)
+    assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["epi_tma"] == 0
+    assert p["workspace_bytes"] >= 2 * (4095 + 3073) * 2048
+
+
+def test_plan_score_batched_short_k():
+    p = plan(4096, 4096, 64, batch=128, sA=4096 * 64, sB=4096 * 64, sD=4096 * 4096)
+    assert p["kernel"] == 2 and p["cta_pair"] == 1 and p["tile_n"] == 256 and p["epi_tma"] == 1
+    assert p["units"] == 32 * 16 * 128
+
+
+def test_plan_misaligned_pointer_forces_pack_and_generic_epilogue():
+    p = plan(1024, 1024, 1024, align=0)
+    assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["epi_tma"] == 0
+
+
+def test_plan_k_zero_and_empty():
+    assert plan(8, 8, 0)["kernel"] == 1
+    assert plan(0, 8, 8)["kernel"] == 0
+
+
+def test_plan_splits_cover_k():
+    for K in (512, 1000, 4096, 65536):
+        p = plan(16, 1024, K)
+        assert 1 <= p["splits"] <= max(1, (K + 63) // 64)
+
+
+def test_options_roundtrip_and_validation():
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 128)
+    assert G.gemm_tn_f16_get_option(G.GEMM_TN_OPT_FORCE_BN) == 128
+    p = plan(8192, 8192, 8192)
+    assert p["tile_n"] == 128
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 0)
+    assert plan(8192, 8192, 8192)["tile_n"] == 256
+    with pytest.raises(G.GemmError):
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 100)
+    with pytest.raises(G.GemmError):
+        G.gemm_tn_f16_set_option(12345, 1)
+    with pytest.raises(G.GemmError):
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_WAIT_TIMEOUT_NS, 10)
