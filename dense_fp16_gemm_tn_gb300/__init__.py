@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     GEMM_TN_OPT_FORCE_SWAP,
     GEMM_TN_OPT_SKIP_FIRST_LOAD,
     GEMM_TN_OPT_WAIT_TIMEOUT_NS,
+    GEMM_TN_STATIC_SCRATCH_BYTES,
     GemmError,
     gemm_status_string,
     gemm_tn_f16,
@@ -33,6 +34,7 @@ from ._binding import (  # noqa: F401
     gemm_tn_f16_plan,
     gemm_tn_f16_set_option,
     gemm_tn_f16_shutdown,
+    gemm_tn_f16_splitk_static,
     gemm_tn_f16_version,
     library_path,
     load_library,

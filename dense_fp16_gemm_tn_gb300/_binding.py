@@ -35,7 +35,9 @@ GEMM_TN_OPT_FORCE_PACK = 8
 
 EXPORTED = ["gemm_tn_f16", "gemm_tn_f16_batched", "gemm_status_string", "gemm_tn_f16_last_device_error",
             "gemm_tn_f16_last_cuda_error", "gemm_tn_f16_shutdown", "gemm_tn_f16_version", "gemm_tn_f16_plan",
-            "gemm_tn_f16_set_option", "gemm_tn_f16_get_option"]
+            "gemm_tn_f16_set_option", "gemm_tn_f16_get_option", "gemm_tn_f16_splitk_static"]
+
+GEMM_TN_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class GemmError(RuntimeError):
@@ -98,6 +100,9 @@ def load_library(build_if_missing: bool = True):
         lib.gemm_tn_f16_set_option.restype = ctypes.c_int
         lib.gemm_tn_f16_get_option.argtypes = [ctypes.c_int32]
         lib.gemm_tn_f16_get_option.restype = ctypes.c_int64
+        lib.gemm_tn_f16_splitk_static.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, f32, f32,
+                                                  ctypes.c_int32, vp]
+        lib.gemm_tn_f16_splitk_static.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -136,6 +141,14 @@ def gemm_tn_f16_batched(A, lda, strideA, B, ldb, strideB, C, ldc, strideC, D, ld
                                             _ptr(D), ldd, strideD, M, N, K, batch, float(alpha), float(beta),
                                             _stream(stream))
     return _check(st, "gemm_tn_f16_batched", check)
+
+
+def gemm_tn_f16_splitk_static(A, lda, B, ldb, C, ldc, D, ldd, M, N, K, alpha, beta, splits=0, stream=None, *,
+                              check=True):
+    """Split-K GEMM whose scratch is a fixed array inside the library: allocates nothing."""
+    st = load_library().gemm_tn_f16_splitk_static(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _ptr(D), ldd, M, N, K,
+                                                  float(alpha), float(beta), int(splits), _stream(stream))
+    return _check(st, "gemm_tn_f16_splitk_static", check)
 
 
 def gemm_status_string(status: int) -> str:

@@ -25,6 +25,14 @@ namespace gtn {
 // Device error word written by timed-out waits (see tc_gemm.cuh).
 __device__ uint32_t g_error_word = 0;
 
+// Device address of the error word on the current device (no allocation).
+cudaError_t error_word_address(uint32_t** out) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_error_word);
+    if (e == cudaSuccess) *out = static_cast<uint32_t*>(p);
+    return e;
+}
+
 namespace {
 
 thread_local int t_last_cuda_error = 0;

@@ -30,6 +30,9 @@ cudaError_t launch_tc_variant(const TcVariant& v, const CUtensorMap& tmA, const 
 // Largest number of CTAs of variant v that can be resident at once on the current device.
 int64_t tc_variant_capacity(const TcVariant& v, int sms);
 
+// Device address of the library's error word on the current device.
+cudaError_t error_word_address(uint32_t** out);
+
 cudaError_t launch_repack(const void* src, int64_t ld_src, int64_t stride_src, void* dst, int64_t ldo, int64_t rows,
                           int64_t K, int64_t batch, int sms, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float* W, int32_t splits, int64_t M, int64_t N, int64_t batch, float alpha,

@@ -186,6 +186,42 @@ enum {
 GEMM_TN_API gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value);
 GEMM_TN_API int64_t gemm_tn_f16_get_option(int32_t option);
 
+/*
+ * Split-K GEMM that allocates nothing.  (The pages have no counterpart: this is
+ * a service of the library, not a step of the method.)
+ *
+ * Same operation, arguments and rules as gemm_tn_f16, plus `splits` (number of
+ * K slices, 0 = automatic), computed by the split-K tensor-core kernel and its
+ * reduction with the fp32 partial sums held in one device array built into the
+ * library (GEMM_TN_STATIC_SCRATCH_BYTES per GPU that loads the library, kept
+ * until the process exits).  It never calls cudaMalloc, cudaFree or any other
+ * allocating routine.  It is meant for callers that must not allocate device
+ * memory when they call the GEMM: an allocator or memory pool calling from its
+ * own internals (re-entering cudaMalloc there can deadlock), or a service whose
+ * device-memory budget is fixed at start-up and whose request path may not
+ * allocate (cudaMalloc can synchronise the device and has no latency bound).
+ *
+ * Limits: splits*M*N*4 bytes must fit in GEMM_TN_STATIC_SCRATCH_BYTES (else
+ * GEMM_ERR_WORKSPACE, nothing launched); A and B must be 16-byte aligned with
+ * lda and ldb multiples of 8, since there is no scratch for a repacked copy
+ * (else GEMM_ERR_MISALIGNED).
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls on a device share the one array and leave
+ * their partial sums in it: calls whose work can overlap on the GPU (for
+ * example on two streams with no ordering between them) race and give wrong
+ * results.  Nothing in the array needs to start at zero.
+ */
+#define GEMM_TN_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+GEMM_TN_API gemm_status_t gemm_tn_f16_splitk_static(const void* A, int64_t lda,
+                                                    const void* B, int64_t ldb,
+                                                    const void* C, int64_t ldc,
+                                                    void* D, int64_t ldd,
+                                                    int64_t M, int64_t N, int64_t K,
+                                                    float alpha, float beta, int32_t splits,
+                                                    gemm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
