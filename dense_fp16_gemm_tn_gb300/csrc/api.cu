@@ -62,6 +62,7 @@ struct DeviceState {
     int major = 0, minor = 0;
     uint32_t* err = nullptr;
     cudaMemPool_t pool = nullptr;
+    int64_t capacity[kMaxVariants];  // resident CTAs per variant, 0 = not queried yet
 };
 
 constexpr int kMaxDevices = 64;
@@ -91,6 +92,7 @@ gemm_status_t device_state(DeviceState** out) {
         uint64_t keep = UINT64_MAX;  // keep freed scratch cached in the pool
         if ((e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep)) != cudaSuccess)
             return cuda_fail(e);
+        for (int64_t& c : d.capacity) c = 0;
         d.ready = true;
     }
     *out = &d;
@@ -117,10 +119,46 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
+// A few recently encoded maps per host thread: steady-state callers that reuse
+// the same buffers skip the driver call (a map depends only on these fields).
+struct MapCacheEntry {
+    const void* base;
+    int64_t inner, rows, batch, ld, stride;
+    bool batched;
+    uint32_t box_inner, box_rows;
+    uint64_t stamp;
+    CUtensorMap map;
+};
+constexpr int kMapCache = 16;
+thread_local MapCacheEntry t_map_cache[kMapCache] = {};
+thread_local uint64_t t_map_clock = 0;
+
+bool encode_map_uncached(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t batch, int64_t ld,
+                         int64_t stride, bool batched, uint32_t box_inner, uint32_t box_rows);
+
 // 3-D fp16 tensor map over (inner, rows, batch) with a box of (box_inner, box_rows, 1)
 // and 128-byte swizzle.  `batched` false maps a single matrix (batch extent 1).
 bool encode_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t batch, int64_t ld,
                 int64_t stride, bool batched, uint32_t box_inner, uint32_t box_rows) {
+    const uint64_t now = ++t_map_clock;
+    int victim = 0;
+    for (int i = 0; i < kMapCache; ++i) {
+        MapCacheEntry& e = t_map_cache[i];
+        if (e.stamp != 0 && e.base == base && e.inner == inner && e.rows == rows && e.batch == batch && e.ld == ld &&
+            e.stride == stride && e.batched == batched && e.box_inner == box_inner && e.box_rows == box_rows) {
+            e.stamp = now;
+            *map = e.map;
+            return true;
+        }
+        if (e.stamp < t_map_cache[victim].stamp) victim = i;
+    }
+    if (!encode_map_uncached(map, base, inner, rows, batch, ld, stride, batched, box_inner, box_rows)) return false;
+    t_map_cache[victim] = {base, inner, rows, batch, ld, stride, batched, box_inner, box_rows, now, *map};
+    return true;
+}
+
+bool encode_map_uncached(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t batch, int64_t ld,
+                         int64_t stride, bool batched, uint32_t box_inner, uint32_t box_rows) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn) return false;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows),
@@ -432,9 +470,14 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     kp.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
     kp.debug_skip_first_load = g_opt_skip_first_load.load() != 0 ? 1 : 0;
 
-    const int64_t cap = tc_variant_capacity(pl.var, dev->sms);
+    int64_t cap = dev->capacity[pl.var.index];
+    if (cap == 0) {
+        cap = tc_variant_capacity(pl.var, dev->sms);
+        if (cap <= 0) cap = dev->sms;
+        dev->capacity[pl.var.index] = cap;
+    }
     int64_t grid = 0;
-    e = launch_tc_variant(pl.var, mapA_op, mapB_op, mapD, kp, cap > 0 ? cap : dev->sms, stream, &grid);
+    e = launch_tc_variant(pl.var, mapA_op, mapB_op, mapD, kp, cap, stream, &grid);
     if (e != cudaSuccess) { release(); return cuda_fail(e); }
     if (pl.pub.splits > 1) {
         e = launch_splitk_reduce(kp.W, pl.pub.splits, p.M, p.N, p.batch, alpha, p.beta, C, p.ldc, p.sC, D, p.ldd,

@@ -16,7 +16,10 @@ struct TcVariant {
     int pair;    // 1 = one CTA per 128-row tile, 2 = CTA pair per 256-row tile
     int stages;  // shared-memory ring depth
     int epi;     // EpiMode
+    int index;   // position in the variant table (for per-device caches)
 };
+
+constexpr int kMaxVariants = 32;
 
 // Looks up the compiled variant for (bn, pair, epi); returns false if none exists.
 bool find_tc_variant(int bn, int pair, int epi, TcVariant* out);

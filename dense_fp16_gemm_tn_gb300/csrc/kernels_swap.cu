@@ -11,12 +11,12 @@ bool launch_family_swap(const TcVariant& v, const CUtensorMap& tmA, const CUtens
         *err = TcLauncher<BN, PAIR, ST, EPI>::launch(tmA, tmB, tmD, p, max_ctas, stream, grid_out);   \
         return true;                                                                                  \
     }
-    GTN_CASE(16, 1, 8, EPI_SWAP)
-    GTN_CASE(32, 1, 8, EPI_SWAP)
-    GTN_CASE(64, 1, 8, EPI_SWAP)
-    GTN_CASE(16, 1, 8, EPI_PARTIAL_SWAP)
-    GTN_CASE(32, 1, 8, EPI_PARTIAL_SWAP)
-    GTN_CASE(64, 1, 8, EPI_PARTIAL_SWAP)
+    GTN_CASE(16, 1, 12, EPI_SWAP)
+    GTN_CASE(32, 1, 11, EPI_SWAP)
+    GTN_CASE(64, 1, 9, EPI_SWAP)
+    GTN_CASE(16, 1, 12, EPI_PARTIAL_SWAP)
+    GTN_CASE(32, 1, 11, EPI_PARTIAL_SWAP)
+    GTN_CASE(64, 1, 9, EPI_PARTIAL_SWAP)
 #undef GTN_CASE
     return false;
 }
@@ -27,12 +27,12 @@ bool capacity_family_swap(const TcVariant& v, int sms, int64_t* cap) {
         *cap = TcLauncher<BN, PAIR, ST, EPI>::capacity(sms);                \
         return true;                                                        \
     }
-    GTN_CASE(16, 1, 8, EPI_SWAP)
-    GTN_CASE(32, 1, 8, EPI_SWAP)
-    GTN_CASE(64, 1, 8, EPI_SWAP)
-    GTN_CASE(16, 1, 8, EPI_PARTIAL_SWAP)
-    GTN_CASE(32, 1, 8, EPI_PARTIAL_SWAP)
-    GTN_CASE(64, 1, 8, EPI_PARTIAL_SWAP)
+    GTN_CASE(16, 1, 12, EPI_SWAP)
+    GTN_CASE(32, 1, 11, EPI_SWAP)
+    GTN_CASE(64, 1, 9, EPI_SWAP)
+    GTN_CASE(16, 1, 12, EPI_PARTIAL_SWAP)
+    GTN_CASE(32, 1, 11, EPI_PARTIAL_SWAP)
+    GTN_CASE(64, 1, 9, EPI_PARTIAL_SWAP)
 #undef GTN_CASE
     return false;
 }

@@ -273,17 +273,32 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t chunk_count = 0;
+        const bool use_c = (EPI == EPI_GENERIC || EPI == EPI_SWAP) && p.beta != 0.0f;
         for (int64_t u = cluster_id; u < p.num_units; u += nclusters) {
             const Unit w = decode_unit(p, u);
+            // First accumulator row / column of this warp, in the tensor-core view.
+            const int64_t arow0 = static_cast<int64_t>(w.tm) * (Cfg::BM * PAIR) + Cfg::BM * rank + quarter * 32;
+            const int64_t acol0 = static_cast<int64_t>(w.tn) * BN;
+            // Predicated epilogue: C of the first 32-column chunk is fetched before the
+            // accumulator is ready, so its memory latency overlaps the main loop.
+            __half cnext[32];
+            auto load_c_chunk = [&](int c, __half (&dst)[32]) {
+                const int64_t col = acol0 + c * 32 + lane;
+                const bool col_ok = col < p.N;
+                const __half* src = static_cast<const __half*>(p.C) + static_cast<int64_t>(w.b) * p.strideC + col;
+#pragma unroll
+                for (int r = 0; r < 32; ++r)
+                    dst[r] = (col_ok && arow0 + r < p.M) ? src[(arow0 + r) * p.ldc] : __ushort_as_half(0);
+            };
+            if constexpr (EPI == EPI_GENERIC) {
+                if (use_c) load_c_chunk(0, cnext);
+            }
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, p.err, p.timeout_ns, abort_flag, 5) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-            // First accumulator row of this warp, in the tensor-core view.
-            const int64_t arow0 = static_cast<int64_t>(w.tm) * (Cfg::BM * PAIR) + Cfg::BM * rank + quarter * 32;
-            const int64_t acol0 = static_cast<int64_t>(w.tn) * BN;
 
             if constexpr (EPI == EPI_TMA) {
 #pragma unroll 1
@@ -324,11 +339,22 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     ++chunk_count;
                 }
             } else if constexpr (EPI == EPI_GENERIC || EPI == EPI_PARTIAL) {
+                // Transpose each 32x32 block through padded shared memory so that a warp
+                // reads C and writes D along rows (coalesced), whatever the alignment.
                 float* T = reinterpret_cast<float*>(ebuf);
                 __half* Dp = static_cast<__half*>(p.D);
-                const __half* Cp = static_cast<const __half*>(p.C);
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
+                    __half ccur[32];
+                    if constexpr (EPI == EPI_GENERIC) {
+                        if (use_c) {
+#pragma unroll
+                            for (int r = 0; r < 32; ++r) ccur[r] = cnext[r];
+                            // Loads for the next chunk are issued before this chunk's stores
+                            // (different columns, so an aliased C == D stays correct).
+                            if (c + 1 < BN / 32) load_c_chunk(c + 1, cnext);
+                        }
+                    }
                     uint32_t v[32];
                     tmem_ld_32x32b_x32(t_row + c * 32, v);
                     tmem_ld_wait();
@@ -338,15 +364,14 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const int64_t col = acol0 + c * 32 + lane;
                     if (col < p.N) {
                         if constexpr (EPI == EPI_GENERIC) {
-                            const int64_t dbase = static_cast<int64_t>(w.b) * p.strideD + col;
-                            const int64_t cbase = static_cast<int64_t>(w.b) * p.strideC + col;
-#pragma unroll 8
+                            __half* dst = Dp + static_cast<int64_t>(w.b) * p.strideD + col;
+#pragma unroll
                             for (int r = 0; r < 32; ++r) {
                                 const int64_t row = arow0 + r;
                                 if (row < p.M) {
                                     float x = p.alpha * T[r * 33 + lane];
-                                    if (p.beta != 0.0f) x = fmaf(p.beta, __half2float(Cp[cbase + row * p.ldc]), x);
-                                    Dp[dbase + row * p.ldd] = __float2half_rn(x);
+                                    if (use_c) x = fmaf(p.beta, __half2float(ccur[r]), x);
+                                    dst[row * p.ldd] = __float2half_rn(x);
                                 }
                             }
                         } else {
@@ -371,19 +396,32 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     tmem_ld_32x32b_x16(t_row + c * 16, v);
                     tmem_ld_wait();
                     if (n < p.N) {
+                        if constexpr (EPI == EPI_SWAP) {
+                            // all C loads of the chunk first, then the stores
+                            __half cv[16];
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int64_t m = acol0 + c * 16 + j;
-                            if (m < p.M) {
-                                const float a = __uint_as_float(v[j]);
-                                if constexpr (EPI == EPI_SWAP) {
-                                    float x = p.alpha * a;
-                                    if (p.beta != 0.0f)
-                                        x = fmaf(p.beta, __half2float(Cp[static_cast<int64_t>(w.b) * p.strideC + m * p.ldc + n]), x);
+                            for (int j = 0; j < 16; ++j) {
+                                const int64_t m = acol0 + c * 16 + j;
+                                cv[j] = (use_c && m < p.M)
+                                            ? Cp[static_cast<int64_t>(w.b) * p.strideC + m * p.ldc + n]
+                                            : __ushort_as_half(0);
+                            }
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int64_t m = acol0 + c * 16 + j;
+                                if (m < p.M) {
+                                    float x = p.alpha * __uint_as_float(v[j]);
+                                    if (use_c) x = fmaf(p.beta, __half2float(cv[j]), x);
                                     Dp[static_cast<int64_t>(w.b) * p.strideD + m * p.ldd + n] = __float2half_rn(x);
-                                } else {
-                                    p.W[((static_cast<int64_t>(w.b) * p.splits + w.split) * p.M + m) * p.N + n] = a;
                                 }
+                            }
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int64_t m = acol0 + c * 16 + j;
+                                if (m < p.M)
+                                    p.W[((static_cast<int64_t>(w.b) * p.splits + w.split) * p.M + m) * p.N + n] =
+                                        __uint_as_float(v[j]);
                             }
                         }
                     }
