@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     GEMM_TN_OPT_FORCE_SPLITS,
     GEMM_TN_OPT_FORCE_SWAP,
     GEMM_TN_OPT_SKIP_FIRST_LOAD,
+    GEMM_TN_OPT_STREAM_K,
     GEMM_TN_OPT_WAIT_TIMEOUT_NS,
     GEMM_TN_STATIC_SCRATCH_BYTES,
     GemmError,

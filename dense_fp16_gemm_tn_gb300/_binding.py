@@ -32,6 +32,7 @@ GEMM_TN_OPT_FORCE_SPLITS = 5
 GEMM_TN_OPT_FORCE_SWAP = 6
 GEMM_TN_OPT_FORCE_GENERIC_EPI = 7
 GEMM_TN_OPT_FORCE_PACK = 8
+GEMM_TN_OPT_STREAM_K = 9
 
 EXPORTED = ["gemm_tn_f16", "gemm_tn_f16_batched", "gemm_status_string", "gemm_tn_f16_last_device_error",
             "gemm_tn_f16_last_cuda_error", "gemm_tn_f16_shutdown", "gemm_tn_f16_version", "gemm_tn_f16_plan",
@@ -51,7 +52,8 @@ class gemm_tn_plan_t(ctypes.Structure):
                 ("cta_pair", ctypes.c_int32), ("swap_ab", ctypes.c_int32), ("splits", ctypes.c_int32),
                 ("stages", ctypes.c_int32), ("epi_tma", ctypes.c_int32), ("pack_a", ctypes.c_int32),
                 ("pack_b", ctypes.c_int32), ("units", ctypes.c_int64), ("grid", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("stream_k", ctypes.c_int32), ("sk_maxc", ctypes.c_int32),
+                ("dp_tiles", ctypes.c_int64), ("sk_tiles", ctypes.c_int64)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

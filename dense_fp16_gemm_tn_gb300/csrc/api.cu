@@ -45,6 +45,7 @@ std::atomic<int64_t> g_opt_force_splits{0};
 std::atomic<int64_t> g_opt_force_swap{0};
 std::atomic<int64_t> g_opt_force_generic{0};
 std::atomic<int64_t> g_opt_force_pack{0};
+std::atomic<int64_t> g_opt_stream_k{0};
 
 gemm_status_t cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -191,6 +192,8 @@ struct Plan {
     int64_t tiles_m, tiles_n;
     int64_t ldo_a, ldo_b;        // leading dims of the packed copies
     int64_t pack_a_bytes, pack_b_bytes, partial_bytes;
+    int64_t sk_w_bytes, sk_ctr_bytes;  // stream-K partial slots and arrival counters
+    int64_t sk_iters;
     int group_m;
 };
 
@@ -211,6 +214,58 @@ gemm_status_t validate(const Problem& p) {
         if (p.sD < (p.M - 1) * p.ldd + p.N) return GEMM_ERR_INVALID_VALUE;  // output entries must be disjoint
     }
     return GEMM_OK;
+}
+
+// Stream-K split of the tiles over `groups` CTA groups (host arithmetic only).
+// The tiles that fill whole waves run data-parallel; when the last wave would
+// leave groups idle, its tiles' k-blocks are spread over every group instead.
+void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
+    gemm_tn_plan_t& pub = pl.pub;
+    const int pair = pub.cta_pair;
+    const int64_t tiles = pl.tiles_m * pl.tiles_n * pr.batch;
+    const int64_t kb = ceil_div(pr.K, 64);
+    const int64_t G = std::max<int64_t>(groups, 1);
+    pub.stream_k = 0;
+    pub.sk_maxc = 0;
+    pub.dp_tiles = tiles;
+    pub.sk_tiles = 0;
+    pl.sk_iters = 0;
+    pl.sk_w_bytes = pl.sk_ctr_bytes = 0;
+    const bool sk_epi = pl.epi == EPI_TMA || pl.epi == EPI_GENERIC || pl.epi == EPI_SWAP;
+    // Automatic stream-K when whole tiles would leave much of the machine idle.  At
+    // full occupancy the GEMM runs at the power limit, so a partly empty last wave
+    // costs less than its share; with the TMA epilogue the fixup is cheap enough
+    // to pay from 10% idle, with the predicated one only from 40%.  Forced on, it
+    // applies whenever the tiles do not divide evenly.
+    const int64_t mode = g_opt_stream_k.load();
+    const double threshold = mode > 0 ? 1.0 : (pl.epi == EPI_TMA ? 0.9 : 0.6);
+    if (mode >= 0 && sk_epi && pub.splits == 1 && kb >= 8 && tiles % G != 0) {
+        const double dp_eff = static_cast<double>(tiles) / static_cast<double>(ceil_div(tiles, G) * G);
+        // Every group must get at least one iteration (contributors to a tile are
+        // then consecutive groups); with no whole wave, launch fewer groups instead.
+        int64_t Gs = G;
+        if (tiles < G) Gs = std::min(G, tiles * kb);
+        const int64_t dp = (tiles / Gs) * Gs;
+        const int64_t sk = tiles - dp;
+        const int64_t I = sk * kb;
+        TcVariant skv;
+        if (dp_eff < threshold && I >= Gs && find_tc_variant(pl.var.bn, pl.var.pair, pl.epi, 1, &skv)) {
+            auto owner = [&](int64_t i) { return ((i + 1) * Gs - 1) / I; };
+            int64_t maxc = 1;
+            for (int64_t t = 0; t < sk; ++t) maxc = std::max(maxc, owner((t + 1) * kb - 1) - owner(t * kb) + 1);
+            pub.stream_k = 1;
+            pub.sk_maxc = static_cast<int32_t>(maxc);
+            pub.dp_tiles = dp;
+            pub.sk_tiles = sk;
+            pl.sk_iters = I;
+            pl.sk_w_bytes = round_up(sk * maxc * pair * 128 * static_cast<int64_t>(pub.tile_n) * 4, 256);
+            pl.sk_ctr_bytes = round_up(sk * pair * 4 * 4, 256);
+        }
+    }
+    find_tc_variant(pl.var.bn, pl.var.pair, pl.epi, pub.stream_k, &pl.var);
+    pub.units = pub.stream_k ? pub.dp_tiles : tiles * pub.splits;
+    pub.grid = pub.stream_k ? std::min<int64_t>(G, tiles * kb) * pair : std::min<int64_t>(pub.units, G) * pair;
+    pub.workspace_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes;
 }
 
 // Tensor-core tile plan; pure host arithmetic, no CUDA calls.
@@ -244,6 +299,8 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
         bn = pr.M <= 16 ? 16 : pr.M <= 32 ? 32 : 64;
         pair = 1;
     } else {
+        // 256x256 CTA-pair tiles are the most efficient shape; smaller tiles only
+        // when short K or few tiles make the pair's fixed costs dominate.
         const int64_t t_pair = ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.batch;
         const int64_t t_256 = ceil_div(pr.M, 128) * ceil_div(pr.N, 256) * pr.batch;
         if (pr.K >= 512 && 2 * t_pair >= slots) {
@@ -264,23 +321,15 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     const int64_t rows_b = swap ? pr.M : pr.N;
     const int64_t kb = ceil_div(pr.K, 64);
 
-    // Split K when the tiles alone cannot fill the machine.
+    // Split-K with a separate reduction only when forced (the default for too
+    // few tiles is the stream-K split decided in plan_stream_k).
     int splits = 1;
-    const int64_t tiles_1 = ceil_div(rows_a, 128) * ceil_div(rows_b, swap ? bn : 128) * pr.batch;
-    if (pair == 1 && kb >= 8 && tiles_1 * 2 <= slots) {
-        int64_t best = INT64_MAX;
-        const int64_t max_s = std::min<int64_t>(64, kb / 4);
-        for (int64_t s = 1; s <= max_s; ++s) {
-            const int64_t cost = ceil_div(tiles_1 * s, slots) * (ceil_div(kb, s) + 2);
-            if (cost < best) {
-                best = cost;
-                splits = static_cast<int>(s);
-            }
-        }
-    }
     const int64_t fsplit = g_opt_force_splits.load();
-    if (fsplit >= 1 && pair == 1) splits = static_cast<int>(std::min<int64_t>(fsplit, kb));
-    if (splits > 1 && !swap) bn = 128;  // the partial-sum variant exists at 128 columns
+    if (fsplit >= 1) {
+        pair = 1;
+        splits = static_cast<int>(std::min<int64_t>(fsplit, kb));
+        if (!swap) bn = 128;  // the partial-sum variant exists at 128 columns
+    }
 
     int epi;
     if (splits > 1) epi = swap ? EPI_PARTIAL_SWAP : EPI_PARTIAL;
@@ -289,12 +338,12 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     else epi = EPI_GENERIC;
 
     TcVariant v;
-    if (!find_tc_variant(bn, pair, epi, &v)) {
+    if (!find_tc_variant(bn, pair, epi, 0, &v)) {
         // Fall back to the single-CTA variant of the same epilogue.
         pair = 1;
-        if (!find_tc_variant(bn, pair, epi, &v)) {
+        if (!find_tc_variant(bn, pair, epi, 0, &v)) {
             bn = 128;
-            find_tc_variant(bn, pair, epi, &v);
+            find_tc_variant(bn, pair, epi, 0, &v);
         }
     }
     pl.var = v;
@@ -313,8 +362,6 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     pub.splits = splits;
     pub.stages = v.stages;
     pub.epi_tma = epi == EPI_TMA ? 1 : 0;
-    pub.units = pl.tiles_m * pl.tiles_n * pr.batch * splits;
-    pub.grid = std::min<int64_t>(pub.units * pair, (slots / pair) * pair);
 
     pl.ldo_a = round_up(pr.K, 8);
     pl.ldo_b = round_up(pr.K, 8);
@@ -323,7 +370,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     pl.pack_a_bytes = pub.pack_a ? round_up(nba * pr.M * pl.ldo_a * 2, 256) : 0;
     pl.pack_b_bytes = pub.pack_b ? round_up(nbb * pr.N * pl.ldo_b * 2, 256) : 0;
     pl.partial_bytes = splits > 1 ? round_up(pr.batch * splits * pr.M * pr.N * 4, 256) : 0;
-    pub.workspace_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes;
+    plan_stream_k(pr, pl, slots / pair);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -394,7 +441,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     if (pl.epi == EPI_TMA &&
         !encode_map(&mapD, D, p.N, p.M, p.batch, p.ldd, p.sD, p.batch > 1, 64, 32)) {
         TcVariant v;
-        if (find_tc_variant(pl.var.bn, pl.var.pair, EPI_GENERIC, &v)) {
+        if (find_tc_variant(pl.var.bn, pl.var.pair, EPI_GENERIC, 0, &v)) {
             pl.var = v;
             pl.epi = EPI_GENERIC;
             pl.pub.epi_tma = 0;
@@ -403,7 +450,15 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
         }
     }
 
-    const int64_t ws_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes;
+    int64_t cap = dev->capacity[pl.var.index];
+    if (cap == 0) {
+        cap = tc_variant_capacity(pl.var, dev->sms);
+        if (cap <= 0) cap = dev->sms;
+        dev->capacity[pl.var.index] = cap;
+    }
+    plan_stream_k(p, pl, cap / pl.var.pair);
+
+    const int64_t ws_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes;
     uint8_t* ws = nullptr;
     if (ws_bytes > 0) {
         e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), static_cast<size_t>(ws_bytes), dev->pool, stream);
@@ -454,7 +509,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     kp.zA = swap ? (b_batched ? 1 : 0) : (a_batched ? 1 : 0);
     kp.zB = swap ? (a_batched ? 1 : 0) : (b_batched ? 1 : 0);
     kp.zD = p.batch > 1 ? 1 : 0;
-    kp.num_units = pl.tiles_m * pl.tiles_n * p.batch * pl.pub.splits;
+    kp.num_units = pl.pub.units;
     kp.M = static_cast<int32_t>(p.M);
     kp.N = static_cast<int32_t>(p.N);
     kp.alpha = alpha;
@@ -470,14 +525,17 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     kp.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
     kp.debug_skip_first_load = g_opt_skip_first_load.load() != 0 ? 1 : 0;
 
-    int64_t cap = dev->capacity[pl.var.index];
-    if (cap == 0) {
-        cap = tc_variant_capacity(pl.var, dev->sms);
-        if (cap <= 0) cap = dev->sms;
-        dev->capacity[pl.var.index] = cap;
+    if (pl.sk_iters > 0) {
+        uint8_t* sk_base = ws + pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes;
+        kp.sk_iters = pl.sk_iters;
+        kp.sk_maxc = pl.pub.sk_maxc;
+        kp.sk_W = reinterpret_cast<float*>(sk_base);
+        kp.sk_counters = reinterpret_cast<uint32_t*>(sk_base + pl.sk_w_bytes);
+        e = cudaMemsetAsync(kp.sk_counters, 0, static_cast<size_t>(pl.sk_ctr_bytes), stream);
+        if (e != cudaSuccess) { release(); return cuda_fail(e); }
     }
     int64_t grid = 0;
-    e = launch_tc_variant(pl.var, mapA_op, mapB_op, mapD, kp, cap, stream, &grid);
+    e = launch_tc_variant(pl.var, mapA_op, mapB_op, mapD, kp, pl.pub.grid, stream, &grid);
     if (e != cudaSuccess) { release(); return cuda_fail(e); }
     if (pl.pub.splits > 1) {
         e = launch_splitk_reduce(kp.W, pl.pub.splits, p.M, p.N, p.batch, alpha, p.beta, C, p.ldc, p.sC, D, p.ldd,
@@ -598,6 +656,10 @@ gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value) {
             return GEMM_OK;
         case GEMM_TN_OPT_FORCE_GENERIC_EPI: g_opt_force_generic = value ? 1 : 0; return GEMM_OK;
         case GEMM_TN_OPT_FORCE_PACK: g_opt_force_pack = value ? 1 : 0; return GEMM_OK;
+        case GEMM_TN_OPT_STREAM_K:
+            if (value < -1 || value > 1) return GEMM_ERR_INVALID_VALUE;
+            g_opt_stream_k = value;
+            return GEMM_OK;
     }
     return GEMM_ERR_INVALID_VALUE;
 }
@@ -612,6 +674,7 @@ int64_t gemm_tn_f16_get_option(int32_t option) {
         case GEMM_TN_OPT_FORCE_SWAP: return g_opt_force_swap.load();
         case GEMM_TN_OPT_FORCE_GENERIC_EPI: return g_opt_force_generic.load();
         case GEMM_TN_OPT_FORCE_PACK: return g_opt_force_pack.load();
+        case GEMM_TN_OPT_STREAM_K: return g_opt_stream_k.load();
     }
     return -1;
 }

@@ -16,13 +16,14 @@ struct TcVariant {
     int pair;    // 1 = one CTA per 128-row tile, 2 = CTA pair per 256-row tile
     int stages;  // shared-memory ring depth
     int epi;     // EpiMode
+    int sk;      // 1: compiled with the stream-K phase
     int index;   // position in the variant table (for per-device caches)
 };
 
-constexpr int kMaxVariants = 32;
+constexpr int kMaxVariants = 48;
 
-// Looks up the compiled variant for (bn, pair, epi); returns false if none exists.
-bool find_tc_variant(int bn, int pair, int epi, TcVariant* out);
+// Looks up the compiled variant for (bn, pair, epi, sk); returns false if none exists.
+bool find_tc_variant(int bn, int pair, int epi, int sk, TcVariant* out);
 
 // Launches a tensor-core variant with a persistent grid of at most `max_ctas`
 // CTAs (rounded to whole CTA pairs).  *grid_out receives the grid used.

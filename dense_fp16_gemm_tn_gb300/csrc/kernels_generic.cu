@@ -6,29 +6,35 @@ namespace gtn {
 bool launch_family_generic(const TcVariant& v, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
                           const KParams& p, int64_t max_ctas, cudaStream_t stream, int64_t* grid_out,
                           cudaError_t* err) {
-#define GTN_CASE(BN, PAIR, ST, EPI)                                                                    \
-    if (v.bn == BN && v.pair == PAIR && v.stages == ST && v.epi == EPI) {                             \
-        *err = TcLauncher<BN, PAIR, ST, EPI>::launch(tmA, tmB, tmD, p, max_ctas, stream, grid_out);   \
+#define GTN_CASE(BN, PAIR, ST, EPI, SK)                                                                    \
+    if (v.bn == BN && v.pair == PAIR && v.stages == ST && v.epi == EPI && v.sk == SK) {                             \
+        *err = TcLauncher<BN, PAIR, ST, EPI, SK>::launch(tmA, tmB, tmD, p, max_ctas, stream, grid_out);   \
         return true;                                                                                  \
     }
-    GTN_CASE(256, 1, 4, EPI_GENERIC)
-    GTN_CASE(256, 2, 6, EPI_GENERIC)
-    GTN_CASE(128, 1, 6, EPI_GENERIC)
-    GTN_CASE(128, 1, 6, EPI_PARTIAL)
+    GTN_CASE(256, 1, 4, EPI_GENERIC, 0)
+    GTN_CASE(256, 1, 4, EPI_GENERIC, 1)
+    GTN_CASE(256, 2, 6, EPI_GENERIC, 0)
+    GTN_CASE(256, 2, 6, EPI_GENERIC, 1)
+    GTN_CASE(128, 1, 6, EPI_GENERIC, 0)
+    GTN_CASE(128, 1, 6, EPI_GENERIC, 1)
+    GTN_CASE(128, 1, 6, EPI_PARTIAL, 0)
 #undef GTN_CASE
     return false;
 }
 
 bool capacity_family_generic(const TcVariant& v, int sms, int64_t* cap) {
-#define GTN_CASE(BN, PAIR, ST, EPI)                                          \
-    if (v.bn == BN && v.pair == PAIR && v.stages == ST && v.epi == EPI) {   \
-        *cap = TcLauncher<BN, PAIR, ST, EPI>::capacity(sms);                \
+#define GTN_CASE(BN, PAIR, ST, EPI, SK)                                          \
+    if (v.bn == BN && v.pair == PAIR && v.stages == ST && v.epi == EPI && v.sk == SK) {   \
+        *cap = TcLauncher<BN, PAIR, ST, EPI, SK>::capacity(sms);                \
         return true;                                                        \
     }
-    GTN_CASE(256, 1, 4, EPI_GENERIC)
-    GTN_CASE(256, 2, 6, EPI_GENERIC)
-    GTN_CASE(128, 1, 6, EPI_GENERIC)
-    GTN_CASE(128, 1, 6, EPI_PARTIAL)
+    GTN_CASE(256, 1, 4, EPI_GENERIC, 0)
+    GTN_CASE(256, 1, 4, EPI_GENERIC, 1)
+    GTN_CASE(256, 2, 6, EPI_GENERIC, 0)
+    GTN_CASE(256, 2, 6, EPI_GENERIC, 1)
+    GTN_CASE(128, 1, 6, EPI_GENERIC, 0)
+    GTN_CASE(128, 1, 6, EPI_GENERIC, 1)
+    GTN_CASE(128, 1, 6, EPI_PARTIAL, 0)
 #undef GTN_CASE
     return false;
 }

@@ -21,7 +21,7 @@ struct KParams {
     int32_t kb_total;          // number of 64-wide k-blocks, ceil(K/64)
     int32_t group_m;           // rasterisation group size along the tile rows
     int32_t zA, zB, zD;        // batch coordinate multipliers (0 = operand not batched)
-    int64_t num_units;
+    int64_t num_units;         // data-parallel units: whole tiles, or (tile, K slice) pairs when splits > 1
     // Problem view, for the epilogue.
     int32_t M, N;
     float alpha, beta;
@@ -30,6 +30,15 @@ struct KParams {
     const void* C;
     int64_t ldc, strideC;
     float* W;  // split-K partials, [batch][splits][M][N] fp32
+    // Stream-K: after its data-parallel units, CTA group g (of G) runs k-block
+    // iterations [g*I/G, (g+1)*I/G) of the I = sk_tiles * kb_total iterations of the
+    // tiles that follow the data-parallel ones.  A tile cut between groups is
+    // finished by whichever group contributes last (arrival counter), which sums
+    // every group's fp32 partial in group order.
+    int64_t sk_iters;          // I; 0 = no stream-K phase
+    int32_t sk_maxc;           // partial slots per stream-K tile (>= contributors of any tile)
+    float* sk_W;               // [sk_tile][sk_maxc][PAIR][128][BN] fp32 partial accumulators
+    uint32_t* sk_counters;     // [sk_tile][PAIR][4 epilogue warps] arrivals; zero before the launch
     uint32_t* err;
     uint64_t timeout_ns;
     int32_t debug_skip_first_load;  // test hook: CTA 0 never issues its first load

@@ -165,7 +165,7 @@ extern "C" GEMM_TN_API gemm_status_t gemm_tn_f16_splitk_static(const void* A, in
     if (s * M * N * 4 > static_cast<int64_t>(GEMM_TN_STATIC_SCRATCH_BYTES)) return GEMM_ERR_WORKSPACE;
 
     TcVariant v;
-    if (!find_tc_variant(bn, 1, swap ? EPI_PARTIAL_SWAP : EPI_PARTIAL, &v)) return GEMM_ERR_UNSUPPORTED;
+    if (!find_tc_variant(bn, 1, swap ? EPI_PARTIAL_SWAP : EPI_PARTIAL, 0, &v)) return GEMM_ERR_UNSUPPORTED;
     CUtensorMap mapA, mapB;
     // MMA A operand: the 128-row side; MMA B operand: the BN-row side.
     if (!operand_map(&mapA, swap ? B : A, K, rows_a, swap ? ldb : lda, 128) ||

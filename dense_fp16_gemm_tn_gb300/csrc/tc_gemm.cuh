@@ -33,6 +33,14 @@
 // clip at the tensor bounds, so ragged shapes need no masks on the fast path;
 // the predicated epilogues mask element by element.
 //
+// Stream-K: when the tiles do not divide evenly over the CTA groups, the last
+// partial wave is not run tile by tile; its k-block iterations are spread
+// evenly over all groups instead.  A group that computes part of a tile writes
+// its fp32 partial accumulator to scratch and counts itself in (per epilogue
+// warp, i.e. per 32 rows); the last group to arrive for those rows sums all
+// partials in group order (deterministic) and runs the epilogue.  No group, and
+// no warp, ever waits for another.
+//
 // Every mbarrier wait is bounded: past `timeout_ns` the waiting thread records
 // an error word, raises a CTA-wide abort flag and returns; the kernel then lets
 // in-flight copies and MMAs drain, frees its tensor memory and exits normally.
@@ -40,6 +48,7 @@
 
 #include <cuda_fp16.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "kparams.h"
 #include "ptx.cuh"
@@ -77,32 +86,100 @@ struct TileCfg {
     static_assert(PAIR == 1 || PAIR == 2, "CTA pair or single CTA");
 };
 
-struct Unit {
+// One piece of work for a CTA (pair): k-blocks [kb0, kb1) of one output tile.
+struct Seg {
     int32_t b, tm, tn, kb0, kb1, split;
+    int32_t sk_tile;  // index among the stream-K tiles, or -1 when this segment finishes its tile alone
+    int32_t sk_j;     // this group's rank among the tile's contributors
+    int32_t sk_n;     // number of contributors to the tile
 };
 
-__device__ __forceinline__ Unit decode_unit(const KParams& p, int64_t u) {
-    Unit w;
-    w.split = static_cast<int32_t>(u % p.splits);
-    const int64_t t = u / p.splits;
+// Iterates the segments of CTA group `g` of `G`: its contiguous range of
+// stream-K iterations, then its data-parallel units g, g+G, ...  Every role of
+// the CTA walks the same sequence.
+struct SegIter {
+    int64_t g, G;
+    int64_t dp_next;
+    int64_t sk_i, sk_end;
+};
+
+__device__ __forceinline__ void tile_coords(const KParams& p, int64_t t, Seg& s) {
     const int64_t per_batch = static_cast<int64_t>(p.tiles_m) * p.tiles_n;
-    w.b = static_cast<int32_t>(t / per_batch);
+    s.b = static_cast<int32_t>(t / per_batch);
     const int64_t r = t % per_batch;
+    // Grouped rasterisation: group_m tile rows are walked column by column, so
+    // the tiles in flight at one time share A rows and B rows in L2.
     const int64_t span = static_cast<int64_t>(p.group_m) * p.tiles_n;
     const int32_t first = static_cast<int32_t>(r / span) * p.group_m;
     const int32_t gm = min(p.group_m, p.tiles_m - first);
     const int64_t rr = r % span;
-    w.tm = first + static_cast<int32_t>(rr % gm);
-    w.tn = static_cast<int32_t>(rr / gm);
-    w.kb0 = static_cast<int32_t>((static_cast<int64_t>(w.split) * p.kb_total) / p.splits);
-    w.kb1 = static_cast<int32_t>((static_cast<int64_t>(w.split + 1) * p.kb_total) / p.splits);
-    return w;
+    s.tm = first + static_cast<int32_t>(rr % gm);
+    s.tn = static_cast<int32_t>(rr / gm);
+}
+
+__device__ __forceinline__ int64_t sk_start(const KParams& p, int64_t g, int64_t G) { return (g * p.sk_iters) / G; }
+
+// Group that owns stream-K iteration i: the largest g with sk_start(g) <= i.
+__device__ __forceinline__ int64_t sk_owner(const KParams& p, int64_t i, int64_t G) {
+    return ((i + 1) * G - 1) / p.sk_iters;
+}
+
+template <bool SK>
+__device__ __forceinline__ SegIter seg_begin(const KParams& p, int64_t g, int64_t G) {
+    SegIter it;
+    it.g = g;
+    it.G = G;
+    it.dp_next = g;
+    it.sk_i = (SK && p.sk_iters > 0) ? sk_start(p, g, G) : 0;
+    it.sk_end = (SK && p.sk_iters > 0) ? sk_start(p, g + 1, G) : 0;
+    return it;
+}
+
+template <bool SK>
+__device__ __forceinline__ bool seg_next(const KParams& p, SegIter& it, Seg& s) {
+    // Stream-K iterations come first, so the tile fixups they lead to overlap the
+    // data-parallel work that follows instead of trailing the kernel.
+    if (SK && it.sk_i < it.sk_end) {
+        const int64_t kb = p.kb_total;
+        const int64_t tsk = it.sk_i / kb;
+        const int64_t k0 = it.sk_i - tsk * kb;
+        const int64_t k1 = min(kb, k0 + (it.sk_end - it.sk_i));
+        tile_coords(p, p.num_units + tsk, s);
+        s.split = 0;
+        s.kb0 = static_cast<int32_t>(k0);
+        s.kb1 = static_cast<int32_t>(k1);
+        if (k0 == 0 && k1 == kb) {
+            s.sk_tile = -1;
+            s.sk_j = 0;
+            s.sk_n = 1;
+        } else {
+            const int64_t first = sk_owner(p, tsk * kb, it.G);
+            s.sk_tile = static_cast<int32_t>(tsk);
+            s.sk_j = static_cast<int32_t>(it.g - first);
+            s.sk_n = static_cast<int32_t>(sk_owner(p, (tsk + 1) * kb - 1, it.G) - first + 1);
+        }
+        it.sk_i += k1 - k0;
+        return true;
+    }
+    if (it.dp_next < p.num_units) {
+        const int64_t u = it.dp_next;
+        it.dp_next += it.G;
+        s.split = static_cast<int32_t>(u % p.splits);
+        tile_coords(p, u / p.splits, s);
+        s.kb0 = static_cast<int32_t>((static_cast<int64_t>(s.split) * p.kb_total) / p.splits);
+        s.kb1 = static_cast<int32_t>((static_cast<int64_t>(s.split + 1) * p.kb_total) / p.splits);
+        s.sk_tile = -1;
+        s.sk_j = 0;
+        s.sk_n = 1;
+        return true;
+    }
+    return false;
 }
 
 // Slow path of a bounded wait.  Returns false (and raises the abort flag) when
 // the wait gave up; records the first failure in the device error word.
 static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint32_t* err, uint64_t timeout_ns,
-                                       volatile int* abort_flag, uint32_t who) {
+                                              volatile int* abort_flag, uint32_t who) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -138,7 +215,9 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
-template <int BN, int PAIR, int STAGES, int EPI>
+// SK: compiled with the stream-K phase (partial slots, arrival counters,
+// fixups); without it the kernel is purely data-parallel.
+template <int BN, int PAIR, int STAGES, int EPI, bool SK>
 __global__ void __launch_bounds__(TileCfg<BN, PAIR, STAGES, EPI>::THREADS, 1)
 gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmD, const KParams p) {
@@ -159,8 +238,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = (PAIR == 2) ? cluster_cta_rank() : 0u;
-    const int64_t cluster_id = blockIdx.x / PAIR;
-    const int64_t nclusters = gridDim.x / PAIR;
+    const int64_t group = blockIdx.x / PAIR;
+    const int64_t ngroups = gridDim.x / PAIR;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -192,8 +271,9 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             uint32_t phase = 0;
             bool ok = true;
             bool first = true;
-            for (int64_t u = cluster_id; u < p.num_units && ok; u += nclusters) {
-                const Unit w = decode_unit(p, u);
+            SegIter it = seg_begin<SK>(p, group, ngroups);
+            Seg w;
+            while (ok && seg_next<SK>(p, it, w)) {
                 const int32_t rowA = w.tm * (Cfg::BM * PAIR) + Cfg::BM * static_cast<int32_t>(rank);
                 const int32_t rowB = w.tn * BN + Cfg::BN_LOCAL * static_cast<int32_t>(rank);
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
@@ -236,8 +316,9 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int64_t u = cluster_id; u < p.num_units && ok; u += nclusters) {
-                const Unit w = decode_unit(p, u);
+            SegIter it = seg_begin<SK>(p, group, ngroups);
+            Seg w;
+            while (ok && seg_next<SK>(p, it, w)) {
                 if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, p.err, p.timeout_ns, abort_flag, 3)) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -274,11 +355,20 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint32_t acc_phase = 0;
         uint32_t chunk_count = 0;
         const bool use_c = (EPI == EPI_GENERIC || EPI == EPI_SWAP) && p.beta != 0.0f;
-        for (int64_t u = cluster_id; u < p.num_units; u += nclusters) {
-            const Unit w = decode_unit(p, u);
+        SegIter it = seg_begin<SK>(p, group, ngroups);
+        Seg w;
+        while (seg_next<SK>(p, it, w)) {
             // First accumulator row / column of this warp, in the tensor-core view.
             const int64_t arow0 = static_cast<int64_t>(w.tm) * (Cfg::BM * PAIR) + Cfg::BM * rank + quarter * 32;
             const int64_t acol0 = static_cast<int64_t>(w.tn) * BN;
+            const bool partial = SK && w.sk_tile >= 0;
+            // This warp's block of the partial-accumulator slot of contributor j,
+            // stored column by column ([col][lane]) so a warp's accesses coalesce.
+            auto slot_block = [&](int j) -> float* {
+                return p.sk_W + (((static_cast<int64_t>(w.sk_tile) * p.sk_maxc + j) * PAIR + rank) * 4 + quarter) *
+                                    static_cast<int64_t>(32 * BN) +
+                       lane;
+            };
             // Predicated epilogue: C of the first 32-column chunk is fetched before the
             // accumulator is ready, so its memory latency overlaps the main loop.
             __half cnext[32];
@@ -291,7 +381,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     dst[r] = (col_ok && arow0 + r < p.M) ? src[(arow0 + r) * p.ldc] : __ushort_as_half(0);
             };
             if constexpr (EPI == EPI_GENERIC) {
-                if (use_c) load_c_chunk(0, cnext);
+                if (use_c && !partial) load_c_chunk(0, cnext);
             }
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, p.err, p.timeout_ns, abort_flag, 5) ? 1 : 0;
@@ -300,141 +390,223 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
 
-            if constexpr (EPI == EPI_TMA) {
-#pragma unroll 1
-                for (int c = 0; c < BN / 64; ++c) {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld_32x32b_x32(t_row + c * 64, v0);
-                    tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
-                    tmem_ld_wait();
-                    const uint32_t buf = chunk_count & 1u;
-                    if (lane == 0) bulk_wait_group_read<1>();
-                    __syncwarp();
-                    const uint32_t sb = smem_u32(ebuf) + buf * 4096u;
-                    const uint32_t row_addr = sb + lane * 128u;
-                    const float al = p.alpha;
+            // Sum of all contributors' partials for this thread's row, columns
+            // [col, col + NC), added in contributor order (deterministic).  Two
+            // contributors' loads are in flight at a time.
+            auto sum_parts = [&](int col, auto& v) {
+                constexpr int NC = sizeof(v) / sizeof(v[0]);
+                float acc_f[NC];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
-                                     pack_half2(al * __uint_as_float(v0[8 * j + 0]), al * __uint_as_float(v0[8 * j + 1])),
-                                     pack_half2(al * __uint_as_float(v0[8 * j + 2]), al * __uint_as_float(v0[8 * j + 3])),
-                                     pack_half2(al * __uint_as_float(v0[8 * j + 4]), al * __uint_as_float(v0[8 * j + 5])),
-                                     pack_half2(al * __uint_as_float(v0[8 * j + 6]), al * __uint_as_float(v0[8 * j + 7])));
-                    }
+                for (int q = 0; q < NC; ++q) acc_f[q] = 0.0f;
+                for (int j = 0; j < w.sk_n; j += 2) {
+                    const float* s0 = slot_block(j) + col * 32;
+                    const float* s1 = slot_block(j + 1 < w.sk_n ? j + 1 : j) + col * 32;
+                    float a[NC], b[NC];
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        st_shared_v4(row_addr + ((static_cast<uint32_t>(j + 4) ^ (lane & 7u)) << 4),
-                                     pack_half2(al * __uint_as_float(v1[8 * j + 0]), al * __uint_as_float(v1[8 * j + 1])),
-                                     pack_half2(al * __uint_as_float(v1[8 * j + 2]), al * __uint_as_float(v1[8 * j + 3])),
-                                     pack_half2(al * __uint_as_float(v1[8 * j + 4]), al * __uint_as_float(v1[8 * j + 5])),
-                                     pack_half2(al * __uint_as_float(v1[8 * j + 6]), al * __uint_as_float(v1[8 * j + 7])));
+                    for (int q = 0; q < NC; ++q) a[q] = __ldcg(s0 + q * 32);
+#pragma unroll
+                    for (int q = 0; q < NC; ++q) b[q] = __ldcg(s1 + q * 32);
+#pragma unroll
+                    for (int q = 0; q < NC; ++q) acc_f[q] += a[q];
+                    if (j + 1 < w.sk_n) {
+#pragma unroll
+                        for (int q = 0; q < NC; ++q) acc_f[q] += b[q];
                     }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tma_store_3d(&tmD, sb, static_cast<int32_t>(acol0 + c * 64), static_cast<int32_t>(arow0),
-                                     w.b * p.zD);
-                        bulk_commit_group();
-                    }
-                    ++chunk_count;
                 }
-            } else if constexpr (EPI == EPI_GENERIC || EPI == EPI_PARTIAL) {
-                // Transpose each 32x32 block through padded shared memory so that a warp
-                // reads C and writes D along rows (coalesced), whatever the alignment.
-                float* T = reinterpret_cast<float*>(ebuf);
-                __half* Dp = static_cast<__half*>(p.D);
+#pragma unroll
+                for (int q = 0; q < NC; ++q) v[q] = __float_as_uint(acc_f[q]);
+            };
+
+            // Writes the finished tile (this warp's 32 rows) from tensor memory, or
+            // (stream-K fixup, PARTS) from the sum of the contributors' partials.
+            auto emit_tile = [&](auto parts_tag) {
+                constexpr bool PARTS = decltype(parts_tag)::value;
+                if constexpr (EPI == EPI_TMA) {
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
-                    __half ccur[32];
+                    for (int c = 0; c < BN / 64; ++c) {
+                        uint32_t v0[32], v1[32];
+                        if constexpr (!PARTS) {
+                            tmem_ld_32x32b_x32(t_row + c * 64, v0);
+                            tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
+                            tmem_ld_wait();
+                        } else {
+                            sum_parts(c * 64, v0);
+                            sum_parts(c * 64 + 32, v1);
+                        }
+                        const uint32_t buf = chunk_count & 1u;
+                        if (lane == 0) bulk_wait_group_read<1>();
+                        __syncwarp();
+                        const uint32_t sb = smem_u32(ebuf) + buf * 4096u;
+                        const uint32_t row_addr = sb + lane * 128u;
+                        const float al = p.alpha;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                                         pack_half2(al * __uint_as_float(v0[8 * j + 0]), al * __uint_as_float(v0[8 * j + 1])),
+                                         pack_half2(al * __uint_as_float(v0[8 * j + 2]), al * __uint_as_float(v0[8 * j + 3])),
+                                         pack_half2(al * __uint_as_float(v0[8 * j + 4]), al * __uint_as_float(v0[8 * j + 5])),
+                                         pack_half2(al * __uint_as_float(v0[8 * j + 6]), al * __uint_as_float(v0[8 * j + 7])));
+                        }
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            st_shared_v4(row_addr + ((static_cast<uint32_t>(j + 4) ^ (lane & 7u)) << 4),
+                                         pack_half2(al * __uint_as_float(v1[8 * j + 0]), al * __uint_as_float(v1[8 * j + 1])),
+                                         pack_half2(al * __uint_as_float(v1[8 * j + 2]), al * __uint_as_float(v1[8 * j + 3])),
+                                         pack_half2(al * __uint_as_float(v1[8 * j + 4]), al * __uint_as_float(v1[8 * j + 5])),
+                                         pack_half2(al * __uint_as_float(v1[8 * j + 6]), al * __uint_as_float(v1[8 * j + 7])));
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_3d(&tmD, sb, static_cast<int32_t>(acol0 + c * 64), static_cast<int32_t>(arow0),
+                                         w.b * p.zD);
+                            bulk_commit_group();
+                        }
+                        ++chunk_count;
+                    }
+                } else if constexpr (EPI == EPI_GENERIC || EPI == EPI_PARTIAL) {
+                    // Transpose each 32x32 block through padded shared memory so that a warp
+                    // reads C and writes D along rows (coalesced), whatever the alignment.
+                    float* T = reinterpret_cast<float*>(ebuf);
+                    __half* Dp = static_cast<__half*>(p.D);
                     if constexpr (EPI == EPI_GENERIC) {
-                        if (use_c) {
-#pragma unroll
-                            for (int r = 0; r < 32; ++r) ccur[r] = cnext[r];
-                            // Loads for the next chunk are issued before this chunk's stores
-                            // (different columns, so an aliased C == D stays correct).
-                            if (c + 1 < BN / 32) load_c_chunk(c + 1, cnext);
-                        }
+                        if (use_c && PARTS) load_c_chunk(0, cnext);
                     }
-                    uint32_t v[32];
-                    tmem_ld_32x32b_x32(t_row + c * 32, v);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) T[lane * 33 + j] = __uint_as_float(v[j]);
-                    __syncwarp();
-                    const int64_t col = acol0 + c * 32 + lane;
-                    if (col < p.N) {
-                        if constexpr (EPI == EPI_GENERIC) {
-                            __half* dst = Dp + static_cast<int64_t>(w.b) * p.strideD + col;
-#pragma unroll
-                            for (int r = 0; r < 32; ++r) {
-                                const int64_t row = arow0 + r;
-                                if (row < p.M) {
-                                    float x = p.alpha * T[r * 33 + lane];
-                                    if (use_c) x = fmaf(p.beta, __half2float(ccur[r]), x);
-                                    dst[row * p.ldd] = __float2half_rn(x);
-                                }
-                            }
-                        } else {
-                            float* Wp = p.W + (static_cast<int64_t>(w.b) * p.splits + w.split) * p.M * p.N + col;
-#pragma unroll 8
-                            for (int r = 0; r < 32; ++r) {
-                                const int64_t row = arow0 + r;
-                                if (row < p.M) Wp[row * p.N] = T[r * 33 + lane];
-                            }
-                        }
-                    }
-                    __syncwarp();
-                }
-            } else {
-                // Swapped operands: accumulator row = problem column n, accumulator column = problem row m.
-                const int64_t n = arow0 + lane;
-                __half* Dp = static_cast<__half*>(p.D);
-                const __half* Cp = static_cast<const __half*>(p.C);
 #pragma unroll 1
-                for (int c = 0; c < BN / 16; ++c) {
-                    uint32_t v[16];
-                    tmem_ld_32x32b_x16(t_row + c * 16, v);
-                    tmem_ld_wait();
-                    if (n < p.N) {
-                        if constexpr (EPI == EPI_SWAP) {
-                            // all C loads of the chunk first, then the stores
-                            __half cv[16];
+                    for (int c = 0; c < BN / 32; ++c) {
+                        __half ccur[32];
+                        if constexpr (EPI == EPI_GENERIC) {
+                            if (use_c) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int64_t m = acol0 + c * 16 + j;
-                                cv[j] = (use_c && m < p.M)
-                                            ? Cp[static_cast<int64_t>(w.b) * p.strideC + m * p.ldc + n]
-                                            : __ushort_as_half(0);
+                                for (int r = 0; r < 32; ++r) ccur[r] = cnext[r];
+                                // Loads for the next chunk are issued before this chunk's stores
+                                // (different columns, so an aliased C == D stays correct).
+                                if (c + 1 < BN / 32) load_c_chunk(c + 1, cnext);
                             }
+                        }
+                        uint32_t v[32];
+                        if constexpr (!PARTS) {
+                            tmem_ld_32x32b_x32(t_row + c * 32, v);
+                            tmem_ld_wait();
+                        } else {
+                            sum_parts(c * 32, v);
+                        }
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int64_t m = acol0 + c * 16 + j;
-                                if (m < p.M) {
-                                    float x = p.alpha * __uint_as_float(v[j]);
-                                    if (use_c) x = fmaf(p.beta, __half2float(cv[j]), x);
-                                    Dp[static_cast<int64_t>(w.b) * p.strideD + m * p.ldd + n] = __float2half_rn(x);
+                        for (int j = 0; j < 32; ++j) T[lane * 33 + j] = __uint_as_float(v[j]);
+                        __syncwarp();
+                        const int64_t col = acol0 + c * 32 + lane;
+                        if (col < p.N) {
+                            if constexpr (EPI == EPI_GENERIC) {
+                                __half* dst = Dp + static_cast<int64_t>(w.b) * p.strideD + col;
+#pragma unroll
+                                for (int r = 0; r < 32; ++r) {
+                                    const int64_t row = arow0 + r;
+                                    if (row < p.M) {
+                                        float x = p.alpha * T[r * 33 + lane];
+                                        if (use_c) x = fmaf(p.beta, __half2float(ccur[r]), x);
+                                        dst[row * p.ldd] = __float2half_rn(x);
+                                    }
+                                }
+                            } else {
+                                float* Wp = p.W + (static_cast<int64_t>(w.b) * p.splits + w.split) * p.M * p.N + col;
+#pragma unroll 8
+                                for (int r = 0; r < 32; ++r) {
+                                    const int64_t row = arow0 + r;
+                                    if (row < p.M) Wp[row * p.N] = T[r * 33 + lane];
                                 }
                             }
+                        }
+                        __syncwarp();
+                    }
+                } else {
+                    // Swapped operands: accumulator row = problem column n, accumulator column = problem row m.
+                    const int64_t n = arow0 + lane;
+                    __half* Dp = static_cast<__half*>(p.D);
+                    const __half* Cp = static_cast<const __half*>(p.C);
+#pragma unroll 1
+                    for (int c = 0; c < BN / 16; ++c) {
+                        uint32_t v[16];
+                        if constexpr (!PARTS) {
+                            tmem_ld_32x32b_x16(t_row + c * 16, v);
+                            tmem_ld_wait();
                         } else {
+                            sum_parts(c * 16, v);
+                        }
+                        if (n < p.N) {
+                            if constexpr (EPI == EPI_SWAP) {
+                                // all C loads of the chunk first, then the stores
+                                __half cv[16];
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int64_t m = acol0 + c * 16 + j;
-                                if (m < p.M)
-                                    p.W[((static_cast<int64_t>(w.b) * p.splits + w.split) * p.M + m) * p.N + n] =
-                                        __uint_as_float(v[j]);
+                                for (int j = 0; j < 16; ++j) {
+                                    const int64_t m = acol0 + c * 16 + j;
+                                    cv[j] = (use_c && m < p.M)
+                                                ? Cp[static_cast<int64_t>(w.b) * p.strideC + m * p.ldc + n]
+                                                : __ushort_as_half(0);
+                                }
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) {
+                                    const int64_t m = acol0 + c * 16 + j;
+                                    if (m < p.M) {
+                                        float x = p.alpha * __uint_as_float(v[j]);
+                                        if (use_c) x = fmaf(p.beta, __half2float(cv[j]), x);
+                                        Dp[static_cast<int64_t>(w.b) * p.strideD + m * p.ldd + n] = __float2half_rn(x);
+                                    }
+                                }
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) {
+                                    const int64_t m = acol0 + c * 16 + j;
+                                    if (m < p.M)
+                                        p.W[((static_cast<int64_t>(w.b) * p.splits + w.split) * p.M + m) * p.N + n] =
+                                            __uint_as_float(v[j]);
+                                }
                             }
                         }
                     }
                 }
+            };
+
+            auto release_accumulator = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (PAIR == 1) mbar_arrive(tempty_bar(acc));
+                    else mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
+                }
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            };
+
+            if (!partial) {
+                emit_tile(std::false_type{});
+                release_accumulator();  // this warp is done reading the accumulator
+            } else if constexpr (SK) {
+                // Stream-K contribution: park this warp's 32 rows of the accumulator in its slot.
+                float* mine = slot_block(w.sk_j);
+                constexpr int PW = (BN % 32 == 0) ? 32 : 16;  // columns per tensor-memory load
+#pragma unroll 1
+                for (int c = 0; c < BN / PW; ++c) {
+                    uint32_t v[PW];
+                    if constexpr (PW == 32) tmem_ld_32x32b_x32(t_row + c * PW, v);
+                    else tmem_ld_32x32b_x16(t_row + c * PW, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < PW; ++q) mine[(c * PW + q) * 32] = __uint_as_float(v[q]);
+                }
+                release_accumulator();
+                // Count this warp's 32 rows in; the last contributor for these rows
+                // finishes them.  Each warp owns its rows outright, so no warp ever
+                // waits for another (an aborted warp cannot strand the others).
+                __threadfence();
+                __syncwarp();
+                uint32_t prev = 0;
+                if (lane == 0)
+                    prev = atomicAdd(p.sk_counters + (static_cast<int64_t>(w.sk_tile) * PAIR + rank) * 4 + quarter, 1u);
+                prev = __shfl_sync(0xffffffffu, prev, 0);
+                if (prev == static_cast<uint32_t>(w.sk_n - 1)) {
+                    __threadfence();
+                    emit_tile(std::true_type{});
+                }
             }
-            // This warp is done reading the accumulator: hand it back to the MMA issuer.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if constexpr (PAIR == 1) mbar_arrive(tempty_bar(acc));
-                else mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
-            }
-            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
         if constexpr (EPI == EPI_TMA) {
             if (lane == 0) bulk_wait_group<0>();

@@ -10,7 +10,7 @@
 
 namespace gtn {
 
-template <int BN, int PAIR, int STAGES, int EPI>
+template <int BN, int PAIR, int STAGES, int EPI, bool SK>
 struct TcLauncher {
     using Cfg = TileCfg<BN, PAIR, STAGES, EPI>;
 
@@ -23,7 +23,7 @@ struct TcLauncher {
         if (e != cudaSuccess) return e;
         std::lock_guard<std::mutex> lock(mu);
         if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-        e = cudaFuncSetAttribute(gemm_tn_tc_kernel<BN, PAIR, STAGES, EPI>,
+        e = cudaFuncSetAttribute(gemm_tn_tc_kernel<BN, PAIR, STAGES, EPI, SK>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) done[dev] = true;
@@ -47,7 +47,7 @@ struct TcLauncher {
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             int clusters = 0;
-            if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_tc_kernel<BN, PAIR, STAGES, EPI>, &cfg) !=
+            if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tn_tc_kernel<BN, PAIR, STAGES, EPI, SK>, &cfg) !=
                     cudaSuccess ||
                 clusters <= 0) {
                 cudaGetLastError();
@@ -61,8 +61,10 @@ struct TcLauncher {
                               const KParams& p, int64_t max_ctas, cudaStream_t stream, int64_t* grid_out) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        int64_t units_ctas = p.num_units * PAIR;
-        int64_t grid = max_ctas < units_ctas ? max_ctas : units_ctas;
+        // Data-parallel only: no more CTAs than units.  With a stream-K phase every
+        // group takes part, so the caller's grid is used as it is.
+        const int64_t units_ctas = p.num_units * PAIR;
+        int64_t grid = (p.sk_iters > 0 || max_ctas < units_ctas) ? max_ctas : units_ctas;
         grid = (grid / PAIR) * PAIR;
         if (grid < PAIR) grid = PAIR;
         cudaLaunchConfig_t cfg = {};
@@ -80,7 +82,7 @@ struct TcLauncher {
             cfg.numAttrs = 1;
         }
         if (grid_out) *grid_out = grid;
-        return cudaLaunchKernelEx(&cfg, gemm_tn_tc_kernel<BN, PAIR, STAGES, EPI>, tmA, tmB, tmD, p);
+        return cudaLaunchKernelEx(&cfg, gemm_tn_tc_kernel<BN, PAIR, STAGES, EPI, SK>, tmA, tmB, tmD, p);
     }
 };
 

@@ -15,29 +15,39 @@ bool capacity_family_generic(const TcVariant&, int, int64_t*);
 bool capacity_family_swap(const TcVariant&, int, int64_t*);
 
 static const TcVariant kVariants[] = {
-    {256, 1, 4, EPI_TMA, 0},
-    {256, 2, 6, EPI_TMA, 0},
-    {128, 1, 6, EPI_TMA, 0},
-    {128, 2, 8, EPI_TMA, 0},
-    {256, 1, 4, EPI_GENERIC, 0},
-    {256, 2, 6, EPI_GENERIC, 0},
-    {128, 1, 6, EPI_GENERIC, 0},
-    {128, 1, 6, EPI_PARTIAL, 0},
-    {16, 1, 12, EPI_SWAP, 0},
-    {32, 1, 11, EPI_SWAP, 0},
-    {64, 1, 9, EPI_SWAP, 0},
-    {16, 1, 12, EPI_PARTIAL_SWAP, 0},
-    {32, 1, 11, EPI_PARTIAL_SWAP, 0},
-    {64, 1, 9, EPI_PARTIAL_SWAP, 0},
+    {256, 1, 4, EPI_TMA, 0, 0},
+    {256, 1, 4, EPI_TMA, 1, 0},
+    {256, 2, 6, EPI_TMA, 0, 0},
+    {256, 2, 6, EPI_TMA, 1, 0},
+    {128, 1, 6, EPI_TMA, 0, 0},
+    {128, 1, 6, EPI_TMA, 1, 0},
+    {128, 2, 8, EPI_TMA, 0, 0},
+    {128, 2, 8, EPI_TMA, 1, 0},
+    {256, 1, 4, EPI_GENERIC, 0, 0},
+    {256, 1, 4, EPI_GENERIC, 1, 0},
+    {256, 2, 6, EPI_GENERIC, 0, 0},
+    {256, 2, 6, EPI_GENERIC, 1, 0},
+    {128, 1, 6, EPI_GENERIC, 0, 0},
+    {128, 1, 6, EPI_GENERIC, 1, 0},
+    {128, 1, 6, EPI_PARTIAL, 0, 0},
+    {16, 1, 12, EPI_SWAP, 0, 0},
+    {16, 1, 12, EPI_SWAP, 1, 0},
+    {32, 1, 11, EPI_SWAP, 0, 0},
+    {32, 1, 11, EPI_SWAP, 1, 0},
+    {64, 1, 9, EPI_SWAP, 0, 0},
+    {64, 1, 9, EPI_SWAP, 1, 0},
+    {16, 1, 12, EPI_PARTIAL_SWAP, 0, 0},
+    {32, 1, 11, EPI_PARTIAL_SWAP, 0, 0},
+    {64, 1, 9, EPI_PARTIAL_SWAP, 0, 0},
 };
 
 static_assert(sizeof(kVariants) / sizeof(kVariants[0]) <= kMaxVariants, "variant table too large");
 
-bool find_tc_variant(int bn, int pair, int epi, TcVariant* out) {
+bool find_tc_variant(int bn, int pair, int epi, int sk, TcVariant* out) {
     const int n = static_cast<int>(sizeof(kVariants) / sizeof(kVariants[0]));
     for (int i = 0; i < n; ++i) {
         const TcVariant& v = kVariants[i];
-        if (v.bn == bn && v.pair == pair && v.epi == epi) {
+        if (v.bn == bn && v.pair == pair && v.epi == epi && v.sk == sk) {
             if (out) {
                 *out = v;
                 out->index = i;

@@ -149,6 +149,10 @@ typedef struct {
     int64_t units;           /* work units (tiles x splits x batch) */
     int64_t grid;            /* CTAs launched */
     int64_t workspace_bytes; /* scratch taken from the pool for this call */
+    int32_t stream_k;        /* 1: the last partial wave of tiles is spread over all CTA groups by k-block */
+    int32_t sk_maxc;         /* stream-K: largest number of CTA groups contributing to one tile */
+    int64_t dp_tiles;        /* tiles computed whole (data-parallel), before the stream-K tiles */
+    int64_t sk_tiles;        /* tiles shared out by k-block */
 } gemm_tn_plan_t;
 
 GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int64_t batch,
@@ -170,6 +174,11 @@ GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int6
  *   GEMM_TN_OPT_FORCE_SWAP        force operand swapping off (-1) or on (1), 0 = automatic.
  *   GEMM_TN_OPT_FORCE_GENERIC_EPI 1: never use the TMA-store epilogue.
  *   GEMM_TN_OPT_FORCE_PACK        1: repack A and B through scratch even when aligned.
+ *   GEMM_TN_OPT_STREAM_K          0 (default): spread the k-blocks of the tiles of a partial
+ *                                 last wave over all CTA groups when whole tiles would use
+ *                                 under 90% (TMA-store epilogue) or 60% (predicated
+ *                                 epilogue) of the machine; 1: whenever the tiles do not
+ *                                 divide evenly; -1: never.
  * A forced setting that no compiled kernel supports for a problem is ignored.
  * Returns GEMM_ERR_INVALID_VALUE for an unknown option or an out-of-range value.
  */
@@ -181,7 +190,8 @@ enum {
     GEMM_TN_OPT_FORCE_SPLITS = 5,
     GEMM_TN_OPT_FORCE_SWAP = 6,
     GEMM_TN_OPT_FORCE_GENERIC_EPI = 7,
-    GEMM_TN_OPT_FORCE_PACK = 8
+    GEMM_TN_OPT_FORCE_PACK = 8,
+    GEMM_TN_OPT_STREAM_K = 9
 };
 GEMM_TN_API gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value);
 GEMM_TN_API int64_t gemm_tn_f16_get_option(int32_t option);

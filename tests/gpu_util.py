@@ -75,7 +75,8 @@ def options(**kw):
     names = {"force_bn": G.GEMM_TN_OPT_FORCE_BN, "force_pair": G.GEMM_TN_OPT_FORCE_PAIR,
              "force_splits": G.GEMM_TN_OPT_FORCE_SPLITS, "force_swap": G.GEMM_TN_OPT_FORCE_SWAP,
              "force_generic": G.GEMM_TN_OPT_FORCE_GENERIC_EPI, "force_pack": G.GEMM_TN_OPT_FORCE_PACK,
-             "skip_first_load": G.GEMM_TN_OPT_SKIP_FIRST_LOAD, "timeout_ns": G.GEMM_TN_OPT_WAIT_TIMEOUT_NS}
+             "skip_first_load": G.GEMM_TN_OPT_SKIP_FIRST_LOAD, "timeout_ns": G.GEMM_TN_OPT_WAIT_TIMEOUT_NS,
+             "stream_k": G.GEMM_TN_OPT_STREAM_K}
     old = {k: G.gemm_tn_f16_get_option(names[k]) for k in kw}
     try:
         for k, v in kw.items():

@@ -104,18 +104,54 @@ def plan(M, N, K, batch=1, lda=None, ldb=None, ldc=None, ldd=None, sA=0, sB=0, s
 
 
 def test_plan_large_square_uses_cta_pairs_and_tma_store():
-    p = plan(8192, 8192, 8192)
+    p = plan(8192, 8192, 8192, sms=152)
     assert p["kernel"] == 2 and p["cta_pair"] == 2 and p["tile_m"] == 256 and p["tile_n"] == 256
     assert p["epi_tma"] == 1 and p["splits"] == 1 and p["pack_a"] == 0 and p["pack_b"] == 0
-    assert p["units"] == 32 * 32 and p["grid"] == 148
-    assert p["workspace_bytes"] == 0
+    # 1024 tiles over 76 pairs = 13.5 waves: well filled, so data-parallel only by default
+    assert p["stream_k"] == 0 and p["units"] == 1024 and p["grid"] == 152 and p["workspace_bytes"] == 0
 
 
-def test_plan_skinny_m_swaps_and_splits_k():
+def test_plan_forced_stream_k_splits_the_partial_wave():
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 1)
+    try:
+        p = plan(8192, 8192, 8192, sms=152)
+        q = plan(8192, 8192, 8192, sms=128)  # 16 whole waves over 64 pairs: nothing to split
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 0)
+    # 13 whole waves run data-parallel, the remaining tiles are shared by k-block
+    assert p["stream_k"] == 1 and p["dp_tiles"] == 13 * 76 and p["sk_tiles"] == 1024 - 13 * 76
+    assert p["grid"] == 152 and p["units"] == 13 * 76
+    assert q["stream_k"] == 0 and q["units"] == 1024
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, -1)
+    try:
+        assert plan(16, 8192, 8192)["stream_k"] == 0
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 0)
+
+
+def test_plan_skinny_m_swaps_and_streams_k():
     p = plan(16, 8192, 8192)
-    assert p["kernel"] == 3 and p["swap_ab"] == 1 and p["tile_n"] == 16 and p["splits"] >= 2
-    assert p["units"] == 64 * p["splits"]
-    assert p["workspace_bytes"] >= p["splits"] * 16 * 8192 * 4
+    assert p["kernel"] == 2 and p["swap_ab"] == 1 and p["tile_n"] == 16 and p["splits"] == 1
+    assert p["stream_k"] == 1 and p["dp_tiles"] == 0 and p["sk_tiles"] == 64 and p["grid"] == 148
+    assert 2 <= p["sk_maxc"] <= 4
+    assert p["workspace_bytes"] >= 64 * p["sk_maxc"] * 128 * 16 * 4
+
+
+def test_plan_stream_k_needs_one_iteration_per_group():
+    p = plan(128, 128, 512)  # one tile, 8 k-blocks: only 8 groups take part
+    assert p["stream_k"] == 1 and p["grid"] == 8 and p["sk_maxc"] == 8
+    p = plan(128, 128, 448)  # 7 k-blocks: too few to share out
+    assert p["stream_k"] == 0 and p["grid"] == 1
+
+
+def test_plan_forced_splits_use_the_reduction_kernel():
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_SPLITS, 4)
+    try:
+        p = plan(16, 8192, 8192)
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_SPLITS, 0)
+    assert p["kernel"] == 3 and p["splits"] == 4 and p["stream_k"] == 0
+    assert p["workspace_bytes"] >= 4 * 16 * 8192 * 4
 
 
 def test_plan_ragged_packed_ld_repacks_operands():
@@ -140,10 +176,12 @@ def test_plan_k_zero_and_empty():
     assert plan(0, 8, 8)["kernel"] == 0
 
 
-def test_plan_splits_cover_k():
-    for K in (512, 1000, 4096, 65536):
-        p = plan(16, 1024, K)
-        assert 1 <= p["splits"] <= max(1, (K + 63) // 64)
+def test_plan_stream_k_grid_never_exceeds_iterations():
+    for M, N, K in ((16, 1024, 512), (16, 1024, 1000), (300, 300, 4096), (1000, 1000, 65536)):
+        p = plan(M, N, K)
+        if p["stream_k"]:
+            tiles = p["dp_tiles"] + p["sk_tiles"]
+            assert p["grid"] // p["cta_pair"] <= tiles * ((K + 63) // 64)
 
 
 def test_options_roundtrip_and_validation():

@@ -52,6 +52,17 @@ CASES = [
     ("batched_pair", dict(M=520, N=520, K=600, batch=2, opts=dict(force_pair=2, force_bn=256))),
     ("batched_swap", dict(M=16, N=300, K=128, batch=3)),
     ("batched_short_k_normal", dict(M=512, N=512, K=64, batch=4, alpha=0.125, dist="normal")),
+    # stream-K: the k-blocks of the tiles that do not fill a whole wave are spread over all CTA groups
+    ("streamk_pair_no_dp_wave", dict(M=1280, N=1280, K=1024)),
+    ("streamk_pair_dp_plus_sk", dict(M=2560, N=2560, K=512, opts=dict(stream_k=1))),
+    ("streamk_pair_generic_forced", dict(M=2000, N=1800, K=900, alpha=0.5, beta=1.5,
+                                         opts=dict(stream_k=1, force_pair=2, force_bn=256))),
+    ("streamk_single_tma_forced", dict(M=1100, N=1032, K=1000, opts=dict(stream_k=1, force_pair=1))),
+    ("streamk_pair_generic_beta", dict(M=1290, N=1288, K=1000, alpha=0.5, beta=1.5)),
+    ("streamk_single_packed_beta", dict(M=1500, N=1100, K=700, alpha=0.5, beta=1.5)),
+    ("streamk_swap_skinny", dict(M=16, N=1024, K=4096)),
+    ("streamk_swap_beta", dict(M=40, N=2000, K=1000, alpha=0.5, beta=1.5)),
+    ("streamk_batched", dict(M=600, N=600, K=640, batch=3)),
 ]
 
 
@@ -67,6 +78,8 @@ EXACT = [
     ("exact_swap", dict(M=16, N=600, K=256)),
     ("exact_splitk", dict(M=16, N=256, K=256, opts=dict(force_splits=4))),
     ("exact_packed", dict(M=129, N=131, K=255)),
+    ("exact_streamk_pair", dict(M=2560, N=2304, K=512, opts=dict(stream_k=1))),
+    ("exact_streamk_swap", dict(M=16, N=1024, K=2048)),
 ]
 
 
