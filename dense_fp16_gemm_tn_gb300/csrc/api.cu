@@ -231,14 +231,14 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
     pub.sk_tiles = 0;
     pl.sk_iters = 0;
     pl.sk_w_bytes = pl.sk_ctr_bytes = 0;
-    const bool sk_epi = pl.epi == EPI_TMA || pl.epi == EPI_GENERIC || pl.epi == EPI_SWAP;
+    const bool sk_epi = pl.epi == EPI_TMA || pl.epi == EPI_TMA_C || pl.epi == EPI_GENERIC || pl.epi == EPI_SWAP;
     // Automatic stream-K when whole tiles would leave much of the machine idle.  At
     // full occupancy the GEMM runs at the power limit, so a partly empty last wave
     // costs less than its share; with the TMA epilogue the fixup is cheap enough
     // to pay from 10% idle, with the predicated one only from 40%.  Forced on, it
     // applies whenever the tiles do not divide evenly.
     const int64_t mode = g_opt_stream_k.load();
-    const double threshold = mode > 0 ? 1.0 : (pl.epi == EPI_TMA ? 0.9 : 0.6);
+    const double threshold = mode > 0 ? 1.0 : ((pl.epi == EPI_TMA || pl.epi == EPI_TMA_C) ? 0.9 : 0.6);
     if (mode >= 0 && sk_epi && pub.splits == 1 && kb >= 8 && tiles % G != 0) {
         const double dp_eff = static_cast<double>(tiles) / static_cast<double>(ceil_div(tiles, G) * G);
         // Every group must get at least one iteration (contributors to a tile are
@@ -286,6 +286,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     pub.pack_a = (force_pack || !operand_tma_ok(pr.align & 1u, pr.lda, pr.sA, pr.batch)) ? 1 : 0;
     pub.pack_b = (force_pack || !operand_tma_ok(pr.align & 2u, pr.ldb, pr.sB, pr.batch)) ? 1 : 0;
     const bool d_ok = operand_tma_ok(pr.align & 8u, pr.ldd, pr.sD, pr.batch);
+    const bool c_ok = pr.beta == 0.0f || operand_tma_ok(pr.align & 4u, pr.ldc, pr.sC, pr.batch);
 
     // Small M: swap operands so that the long N side fills the 128 tensor-memory lanes.
     bool swap = pr.M <= 64 && pr.N >= 128 && pr.N >= 2 * pr.M;
@@ -334,7 +335,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     int epi;
     if (splits > 1) epi = swap ? EPI_PARTIAL_SWAP : EPI_PARTIAL;
     else if (swap) epi = EPI_SWAP;
-    else if (pr.beta == 0.0f && d_ok && g_opt_force_generic.load() == 0) epi = EPI_TMA;
+    else if (d_ok && c_ok && g_opt_force_generic.load() == 0) epi = pr.beta == 0.0f ? EPI_TMA : EPI_TMA_C;
     else epi = EPI_GENERIC;
 
     TcVariant v;
@@ -361,7 +362,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     pub.swap_ab = swap ? 1 : 0;
     pub.splits = splits;
     pub.stages = v.stages;
-    pub.epi_tma = epi == EPI_TMA ? 1 : 0;
+    pub.epi_tma = (epi == EPI_TMA || epi == EPI_TMA_C) ? 1 : 0;
 
     pl.ldo_a = round_up(pr.K, 8);
     pl.ldo_b = round_up(pr.K, 8);
@@ -428,7 +429,8 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     // Tensor maps first: an operand whose map the driver rejects is repacked instead.
     const bool swap = pl.pub.swap_ab != 0;
     const uint32_t box_rows_b = static_cast<uint32_t>(pl.var.bn / pl.var.pair);
-    CUtensorMap mapA_op, mapB_op, mapD;
+    CUtensorMap mapA_op, mapB_op, mapC, mapD;
+    std::memset(&mapC, 0, sizeof(mapC));
     std::memset(&mapD, 0, sizeof(mapD));
     // Problem operand A is the MMA's B operand when swapped, else its A operand.
     const uint32_t boxA = swap ? box_rows_b : 128u;
@@ -438,8 +440,10 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
         pl.pub.pack_a = 1, pl.pack_a_bytes = round_up(((p.batch > 1 && p.sA != 0) ? p.batch : 1) * p.M * pl.ldo_a * 2, 256);
     if (!pl.pub.pack_b && !encode_map(&mapPB, B, p.K, p.N, p.batch, p.ldb, p.sB, p.batch > 1 && p.sB != 0, 64, boxB))
         pl.pub.pack_b = 1, pl.pack_b_bytes = round_up(((p.batch > 1 && p.sB != 0) ? p.batch : 1) * p.N * pl.ldo_b * 2, 256);
-    if (pl.epi == EPI_TMA &&
-        !encode_map(&mapD, D, p.N, p.M, p.batch, p.ldd, p.sD, p.batch > 1, 64, 32)) {
+    if ((pl.epi == EPI_TMA || pl.epi == EPI_TMA_C) &&
+        (!encode_map(&mapD, D, p.N, p.M, p.batch, p.ldd, p.sD, p.batch > 1, 64, 32) ||
+         (pl.epi == EPI_TMA_C &&
+          !encode_map(&mapC, C, p.N, p.M, p.batch, p.ldc, p.sC, p.batch > 1 && p.sC != 0, 64, 32)))) {
         TcVariant v;
         if (find_tc_variant(pl.var.bn, pl.var.pair, EPI_GENERIC, 0, &v)) {
             pl.var = v;
@@ -473,10 +477,11 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
 
     const bool a_batched = p.batch > 1 && p.sA != 0;
     const bool b_batched = p.batch > 1 && p.sB != 0;
+    RepackArgs jobs[2];
+    int njobs = 0;
     if (pl.pub.pack_a) {
         void* dst = ws;
-        e = launch_repack(A, p.lda, p.sA, dst, pl.ldo_a, p.M, p.K, a_batched ? p.batch : 1, dev->sms, stream);
-        if (e != cudaSuccess) { release(); return cuda_fail(e); }
+        jobs[njobs++] = {A, p.lda, p.sA, dst, pl.ldo_a, p.M, p.K, a_batched ? p.batch : 1};
         if (!encode_map(&mapPA, dst, p.K, p.M, p.batch, pl.ldo_a, p.M * pl.ldo_a, a_batched, 64, boxA)) {
             release();
             return GEMM_ERR_UNSUPPORTED;
@@ -484,16 +489,20 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     }
     if (pl.pub.pack_b) {
         void* dst = ws + pl.pack_a_bytes;
-        e = launch_repack(B, p.ldb, p.sB, dst, pl.ldo_b, p.N, p.K, b_batched ? p.batch : 1, dev->sms, stream);
-        if (e != cudaSuccess) { release(); return cuda_fail(e); }
+        jobs[njobs++] = {B, p.ldb, p.sB, dst, pl.ldo_b, p.N, p.K, b_batched ? p.batch : 1};
         if (!encode_map(&mapPB, dst, p.K, p.N, p.batch, pl.ldo_b, p.N * pl.ldo_b, b_batched, 64, boxB)) {
             release();
             return GEMM_ERR_UNSUPPORTED;
         }
     }
+    if (njobs > 0) {
+        e = launch_repack(jobs, njobs, dev->sms, stream);
+        if (e != cudaSuccess) { release(); return cuda_fail(e); }
+    }
     mapA_op = swap ? mapPB : mapPA;
     mapB_op = swap ? mapPA : mapPB;
-    if (pl.epi != EPI_TMA) mapD = mapA_op;  // unused by the kernel; any valid map
+    if (pl.epi != EPI_TMA && pl.epi != EPI_TMA_C) mapD = mapA_op;  // unused by the kernel; any valid map
+    if (pl.epi != EPI_TMA_C) mapC = mapD;
 
     KParams kp;
     std::memset(&kp, 0, sizeof(kp));
@@ -508,6 +517,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     kp.group_m = pl.group_m;
     kp.zA = swap ? (b_batched ? 1 : 0) : (a_batched ? 1 : 0);
     kp.zB = swap ? (a_batched ? 1 : 0) : (b_batched ? 1 : 0);
+    kp.zC = (p.batch > 1 && p.sC != 0) ? 1 : 0;
     kp.zD = p.batch > 1 ? 1 : 0;
     kp.num_units = pl.pub.units;
     kp.M = static_cast<int32_t>(p.M);
@@ -535,7 +545,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
         if (e != cudaSuccess) { release(); return cuda_fail(e); }
     }
     int64_t grid = 0;
-    e = launch_tc_variant(pl.var, mapA_op, mapB_op, mapD, kp, pl.pub.grid, stream, &grid);
+    e = launch_tc_variant(pl.var, mapA_op, mapB_op, mapC, mapD, kp, pl.pub.grid, stream, &grid);
     if (e != cudaSuccess) { release(); return cuda_fail(e); }
     if (pl.pub.splits > 1) {
         e = launch_splitk_reduce(kp.W, pl.pub.splits, p.M, p.N, p.batch, alpha, p.beta, C, p.ldc, p.sC, D, p.ldd,

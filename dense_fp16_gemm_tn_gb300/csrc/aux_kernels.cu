@@ -17,25 +17,90 @@
 
 namespace gtn {
 
-// dst[b][r][0..ldo) = src[b][r][0..K) followed by zeros; ldo % 8 == 0 and dst 16-byte aligned.
-// One thread writes one 16-byte group of 8 halves.
-__global__ void repack_rows_kernel(const __half* __restrict__ src, int64_t ld_src, int64_t stride_src,
-                                   __half* __restrict__ dst, int64_t ldo, int64_t rows, int64_t K,
-                                   int64_t batch) {
-    const int64_t groups_per_row = ldo / 8;
-    const int64_t total = batch * rows * groups_per_row;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t g = i % groups_per_row;
-        const int64_t rb = i / groups_per_row;  // b * rows + r
-        const int64_t r = rb % rows;
-        const int64_t b = rb / rows;
-        const __half* s = src + b * stride_src + r * ld_src;
-        const int64_t k0 = g * 8;
-        alignas(16) __half v[8];
+struct RepackJob {
+    const __half* src;
+    int64_t ld_src, stride_src;
+    __half* dst;
+    int64_t ldo, rows, K, batch;
+};
+
+// The 16 bytes starting `shift` bytes (even, 0..14) into the 32-byte window w0..w7.
+// `shift` is the same for every group of a row, so the switch does not diverge.
+__device__ __forceinline__ uint4 window16(const uint32_t (&w)[8], uint32_t shift) {
+    const bool half = (shift & 2u) != 0;
+    auto f = [&](uint32_t lo, uint32_t hi) { return half ? __funnelshift_r(lo, hi, 16) : lo; };
+    switch (shift >> 2) {
+        case 0: return make_uint4(f(w[0], w[1]), f(w[1], w[2]), f(w[2], w[3]), f(w[3], w[4]));
+        case 1: return make_uint4(f(w[1], w[2]), f(w[2], w[3]), f(w[3], w[4]), f(w[4], w[5]));
+        case 2: return make_uint4(f(w[2], w[3]), f(w[3], w[4]), f(w[4], w[5]), f(w[5], w[6]));
+        default: return make_uint4(f(w[3], w[4]), f(w[4], w[5]), f(w[5], w[6]), f(w[6], w[7]));
+    }
+}
+
+// dst[b][r][0..ldo) = src[b][r][0..K) followed by zeros, for up to two operands in one
+// launch; ldo % 8 == 0 and dst 16-byte aligned.  A thread writes 16-byte groups of 8
+// halves.  Their source halves start at any 2-byte boundary: the thread loads the
+// aligned 16-byte block holding the first one and, when the group straddles into the
+// next block and that block holds a half of the row, that block too, then shifts
+// the 32-byte window into place.  No load leaves the blocks that hold row data.
+// One row per block iteration (row index arithmetic once per row); each thread
+// keeps two groups in flight.
+__global__ void repack_rows_kernel(RepackJob j0, RepackJob j1) {
+    const int64_t rows0 = j0.batch * j0.rows;
+    const int64_t rows_total = rows0 + j1.batch * j1.rows;
+    for (int64_t row = blockIdx.x; row < rows_total; row += gridDim.x) {
+        const bool second = row >= rows0;
+        const RepackJob& jb = second ? j1 : j0;
+        const int64_t rb = second ? row - rows0 : row;  // b * rows + r
+        const int64_t b = rb / jb.rows;
+        const int64_t r = rb - b * jb.rows;
+        const __half* src_row = jb.src + b * jb.stride_src + r * jb.ld_src;
+        __half* dst_row = jb.dst + rb * jb.ldo;
+        const int32_t groups = static_cast<int32_t>(jb.ldo / 8);
+        const int32_t K = static_cast<int32_t>(jb.K);
+        const uint32_t shift = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src_row) & 15u);  // bytes, even
+        const uint4* row_blk = reinterpret_cast<const uint4*>(reinterpret_cast<uintptr_t>(src_row) - shift);
+        for (int32_t g0 = threadIdx.x; g0 < groups; g0 += 2 * blockDim.x) {
+            uint32_t w[2][8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = (k0 + j < K) ? s[k0 + j] : __ushort_as_half(0);
-        *reinterpret_cast<uint4*>(dst + rb * ldo + k0) = *reinterpret_cast<const uint4*>(v);
+            for (int u = 0; u < 2; ++u) {
+                const int32_t g = g0 + u * blockDim.x;
+                const int32_t k0 = g * 8;
+#pragma unroll
+                for (int t = 0; t < 8; ++t) w[u][t] = 0;
+                if (g < groups && k0 < K) {
+                    const uint4 v0 = __ldg(row_blk + g);
+                    w[u][0] = v0.x; w[u][1] = v0.y; w[u][2] = v0.z; w[u][3] = v0.w;
+                    // first half held by the next block: element k0 + (16 - shift) / 2
+                    if (shift != 0 && k0 + static_cast<int32_t>((16u - shift) / 2u) < K) {
+                        const uint4 v1 = __ldg(row_blk + g + 1);
+                        w[u][4] = v1.x; w[u][5] = v1.y; w[u][6] = v1.z; w[u][7] = v1.w;
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int32_t g = g0 + u * blockDim.x;
+                if (g >= groups) break;
+                const int32_t k0 = g * 8;
+                uint4 out = make_uint4(0, 0, 0, 0);
+                if (k0 < K) {
+                    out = window16(w[u], shift);
+                    // zero the halves past the end of the row
+                    const int32_t valid = K - k0;
+                    if (valid < 8) {
+                        uint32_t o[4] = {out.x, out.y, out.z, out.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            if (2 * t >= valid) o[t] = 0;
+                            else if (2 * t + 1 >= valid) o[t] &= 0xFFFFu;
+                        }
+                        out = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+                *reinterpret_cast<uint4*>(dst_row + k0) = out;
+            }
+        }
     }
 }
 
@@ -85,11 +150,18 @@ static int grid_for(int64_t total, int threads, int sms) {
     return static_cast<int>(blocks);
 }
 
-cudaError_t launch_repack(const void* src, int64_t ld_src, int64_t stride_src, void* dst, int64_t ldo, int64_t rows,
-                          int64_t K, int64_t batch, int sms, cudaStream_t stream) {
-    const int64_t total = batch * rows * (ldo / 8);
-    repack_rows_kernel<<<grid_for(total, 256, sms), 256, 0, stream>>>(
-        static_cast<const __half*>(src), ld_src, stride_src, static_cast<__half*>(dst), ldo, rows, K, batch);
+cudaError_t launch_repack(const RepackArgs* ops, int count, int sms, cudaStream_t stream) {
+    RepackJob jobs[2] = {};
+    for (int i = 0; i < count && i < 2; ++i) {
+        const RepackArgs& o = ops[i];
+        jobs[i] = {static_cast<const __half*>(o.src), o.ld_src, o.stride_src, static_cast<__half*>(o.dst),
+                   o.ldo, o.rows, o.K, o.batch};
+    }
+    const int64_t rows = jobs[0].batch * jobs[0].rows + jobs[1].batch * jobs[1].rows;
+    if (rows == 0) return cudaSuccess;
+    // one 256-thread block per row (enough for a 2048-half row in one pass), 8 per SM
+    int64_t blocks = rows < static_cast<int64_t>(sms) * 8 ? rows : static_cast<int64_t>(sms) * 8;
+    repack_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(jobs[0], jobs[1]);
     return cudaGetLastError();
 }
 

@@ -28,8 +28,8 @@ bool find_tc_variant(int bn, int pair, int epi, int sk, TcVariant* out);
 // Launches a tensor-core variant with a persistent grid of at most `max_ctas`
 // CTAs (rounded to whole CTA pairs).  *grid_out receives the grid used.
 cudaError_t launch_tc_variant(const TcVariant& v, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                              const CUtensorMap& tmD, const KParams& p, int64_t max_ctas, cudaStream_t stream,
-                              int64_t* grid_out);
+                              const CUtensorMap& tmC, const CUtensorMap& tmD, const KParams& p, int64_t max_ctas,
+                              cudaStream_t stream, int64_t* grid_out);
 
 // Largest number of CTAs of variant v that can be resident at once on the current device.
 int64_t tc_variant_capacity(const TcVariant& v, int sms);
@@ -37,8 +37,15 @@ int64_t tc_variant_capacity(const TcVariant& v, int sms);
 // Device address of the library's error word on the current device.
 cudaError_t error_word_address(uint32_t** out);
 
-cudaError_t launch_repack(const void* src, int64_t ld_src, int64_t stride_src, void* dst, int64_t ldo, int64_t rows,
-                          int64_t K, int64_t batch, int sms, cudaStream_t stream);
+// One operand to copy into a dense scratch copy whose leading dimension ldo is a multiple of 8.
+struct RepackArgs {
+    const void* src;
+    int64_t ld_src, stride_src;
+    void* dst;
+    int64_t ldo, rows, K, batch;
+};
+// Repacks up to two operands in one launch.
+cudaError_t launch_repack(const RepackArgs* ops, int count, int sms, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float* W, int32_t splits, int64_t M, int64_t N, int64_t batch, float alpha,
                                  float beta, const void* C, int64_t ldc, int64_t strideC, void* D, int64_t ldd,
                                  int64_t strideD, int sms, cudaStream_t stream);

@@ -3,12 +3,12 @@
 
 namespace gtn {
 
-bool launch_family_generic(const TcVariant& v, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
-                          const KParams& p, int64_t max_ctas, cudaStream_t stream, int64_t* grid_out,
+bool launch_family_generic(const TcVariant& v, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                          const CUtensorMap& tmD, const KParams& p, int64_t max_ctas, cudaStream_t stream, int64_t* grid_out,
                           cudaError_t* err) {
 #define GTN_CASE(BN, PAIR, ST, EPI, SK)                                                                    \
     if (v.bn == BN && v.pair == PAIR && v.stages == ST && v.epi == EPI && v.sk == SK) {                             \
-        *err = TcLauncher<BN, PAIR, ST, EPI, SK>::launch(tmA, tmB, tmD, p, max_ctas, stream, grid_out);   \
+        *err = TcLauncher<BN, PAIR, ST, EPI, SK>::launch(tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out);   \
         return true;                                                                                  \
     }
     GTN_CASE(256, 1, 4, EPI_GENERIC, 0)

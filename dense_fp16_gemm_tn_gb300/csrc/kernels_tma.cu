@@ -1,24 +1,32 @@
-// Variants whose epilogue writes D with TMA stores (beta == 0, aligned D).
+// Variants whose epilogue writes D with TMA stores (aligned D; with EPI_TMA_C, C is read by TMA too).
 #include "tc_launch.cuh"
 
 namespace gtn {
 
-bool launch_family_tma(const TcVariant& v, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
-                          const KParams& p, int64_t max_ctas, cudaStream_t stream, int64_t* grid_out,
+bool launch_family_tma(const TcVariant& v, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                          const CUtensorMap& tmD, const KParams& p, int64_t max_ctas, cudaStream_t stream, int64_t* grid_out,
                           cudaError_t* err) {
 #define GTN_CASE(BN, PAIR, ST, EPI, SK)                                                                    \
     if (v.bn == BN && v.pair == PAIR && v.stages == ST && v.epi == EPI && v.sk == SK) {                             \
-        *err = TcLauncher<BN, PAIR, ST, EPI, SK>::launch(tmA, tmB, tmD, p, max_ctas, stream, grid_out);   \
+        *err = TcLauncher<BN, PAIR, ST, EPI, SK>::launch(tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out);   \
         return true;                                                                                  \
     }
     GTN_CASE(256, 1, 4, EPI_TMA, 0)
+    GTN_CASE(256, 1, 4, EPI_TMA_C, 0)
     GTN_CASE(256, 1, 4, EPI_TMA, 1)
+    GTN_CASE(256, 1, 4, EPI_TMA_C, 1)
     GTN_CASE(256, 2, 6, EPI_TMA, 0)
+    GTN_CASE(256, 2, 6, EPI_TMA_C, 0)
     GTN_CASE(256, 2, 6, EPI_TMA, 1)
+    GTN_CASE(256, 2, 6, EPI_TMA_C, 1)
     GTN_CASE(128, 1, 6, EPI_TMA, 0)
+    GTN_CASE(128, 1, 6, EPI_TMA_C, 0)
     GTN_CASE(128, 1, 6, EPI_TMA, 1)
+    GTN_CASE(128, 1, 6, EPI_TMA_C, 1)
     GTN_CASE(128, 2, 8, EPI_TMA, 0)
+    GTN_CASE(128, 2, 8, EPI_TMA_C, 0)
     GTN_CASE(128, 2, 8, EPI_TMA, 1)
+    GTN_CASE(128, 2, 8, EPI_TMA_C, 1)
 #undef GTN_CASE
     return false;
 }
@@ -30,13 +38,21 @@ bool capacity_family_tma(const TcVariant& v, int sms, int64_t* cap) {
         return true;                                                        \
     }
     GTN_CASE(256, 1, 4, EPI_TMA, 0)
+    GTN_CASE(256, 1, 4, EPI_TMA_C, 0)
     GTN_CASE(256, 1, 4, EPI_TMA, 1)
+    GTN_CASE(256, 1, 4, EPI_TMA_C, 1)
     GTN_CASE(256, 2, 6, EPI_TMA, 0)
+    GTN_CASE(256, 2, 6, EPI_TMA_C, 0)
     GTN_CASE(256, 2, 6, EPI_TMA, 1)
+    GTN_CASE(256, 2, 6, EPI_TMA_C, 1)
     GTN_CASE(128, 1, 6, EPI_TMA, 0)
+    GTN_CASE(128, 1, 6, EPI_TMA_C, 0)
     GTN_CASE(128, 1, 6, EPI_TMA, 1)
+    GTN_CASE(128, 1, 6, EPI_TMA_C, 1)
     GTN_CASE(128, 2, 8, EPI_TMA, 0)
+    GTN_CASE(128, 2, 8, EPI_TMA_C, 0)
     GTN_CASE(128, 2, 8, EPI_TMA, 1)
+    GTN_CASE(128, 2, 8, EPI_TMA_C, 1)
 #undef GTN_CASE
     return false;
 }

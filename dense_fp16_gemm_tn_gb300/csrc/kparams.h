@@ -11,6 +11,7 @@ enum EpiMode : int {
     EPI_SWAP = 2,          // same, accumulator holds D^T (swapped operands)
     EPI_PARTIAL = 3,       // fp32 partial sums of one K slice -> workspace
     EPI_PARTIAL_SWAP = 4,  // same, accumulator holds D^T
+    EPI_TMA_C = 5,         // D = alpha*acc + beta*C, C loaded and D stored by TMA (aligned C and D)
 };
 
 struct KParams {
@@ -20,7 +21,7 @@ struct KParams {
     int32_t splits;            // K slices per tile
     int32_t kb_total;          // number of 64-wide k-blocks, ceil(K/64)
     int32_t group_m;           // rasterisation group size along the tile rows
-    int32_t zA, zB, zD;        // batch coordinate multipliers (0 = operand not batched)
+    int32_t zA, zB, zC, zD;    // batch coordinate multipliers (0 = operand not batched)
     int64_t num_units;         // data-parallel units: whole tiles, or (tile, K slice) pairs when splits > 1
     // Problem view, for the epilogue.
     int32_t M, N;

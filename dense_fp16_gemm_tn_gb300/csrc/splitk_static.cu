@@ -197,7 +197,7 @@ extern "C" GEMM_TN_API gemm_status_t gemm_tn_f16_splitk_static(const void* A, in
     kp.timeout_ns = 2000000000ull;
 
     int64_t grid = 0;
-    if (launch_tc_variant(v, mapA, mapB, mapA, kp, dev->sms, stream, &grid) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (launch_tc_variant(v, mapA, mapB, mapA, mapA, kp, dev->sms, stream, &grid) != cudaSuccess) return GEMM_ERR_CUDA;
     if (launch_splitk_reduce(dev->scratch, static_cast<int32_t>(s), M, N, 1, alpha, beta, C, ldc, 0, D, ldd, 0,
                              dev->sms, stream) != cudaSuccess)
         return GEMM_ERR_CUDA;

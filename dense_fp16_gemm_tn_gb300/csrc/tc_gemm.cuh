@@ -68,12 +68,12 @@ struct TileCfg {
     static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
     static constexpr int EPI_WARP_BYTES =
-        (EPI == EPI_TMA) ? 2 * 32 * 128 : (EPI == EPI_GENERIC || EPI == EPI_PARTIAL) ? 32 * 33 * 4 : 0;
+        (EPI == EPI_TMA || EPI == EPI_TMA_C) ? 2 * 32 * 128 : (EPI == EPI_GENERIC || EPI == EPI_PARTIAL) ? 32 * 33 * 4 : 0;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
     static constexpr int OFF_BAR = OFF_EPI + ((EPI_WARPS * EPI_WARP_BYTES + 1023) / 1024) * 1024;
-    static constexpr int NUM_BARS = 2 * STAGES + 4;
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + (EPI == EPI_TMA_C ? 2 * EPI_WARPS : 0);  // + C-load barriers
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
     static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;  // + slack to align the base to 1024
@@ -81,7 +81,7 @@ struct TileCfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N in [16,256], N%16==0");
     static_assert(BN_LOCAL % 8 == 0, "B tile must hold whole 8-row swizzle atoms");
     static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "tiles must stay 1024-byte aligned");
-    static_assert(EPI != EPI_TMA || BN % 64 == 0, "TMA epilogue stores 64-column chunks");
+    static_assert((EPI != EPI_TMA && EPI != EPI_TMA_C) || BN % 64 == 0, "TMA epilogue stores 64-column chunks");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory per CTA");
     static_assert(PAIR == 1 || PAIR == 2, "CTA pair or single CTA");
 };
@@ -220,7 +220,8 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 template <int BN, int PAIR, int STAGES, int EPI, bool SK>
 __global__ void __launch_bounds__(TileCfg<BN, PAIR, STAGES, EPI>::THREADS, 1)
 gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const __grid_constant__ CUtensorMap tmD, const KParams p) {
+                  const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
+                  const KParams p) {
     using Cfg = TileCfg<BN, PAIR, STAGES, EPI>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -232,6 +233,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+    // C tile loads of the TMA epilogue: buffer b of epilogue warp ew.
+    auto cload_bar = [&](int ew, int b) { return bar0 + 8u * (2 * STAGES + 4 + 2 * ew + b); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_TMEM_SLOT);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_ABORT);
 
@@ -250,13 +253,16 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             mbar_init(tfull_bar(a), 1);
             mbar_init(tempty_bar(a), Cfg::EPI_WARPS * PAIR);
         }
+        if constexpr (EPI == EPI_TMA_C)
+            for (int e = 0; e < 2 * Cfg::EPI_WARPS; ++e) mbar_init(cload_bar(e / 2, e % 2), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
-        if constexpr (EPI == EPI_TMA) prefetch_tensormap(&tmD);
+        if constexpr (EPI == EPI_TMA || EPI == EPI_TMA_C) prefetch_tensormap(&tmD);
+        if constexpr (EPI == EPI_TMA_C) prefetch_tensormap(&tmC);
     }
     if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
     tc_fence_before();
@@ -355,6 +361,9 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint32_t acc_phase = 0;
         uint32_t chunk_count = 0;
         const bool use_c = (EPI == EPI_GENERIC || EPI == EPI_SWAP) && p.beta != 0.0f;
+        // TMA epilogue with beta != 0: C boxes are fetched by TMA into the staging buffers.
+        constexpr bool tma_c = EPI == EPI_TMA_C;
+        uint32_t cphase = 0u;  // bit b: parity of the next C load into staging buffer b
         SegIter it = seg_begin<SK>(p, group, ngroups);
         Seg w;
         while (seg_next<SK>(p, it, w)) {
@@ -382,6 +391,25 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             };
             if constexpr (EPI == EPI_GENERIC) {
                 if (use_c && !partial) load_c_chunk(0, cnext);
+            }
+            // TMA epilogue: request the C box (32 rows x 64 columns) of chunk c into staging
+            // buffer b (lane 0 only).
+            auto issue_c = [&](int c, uint32_t b) {
+                const uint32_t cb = cload_bar(ew, static_cast<int>(b));
+                mbar_arrive_expect_tx(cb, 4096u);
+                tma_load_3d(smem_u32(ebuf) + b * 4096u, &tmC, cb, static_cast<int32_t>(acol0 + c * 64),
+                            static_cast<int32_t>(arow0), w.b * p.zC);
+            };
+            // The first chunk's C is requested before the accumulator is ready; the buffer
+            // it lands in was last read by the store issued two chunks ago.
+            auto issue_first_c = [&]() {
+                if (lane == 0) {
+                    bulk_wait_group_read<1>();
+                    issue_c(0, chunk_count & 1u);
+                }
+            };
+            if constexpr (EPI == EPI_TMA_C) {
+                if (!partial) issue_first_c();
             }
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, p.err, p.timeout_ns, abort_flag, 5) ? 1 : 0;
@@ -421,10 +449,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // (stream-K fixup, PARTS) from the sum of the contributors' partials.
             auto emit_tile = [&](auto parts_tag) {
                 constexpr bool PARTS = decltype(parts_tag)::value;
-                if constexpr (EPI == EPI_TMA) {
-#pragma unroll 1
-                    for (int c = 0; c < BN / 64; ++c) {
-                        uint32_t v0[32], v1[32];
+                if constexpr (EPI == EPI_TMA || EPI == EPI_TMA_C) {
+                    auto fetch64 = [&](int c, uint32_t (&v0)[32], uint32_t (&v1)[32]) {
                         if constexpr (!PARTS) {
                             tmem_ld_32x32b_x32(t_row + c * 64, v0);
                             tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
@@ -433,28 +459,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             sum_parts(c * 64, v0);
                             sum_parts(c * 64 + 32, v1);
                         }
-                        const uint32_t buf = chunk_count & 1u;
-                        if (lane == 0) bulk_wait_group_read<1>();
-                        __syncwarp();
-                        const uint32_t sb = smem_u32(ebuf) + buf * 4096u;
-                        const uint32_t row_addr = sb + lane * 128u;
-                        const float al = p.alpha;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
-                                         pack_half2(al * __uint_as_float(v0[8 * j + 0]), al * __uint_as_float(v0[8 * j + 1])),
-                                         pack_half2(al * __uint_as_float(v0[8 * j + 2]), al * __uint_as_float(v0[8 * j + 3])),
-                                         pack_half2(al * __uint_as_float(v0[8 * j + 4]), al * __uint_as_float(v0[8 * j + 5])),
-                                         pack_half2(al * __uint_as_float(v0[8 * j + 6]), al * __uint_as_float(v0[8 * j + 7])));
-                        }
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            st_shared_v4(row_addr + ((static_cast<uint32_t>(j + 4) ^ (lane & 7u)) << 4),
-                                         pack_half2(al * __uint_as_float(v1[8 * j + 0]), al * __uint_as_float(v1[8 * j + 1])),
-                                         pack_half2(al * __uint_as_float(v1[8 * j + 2]), al * __uint_as_float(v1[8 * j + 3])),
-                                         pack_half2(al * __uint_as_float(v1[8 * j + 4]), al * __uint_as_float(v1[8 * j + 5])),
-                                         pack_half2(al * __uint_as_float(v1[8 * j + 6]), al * __uint_as_float(v1[8 * j + 7])));
-                        }
+                    };
+                    auto store_chunk = [&](int c, uint32_t sb) {
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (lane == 0) {
@@ -463,6 +469,80 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             bulk_commit_group();
                         }
                         ++chunk_count;
+                    };
+                    if constexpr (!tma_c) {
+                        // D = alpha * acc
+#pragma unroll 1
+                        for (int c = 0; c < BN / 64; ++c) {
+                            uint32_t v0[32], v1[32];
+                            fetch64(c, v0, v1);
+                            const uint32_t buf = chunk_count & 1u;
+                            if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+                            __syncwarp();
+                            const uint32_t sb = smem_u32(ebuf) + buf * 4096u;
+                            const uint32_t row_addr = sb + lane * 128u;
+                            const float al = p.alpha;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                                             pack_half2(al * __uint_as_float(v0[8 * j + 0]), al * __uint_as_float(v0[8 * j + 1])),
+                                             pack_half2(al * __uint_as_float(v0[8 * j + 2]), al * __uint_as_float(v0[8 * j + 3])),
+                                             pack_half2(al * __uint_as_float(v0[8 * j + 4]), al * __uint_as_float(v0[8 * j + 5])),
+                                             pack_half2(al * __uint_as_float(v0[8 * j + 6]), al * __uint_as_float(v0[8 * j + 7])));
+                            }
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                st_shared_v4(row_addr + ((static_cast<uint32_t>(j + 4) ^ (lane & 7u)) << 4),
+                                             pack_half2(al * __uint_as_float(v1[8 * j + 0]), al * __uint_as_float(v1[8 * j + 1])),
+                                             pack_half2(al * __uint_as_float(v1[8 * j + 2]), al * __uint_as_float(v1[8 * j + 3])),
+                                             pack_half2(al * __uint_as_float(v1[8 * j + 4]), al * __uint_as_float(v1[8 * j + 5])),
+                                             pack_half2(al * __uint_as_float(v1[8 * j + 6]), al * __uint_as_float(v1[8 * j + 7])));
+                            }
+                            store_chunk(c, sb);
+                        }
+                    } else {
+                        // D = alpha * acc + beta * C, C boxes loaded by TMA into the staging buffers
+                        if constexpr (PARTS) issue_first_c();
+#pragma unroll 1
+                        for (int c = 0; c < BN / 64; ++c) {
+                            uint32_t v0[32], v1[32];
+                            fetch64(c, v0, v1);
+                            const uint32_t buf = chunk_count & 1u;
+                            if (lane == 0) {
+                                // the other buffer's store (last chunk) must have read its data
+                                // before the next chunk's C lands there
+                                bulk_wait_group_read<0>();
+                                if (c + 1 < BN / 64) issue_c(c + 1, buf ^ 1u);
+                                wait_bounded(cload_bar(ew, static_cast<int>(buf)), (cphase >> buf) & 1u, p.err,
+                                             p.timeout_ns, abort_flag, 6);
+                            }
+                            cphase ^= 1u << buf;
+                            __syncwarp();
+                            const uint32_t sb = smem_u32(ebuf) + buf * 4096u;
+                            const uint32_t row_addr = sb + lane * 128u;
+                            const float al = p.alpha, be = p.beta;
+                            // alpha * acc + beta * C for 8 columns, rounded once to fp16, in place
+                            auto out8 = [&](const uint32_t* v, uint32_t addr) {
+                                uint32_t cw[4];
+                                ld_shared_v4(addr, cw[0], cw[1], cw[2], cw[3]);
+                                float x[8];
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    const float2 cf = __half22float2(*reinterpret_cast<const __half2*>(&cw[q]));
+                                    x[2 * q] = fmaf(be, cf.x, al * __uint_as_float(v[2 * q]));
+                                    x[2 * q + 1] = fmaf(be, cf.y, al * __uint_as_float(v[2 * q + 1]));
+                                }
+                                st_shared_v4(addr, pack_half2(x[0], x[1]), pack_half2(x[2], x[3]), pack_half2(x[4], x[5]),
+                                             pack_half2(x[6], x[7]));
+                            };
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                out8(v0 + 8 * j, row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4));
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                out8(v1 + 8 * j, row_addr + ((static_cast<uint32_t>(j + 4) ^ (lane & 7u)) << 4));
+                            store_chunk(c, sb);
+                        }
                     }
                 } else if constexpr (EPI == EPI_GENERIC || EPI == EPI_PARTIAL) {
                     // Transpose each 32x32 block through padded shared memory so that a warp
@@ -608,7 +688,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             }
         }
-        if constexpr (EPI == EPI_TMA) {
+        if constexpr (EPI == EPI_TMA || EPI == EPI_TMA_C) {
             if (lane == 0) bulk_wait_group<0>();
             __syncwarp();
         }

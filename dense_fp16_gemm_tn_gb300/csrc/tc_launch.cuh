@@ -57,8 +57,9 @@ struct TcLauncher {
         }
     }
 
-    static cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmD,
-                              const KParams& p, int64_t max_ctas, cudaStream_t stream, int64_t* grid_out) {
+    static cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                              const CUtensorMap& tmD, const KParams& p, int64_t max_ctas, cudaStream_t stream,
+                              int64_t* grid_out) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
         // Data-parallel only: no more CTAs than units.  With a stream-K phase every
@@ -82,7 +83,7 @@ struct TcLauncher {
             cfg.numAttrs = 1;
         }
         if (grid_out) *grid_out = grid;
-        return cudaLaunchKernelEx(&cfg, gemm_tn_tc_kernel<BN, PAIR, STAGES, EPI, SK>, tmA, tmB, tmD, p);
+        return cudaLaunchKernelEx(&cfg, gemm_tn_tc_kernel<BN, PAIR, STAGES, EPI, SK>, tmA, tmB, tmC, tmD, p);
     }
 };
 

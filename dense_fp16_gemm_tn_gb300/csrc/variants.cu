@@ -4,11 +4,11 @@
 
 namespace gtn {
 
-bool launch_family_tma(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KParams&,
+bool launch_family_tma(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KParams&,
                        int64_t, cudaStream_t, int64_t*, cudaError_t*);
-bool launch_family_generic(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+bool launch_family_generic(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                            const KParams&, int64_t, cudaStream_t, int64_t*, cudaError_t*);
-bool launch_family_swap(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KParams&,
+bool launch_family_swap(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KParams&,
                         int64_t, cudaStream_t, int64_t*, cudaError_t*);
 bool capacity_family_tma(const TcVariant&, int, int64_t*);
 bool capacity_family_generic(const TcVariant&, int, int64_t*);
@@ -16,13 +16,21 @@ bool capacity_family_swap(const TcVariant&, int, int64_t*);
 
 static const TcVariant kVariants[] = {
     {256, 1, 4, EPI_TMA, 0, 0},
+    {256, 1, 4, EPI_TMA_C, 0, 0},
     {256, 1, 4, EPI_TMA, 1, 0},
+    {256, 1, 4, EPI_TMA_C, 1, 0},
     {256, 2, 6, EPI_TMA, 0, 0},
+    {256, 2, 6, EPI_TMA_C, 0, 0},
     {256, 2, 6, EPI_TMA, 1, 0},
+    {256, 2, 6, EPI_TMA_C, 1, 0},
     {128, 1, 6, EPI_TMA, 0, 0},
+    {128, 1, 6, EPI_TMA_C, 0, 0},
     {128, 1, 6, EPI_TMA, 1, 0},
+    {128, 1, 6, EPI_TMA_C, 1, 0},
     {128, 2, 8, EPI_TMA, 0, 0},
+    {128, 2, 8, EPI_TMA_C, 0, 0},
     {128, 2, 8, EPI_TMA, 1, 0},
+    {128, 2, 8, EPI_TMA_C, 1, 0},
     {256, 1, 4, EPI_GENERIC, 0, 0},
     {256, 1, 4, EPI_GENERIC, 1, 0},
     {256, 2, 6, EPI_GENERIC, 0, 0},
@@ -59,12 +67,12 @@ bool find_tc_variant(int bn, int pair, int epi, int sk, TcVariant* out) {
 }
 
 cudaError_t launch_tc_variant(const TcVariant& v, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                              const CUtensorMap& tmD, const KParams& p, int64_t max_ctas, cudaStream_t stream,
-                              int64_t* grid_out) {
+                              const CUtensorMap& tmC, const CUtensorMap& tmD, const KParams& p, int64_t max_ctas,
+                              cudaStream_t stream, int64_t* grid_out) {
     cudaError_t e = cudaErrorInvalidValue;
-    if (launch_family_tma(v, tmA, tmB, tmD, p, max_ctas, stream, grid_out, &e)) return e;
-    if (launch_family_generic(v, tmA, tmB, tmD, p, max_ctas, stream, grid_out, &e)) return e;
-    if (launch_family_swap(v, tmA, tmB, tmD, p, max_ctas, stream, grid_out, &e)) return e;
+    if (launch_family_tma(v, tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out, &e)) return e;
+    if (launch_family_generic(v, tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out, &e)) return e;
+    if (launch_family_swap(v, tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out, &e)) return e;
     return cudaErrorInvalidValue;
 }
 

@@ -143,7 +143,7 @@ typedef struct {
     int32_t swap_ab;         /* 1: computes D^T = B . A^T (small M) */
     int32_t splits;          /* K slices (1 = no split) */
     int32_t stages;          /* shared-memory pipeline depth */
-    int32_t epi_tma;         /* 1: D written by tensor stores; 0: plain predicated stores */
+    int32_t epi_tma;         /* 1: D written (and C read, if beta != 0) by tensor copies; 0: plain predicated accesses */
     int32_t pack_a;          /* 1: A is first repacked to an aligned scratch copy */
     int32_t pack_b;          /* 1: B is first repacked */
     int64_t units;           /* work units (tiles x splits x batch) */

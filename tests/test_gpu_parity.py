@@ -27,6 +27,14 @@ CASES = [
     ("generic_beta_bn128", dict(M=300, N=520, K=200, alpha=0.5, beta=1.5, opts=dict(force_bn=128, force_pair=1))),
     ("generic_beta_pair", dict(M=600, N=776, K=520, alpha=0.5, beta=1.5, opts=dict(force_bn=256, force_pair=2))),
     ("generic_forced_beta0", dict(M=260, N=390, K=70, opts=dict(force_generic=1))),
+    # TMA-store epilogue with beta != 0: C tiles fetched by TMA (aligned C)
+    ("tma_beta_single", dict(M=300, N=520, K=200, alpha=0.5, beta=1.5, opts=dict(force_bn=256, force_pair=1))),
+    ("tma_beta_bn128", dict(M=300, N=264, K=130, alpha=-1.0, beta=0.25, opts=dict(force_bn=128, force_pair=1))),
+    ("tma_beta_pair", dict(M=600, N=776, K=520, alpha=0.5, beta=1.5, opts=dict(force_bn=256, force_pair=2))),
+    ("tma_beta_ldc_padded", dict(M=257, N=264, K=96, alpha=0.5, beta=1.5, ldc=272, ldd=280)),
+    ("tma_beta_streamk", dict(M=1280, N=1280, K=1024, alpha=0.5, beta=1.5)),
+    ("tma_beta_batched", dict(M=200, N=136, K=72, batch=3, alpha=0.125, beta=1.0)),
+    ("tma_beta_batched_bcast_c_free", dict(M=256, N=256, K=128, batch=2, beta=-0.5)),
     ("packed_ragged", dict(M=257, N=263, K=129, alpha=0.5, beta=1.5)),
     ("packed_padded_ld", dict(M=200, N=136, K=100, lda=103, ldb=101, ldc=140, ldd=139, beta=-1.0)),
     ("packed_forced", dict(M=256, N=256, K=256, opts=dict(force_pack=1))),
@@ -126,10 +134,12 @@ def test_c_aliases_d():
     B = t.from_numpy(rng.integers(-2, 3, (N, K)).astype(np.float16)).cuda()
     C = t.from_numpy(rng.integers(-4, 5, (M, N)).astype(np.float16)).cuda()
     want = (A.float() @ B.float().T) * 2.0 - C.float()
-    D = C.clone()
-    G.gemm_tn_f16(A, K, B, K, D, N, D, N, M, N, K, 2.0, -1.0)
-    t.cuda.synchronize()
-    assert t.equal(D.float(), want)
+    for opts in ({}, {"force_generic": 1}):  # TMA-loaded C, then predicated loads
+        D = C.clone()
+        with options(**opts):
+            G.gemm_tn_f16(A, K, B, K, D, N, D, N, M, N, K, 2.0, -1.0)
+        t.cuda.synchronize()
+        assert t.equal(D.float(), want)
 
 
 def test_all_ones_closed_form_ragged_workload_shape():
