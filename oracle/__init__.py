@@ -67,6 +67,10 @@ def _bind(path):
                                             i64, ctypes.c_float, ctypes.c_float,
                                             i64p, i64p, i64p, i64, u16p]
     lib.gto_gemm_tn_f16_entries.restype = None
+    lib.gto_gemm_f16_strided.argtypes = [u16p, i64, i64, i64, u16p, i64, i64, i64, u16p, i64, i64,
+                                         u16p, i64, i64, i64, i64, i64,
+                                         ctypes.c_float, ctypes.c_float, i64, i64]
+    lib.gto_gemm_f16_strided.restype = None
     return lib
 
 
@@ -116,6 +120,9 @@ class Oracle:
     def gemm_tn_entries(self, *args, **kw):
         return _gemm_tn_entries(self.lib, *args, **kw)
 
+    def gemm_strided(self, *args, **kw):
+        return _gemm_strided(self.lib, *args, **kw)
+
 
 def _u16ptr(a):
     if a is None:
@@ -138,6 +145,10 @@ def gemm_tn(*args, **kw):
 
 def gemm_tn_entries(*args, **kw):
     return _gemm_tn_entries(_load(), *args, **kw)
+
+
+def gemm_strided(*args, **kw):
+    return _gemm_strided(_load(), *args, **kw)
 
 
 def default_threads() -> int:
@@ -209,3 +220,30 @@ def _gemm_tn_entries(lib, A, B, C, K, alpha, beta, b_idx, m_idx, n_idx, *, lda, 
         with ThreadPoolExecutor(max_workers=nthr) as ex:
             list(ex.map(lambda lo: run(lo, min(count, lo + chunk)), range(0, count, chunk)))
     return out[:count]
+
+
+def _gemm_strided(lib, A, a_strides, B, b_strides, C, M, N, K, alpha, beta, *, ldc=None, ldd=None,
+                  batch=1, strideA=0, strideB=0, strideC=None, strideD=None, D=None, threads=None):
+    """Oracle GEMM with generic element strides: A(m,k) = A[b*strideA + m*a_strides[0] +
+    k*a_strides[1]], B(n,k) likewise; C and D row-major with ldc / ldd."""
+    ldc = N if ldc is None else ldc
+    ldd = N if ldd is None else ldd
+    strideC = M * ldc if strideC is None else strideC
+    strideD = M * ldd if strideD is None else strideD
+    if D is None:
+        D = np.zeros(max(batch * strideD, 1), dtype=np.uint16)
+    rows = batch * M
+    if rows == 0 or N == 0:
+        return D
+    Cp = _u16ptr(C) if beta != 0 else _u16ptr(None)
+    args_pre = (_u16ptr(A), a_strides[0], a_strides[1], strideA, _u16ptr(B), b_strides[0], b_strides[1], strideB,
+                Cp, ldc, strideC, _u16ptr(D), ldd, strideD, M, N, K, float(alpha), float(beta))
+    nthr = default_threads() if threads is None else threads
+    if nthr <= 1 or rows * N * max(K, 1) < (1 << 22):
+        lib.gto_gemm_f16_strided(*args_pre, 0, rows)
+        return D
+    chunk = max(1, (rows + 4 * nthr - 1) // (4 * nthr))
+    spans = [(r, min(rows, r + chunk)) for r in range(0, rows, chunk)]
+    with ThreadPoolExecutor(max_workers=nthr) as ex:
+        list(ex.map(lambda s: lib.gto_gemm_f16_strided(*args_pre, s[0], s[1]), spans))
+    return D

@@ -150,3 +150,32 @@ void gto_gemm_tn_f16_entries(const uint16_t* A, int64_t lda, int64_t strideA,
         out[i] = one_entry(a_row, b_row, K, al, be, c_elem);
     }
 }
+
+/* Generic strides: the k-ordered fp64 sum of A(m,k)*B(n,k), then alpha, beta, RNE. */
+void gto_gemm_f16_strided(const uint16_t* A, int64_t a_rs, int64_t a_cs, int64_t strideA,
+                          const uint16_t* B, int64_t b_rs, int64_t b_cs, int64_t strideB,
+                          const uint16_t* C, int64_t ldc, int64_t strideC,
+                          uint16_t* D, int64_t ldd, int64_t strideD,
+                          int64_t M, int64_t N, int64_t K,
+                          float alpha, float beta,
+                          int64_t r_begin, int64_t r_end)
+{
+    decode_table_init();
+    if (M <= 0 || N <= 0) return;
+    const double al = (double)alpha;
+    const double be = (double)beta;
+    for (int64_t r = r_begin; r < r_end; ++r) {
+        const int64_t b = r / M;
+        const int64_t m = r % M;
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                acc += g_decode[A[b * strideA + m * a_rs + k * a_cs]] *
+                       g_decode[B[b * strideB + n * b_rs + k * b_cs]];
+            }
+            double v = al * acc;
+            if (be != 0.0) v = v + be * g_decode[C[b * strideC + m * ldc + n]];
+            D[b * strideD + m * ldd + n] = gto_double_to_half(v);
+        }
+    }
+}

@@ -70,6 +70,21 @@ void gto_gemm_tn_f16_entries(const uint16_t* A, int64_t lda, int64_t strideA,
                              const int64_t* n_idx, int64_t count,
                              uint16_t* out);
 
+/*
+ * The same definition with generic element strides, as the gemm_device page's
+ * kernel takes them (dA, dB, dC: "CuTe C++ 简介01 / gemm_device 逐行解析",
+ * section 1): A(m,k) = A[b*strideA + m*a_rs + k*a_cs], B(n,k) = B[b*strideB +
+ * n*b_rs + k*b_cs]; C and D are row-major (ldc, ldd) as above.  Rows
+ * r = b*M + m in [r_begin, r_end).
+ */
+void gto_gemm_f16_strided(const uint16_t* A, int64_t a_rs, int64_t a_cs, int64_t strideA,
+                          const uint16_t* B, int64_t b_rs, int64_t b_cs, int64_t strideB,
+                          const uint16_t* C, int64_t ldc, int64_t strideC,
+                          uint16_t* D, int64_t ldd, int64_t strideD,
+                          int64_t M, int64_t N, int64_t K,
+                          float alpha, float beta,
+                          int64_t r_begin, int64_t r_end);
+
 #ifdef __cplusplus
 }
 #endif

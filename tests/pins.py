@@ -317,7 +317,32 @@ def check_degenerate(o):
     assert np.array_equal(bits_to_f64(D).reshape(2, 3), 0.5 * np.arange(6).reshape(2, 3))
 
 
-GEMM_CHECKS = [check_bruteforce_exact, check_identity, check_permutation, check_all_ones,
+def check_strided_layouts(o, seed=14):
+    """Generic strides: with TN strides it is the TN oracle bit for bit; with A or B
+    stored transposed it equals the TN oracle on explicitly transposed copies; small
+    integers give numpy's exact integer matmul for every layout."""
+    rng = np.random.default_rng(seed)
+    M, N, K = 23, 17, 45
+    A = half_bits(rng.uniform(-1, 1, (M, K)))
+    B = half_bits(rng.uniform(-1, 1, (N, K)))
+    C = half_bits(rng.uniform(-1, 1, (M, N)))
+    ref = o.gemm_tn(A, B, C, M, N, K, 0.5, 1.5).reshape(M, N)
+    got = o.gemm_strided(A, (K, 1), B, (K, 1), C, M, N, K, 0.5, 1.5).reshape(M, N)
+    assert np.array_equal(got, ref)
+    At = np.ascontiguousarray(A.T)  # stored K x M (M contiguous)
+    Bt = np.ascontiguousarray(B.T)  # stored K x N
+    for a_store, a_st, b_store, b_st in ((At, (1, M), B, (K, 1)), (A, (K, 1), Bt, (1, N)), (At, (1, M), Bt, (1, N))):
+        got = o.gemm_strided(a_store, a_st, b_store, b_st, C, M, N, K, 0.5, 1.5).reshape(M, N)
+        assert np.array_equal(got, ref)
+    Ai = rng.integers(-2, 3, (M, K)); Bi = rng.integers(-2, 3, (N, K))
+    want = (Ai @ Bi.T).astype(np.float64)
+    for a_store, a_st in ((half_bits(Ai), (K, 1)), (half_bits(np.ascontiguousarray(Ai.T)), (1, M))):
+        for b_store, b_st in ((half_bits(Bi), (K, 1)), (half_bits(np.ascontiguousarray(Bi.T)), (1, N))):
+            got = o.gemm_strided(a_store, a_st, b_store, b_st, None, M, N, K, 1.0, 0.0).reshape(M, N)
+            assert np.array_equal(bits_to_f64(got), want)
+
+
+GEMM_CHECKS = [check_bruteforce_exact, check_strided_layouts, check_identity, check_permutation, check_all_ones,
                check_transpose_invariant, check_small_integers, check_beta_zero_does_not_read_c,
                check_leading_dims, check_batched, check_entries_match_full, check_degenerate]
 CONVERSION_CHECKS = [check_decode_exhaustive, check_encode_specials, check_encode_random_vs_numpy,
