@@ -24,8 +24,9 @@ MUTANTS = [
     ("subnormal_scale", "v = ldexp((double)frac, -24);", "v = ldexp((double)frac, -25);"),
     ("exponent_bias", "expo - 25);", "expo - 24);"),
     ("lost_sign", "return sign ? -v : v;", "return v;"),
-    ("strided_a_axes_swapped", "A[b * strideA + m * a_rs + k * a_cs]", "A[b * strideA + m * a_cs + k * a_rs]"),
-    ("strided_b_row_stride", "B[b * strideB + n * b_rs + k * b_cs]", "B[b * strideB + n * b_cs + k * b_cs]"),
+    # (mutants stay inside the operand buffers: an out-of-range read would be undefined)
+    ("strided_a_unit_k_stride", "A[b * strideA + m * a_rs + k * a_cs]", "A[b * strideA + m * a_rs + k]"),
+    ("strided_b_unit_row_stride", "B[b * strideB + n * b_rs + k * b_cs]", "B[b * strideB + n + k * b_cs]"),
     ("flush_subnormals", "const int q = (E < -14) ? -24 : E - 10;", "const int q = (E < -14) ? 99 : E - 10;"),
 ]
 
