@@ -14,6 +14,8 @@ from ._binding import (  # noqa: F401
     GEMM_ERR_TIMEOUT,
     GEMM_ERR_UNSUPPORTED,
     GEMM_ERR_WORKSPACE,
+    GEMM_K_MAJOR,
+    GEMM_MN_MAJOR,
     GEMM_OK,
     GEMM_TN_OPT_FORCE_BN,
     GEMM_TN_OPT_FORCE_GENERIC_EPI,
@@ -26,6 +28,7 @@ from ._binding import (  # noqa: F401
     GEMM_TN_OPT_WAIT_TIMEOUT_NS,
     GEMM_TN_STATIC_SCRATCH_BYTES,
     GemmError,
+    gemm_f16,
     gemm_status_string,
     gemm_tn_f16,
     gemm_tn_f16_batched,

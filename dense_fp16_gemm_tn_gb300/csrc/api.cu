@@ -182,7 +182,14 @@ struct Problem {
     int64_t sA, sB, sC, sD;
     float beta;
     uint32_t align;  // bit i: operand i (A,B,C,D) base is 16-byte aligned
+    int32_t a_mn = 0, b_mn = 0;  // 1: A stored K x lda (M contiguous) / B stored K x ldb (N contiguous)
 };
+
+// Elements of an operand's rows in memory (its contiguous extent) and their count.
+int64_t a_rows(const Problem& p) { return p.a_mn ? p.K : p.M; }
+int64_t a_len(const Problem& p) { return p.a_mn ? p.M : p.K; }
+int64_t b_rows(const Problem& p) { return p.b_mn ? p.K : p.N; }
+int64_t b_len(const Problem& p) { return p.b_mn ? p.N : p.K; }
 
 struct Plan {
     gemm_tn_plan_t pub;
@@ -207,7 +214,7 @@ gemm_status_t validate(const Problem& p) {
     if (p.M >= lim || p.N >= lim || p.K >= lim || p.batch >= lim) return GEMM_ERR_UNSUPPORTED;
     if (p.M == 0 || p.N == 0 || p.batch == 0) return GEMM_OK;
     if (p.ldd < std::max<int64_t>(p.N, 1)) return GEMM_ERR_INVALID_VALUE;
-    if (p.K > 0 && (p.lda < p.K || p.ldb < p.K)) return GEMM_ERR_INVALID_VALUE;
+    if (p.K > 0 && (p.lda < a_len(p) || p.ldb < b_len(p))) return GEMM_ERR_INVALID_VALUE;
     if (p.beta != 0.0f && p.ldc < std::max<int64_t>(p.N, 1)) return GEMM_ERR_INVALID_VALUE;
     if (p.batch > 1) {
         if (p.sA < 0 || p.sB < 0 || p.sC < 0 || p.sD < 0) return GEMM_ERR_INVALID_VALUE;
@@ -288,11 +295,12 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     const bool d_ok = operand_tma_ok(pr.align & 8u, pr.ldd, pr.sD, pr.batch);
     const bool c_ok = pr.beta == 0.0f || operand_tma_ok(pr.align & 4u, pr.ldc, pr.sC, pr.batch);
 
-    // Small M: swap operands so that the long N side fills the 128 tensor-memory lanes.
+    // Small M: swap operands so that the long N side fills the 128 tensor-memory lanes
+    // (K-major operands only: the swapped kernels have tiles narrower than an MN box).
     bool swap = pr.M <= 64 && pr.N >= 128 && pr.N >= 2 * pr.M;
     const int64_t fs = g_opt_force_swap.load();
     if (fs > 0 && pr.M <= 64) swap = true;
-    if (fs < 0) swap = false;
+    if (fs < 0 || pr.a_mn || pr.b_mn) swap = false;
 
     int bn, pair;
     const int64_t slots = std::max(sms, 1);
@@ -326,7 +334,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     // few tiles is the stream-K split decided in plan_stream_k).
     int splits = 1;
     const int64_t fsplit = g_opt_force_splits.load();
-    if (fsplit >= 1) {
+    if (fsplit >= 1 && !pr.a_mn && !pr.b_mn) {
         pair = 1;
         splits = static_cast<int>(std::min<int64_t>(fsplit, kb));
         if (!swap) bn = 128;  // the partial-sum variant exists at 128 columns
@@ -364,12 +372,12 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     pub.stages = v.stages;
     pub.epi_tma = (epi == EPI_TMA || epi == EPI_TMA_C) ? 1 : 0;
 
-    pl.ldo_a = round_up(pr.K, 8);
-    pl.ldo_b = round_up(pr.K, 8);
+    pl.ldo_a = round_up(a_len(pr), 8);
+    pl.ldo_b = round_up(b_len(pr), 8);
     const int64_t nba = (pr.batch > 1 && pr.sA != 0) ? pr.batch : 1;
     const int64_t nbb = (pr.batch > 1 && pr.sB != 0) ? pr.batch : 1;
-    pl.pack_a_bytes = pub.pack_a ? round_up(nba * pr.M * pl.ldo_a * 2, 256) : 0;
-    pl.pack_b_bytes = pub.pack_b ? round_up(nbb * pr.N * pl.ldo_b * 2, 256) : 0;
+    pl.pack_a_bytes = pub.pack_a ? round_up(nba * a_rows(pr) * pl.ldo_a * 2, 256) : 0;
+    pl.pack_b_bytes = pub.pack_b ? round_up(nbb * b_rows(pr) * pl.ldo_b * 2, 256) : 0;
     pl.partial_bytes = splits > 1 ? round_up(pr.batch * splits * pr.M * pr.N * 4, 256) : 0;
     plan_stream_k(pr, pl, slots / pair);
 }
@@ -399,8 +407,8 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     // D must not overlap any input, except C exactly.
     const int64_t d_bytes = extent_bytes(pr.M, pr.N, pr.ldd, pr.sD, pr.batch);
     if (pr.K > 0) {
-        if (ranges_overlap(D, d_bytes, A, extent_bytes(pr.M, pr.K, pr.lda, pr.sA, pr.batch)) ||
-            ranges_overlap(D, d_bytes, B, extent_bytes(pr.N, pr.K, pr.ldb, pr.sB, pr.batch)))
+        if (ranges_overlap(D, d_bytes, A, extent_bytes(a_rows(pr), a_len(pr), pr.lda, pr.sA, pr.batch)) ||
+            ranges_overlap(D, d_bytes, B, extent_bytes(b_rows(pr), b_len(pr), pr.ldb, pr.sB, pr.batch)))
             return GEMM_ERR_INVALID_VALUE;
     }
     if (pr.beta != 0.0f) {
@@ -432,14 +440,20 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     CUtensorMap mapA_op, mapB_op, mapC, mapD;
     std::memset(&mapC, 0, sizeof(mapC));
     std::memset(&mapD, 0, sizeof(mapD));
-    // Problem operand A is the MMA's B operand when swapped, else its A operand.
-    const uint32_t boxA = swap ? box_rows_b : 128u;
-    const uint32_t boxB = swap ? 128u : box_rows_b;
+    // Problem operand A is the MMA's B operand when swapped, else its A operand.  A
+    // K-major operand is fetched in boxes of 64 K x rows, an MN-major one in boxes of
+    // 64 (M or N) x 64 K.
+    const uint32_t boxA = p.a_mn ? 64u : (swap ? box_rows_b : 128u);
+    const uint32_t boxB = p.b_mn ? 64u : (swap ? 128u : box_rows_b);
     CUtensorMap mapPA, mapPB;
-    if (!pl.pub.pack_a && !encode_map(&mapPA, A, p.K, p.M, p.batch, p.lda, p.sA, p.batch > 1 && p.sA != 0, 64, boxA))
-        pl.pub.pack_a = 1, pl.pack_a_bytes = round_up(((p.batch > 1 && p.sA != 0) ? p.batch : 1) * p.M * pl.ldo_a * 2, 256);
-    if (!pl.pub.pack_b && !encode_map(&mapPB, B, p.K, p.N, p.batch, p.ldb, p.sB, p.batch > 1 && p.sB != 0, 64, boxB))
-        pl.pub.pack_b = 1, pl.pack_b_bytes = round_up(((p.batch > 1 && p.sB != 0) ? p.batch : 1) * p.N * pl.ldo_b * 2, 256);
+    if (!pl.pub.pack_a && !encode_map(&mapPA, A, a_len(p), a_rows(p), p.batch, p.lda, p.sA, p.batch > 1 && p.sA != 0,
+                                      64, boxA))
+        pl.pub.pack_a = 1,
+        pl.pack_a_bytes = round_up(((p.batch > 1 && p.sA != 0) ? p.batch : 1) * a_rows(p) * pl.ldo_a * 2, 256);
+    if (!pl.pub.pack_b && !encode_map(&mapPB, B, b_len(p), b_rows(p), p.batch, p.ldb, p.sB, p.batch > 1 && p.sB != 0,
+                                      64, boxB))
+        pl.pub.pack_b = 1,
+        pl.pack_b_bytes = round_up(((p.batch > 1 && p.sB != 0) ? p.batch : 1) * b_rows(p) * pl.ldo_b * 2, 256);
     if ((pl.epi == EPI_TMA || pl.epi == EPI_TMA_C) &&
         (!encode_map(&mapD, D, p.N, p.M, p.batch, p.ldd, p.sD, p.batch > 1, 64, 32) ||
          (pl.epi == EPI_TMA_C &&
@@ -481,16 +495,18 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     int njobs = 0;
     if (pl.pub.pack_a) {
         void* dst = ws;
-        jobs[njobs++] = {A, p.lda, p.sA, dst, pl.ldo_a, p.M, p.K, a_batched ? p.batch : 1};
-        if (!encode_map(&mapPA, dst, p.K, p.M, p.batch, pl.ldo_a, p.M * pl.ldo_a, a_batched, 64, boxA)) {
+        jobs[njobs++] = {A, p.lda, p.sA, dst, pl.ldo_a, a_rows(p), a_len(p), a_batched ? p.batch : 1};
+        if (!encode_map(&mapPA, dst, a_len(p), a_rows(p), p.batch, pl.ldo_a, a_rows(p) * pl.ldo_a, a_batched, 64,
+                        boxA)) {
             release();
             return GEMM_ERR_UNSUPPORTED;
         }
     }
     if (pl.pub.pack_b) {
         void* dst = ws + pl.pack_a_bytes;
-        jobs[njobs++] = {B, p.ldb, p.sB, dst, pl.ldo_b, p.N, p.K, b_batched ? p.batch : 1};
-        if (!encode_map(&mapPB, dst, p.K, p.N, p.batch, pl.ldo_b, p.N * pl.ldo_b, b_batched, 64, boxB)) {
+        jobs[njobs++] = {B, p.ldb, p.sB, dst, pl.ldo_b, b_rows(p), b_len(p), b_batched ? p.batch : 1};
+        if (!encode_map(&mapPB, dst, b_len(p), b_rows(p), p.batch, pl.ldo_b, b_rows(p) * pl.ldo_b, b_batched, 64,
+                        boxB)) {
             release();
             return GEMM_ERR_UNSUPPORTED;
         }
@@ -519,6 +535,8 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     kp.zB = swap ? (a_batched ? 1 : 0) : (b_batched ? 1 : 0);
     kp.zC = (p.batch > 1 && p.sC != 0) ? 1 : 0;
     kp.zD = p.batch > 1 ? 1 : 0;
+    kp.a_mn = p.a_mn;  // operands are never swapped when one is MN-major
+    kp.b_mn = p.b_mn;
     kp.num_units = pl.pub.units;
     kp.M = static_cast<int32_t>(p.M);
     kp.N = static_cast<int32_t>(p.N);
@@ -575,6 +593,18 @@ gemm_status_t gemm_tn_f16_batched(const void* A, int64_t lda, int64_t strideA, c
                                   int64_t strideD, int64_t M, int64_t N, int64_t K, int64_t batch, float alpha,
                                   float beta, gemm_stream_t stream) {
     Problem p = {M, N, K, batch, lda, ldb, ldc, ldd, strideA, strideB, strideC, strideD, beta, 0};
+    return run(A, B, C, D, p, alpha, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_f16(int32_t a_major, int32_t b_major, const void* A, int64_t lda, int64_t strideA, const void* B,
+                       int64_t ldb, int64_t strideB, const void* C, int64_t ldc, int64_t strideC, void* D, int64_t ldd,
+                       int64_t strideD, int64_t M, int64_t N, int64_t K, int64_t batch, float alpha, float beta,
+                       gemm_stream_t stream) {
+    if ((a_major != GEMM_K_MAJOR && a_major != GEMM_MN_MAJOR) || (b_major != GEMM_K_MAJOR && b_major != GEMM_MN_MAJOR))
+        return GEMM_ERR_INVALID_VALUE;
+    Problem p = {M, N, K, batch, lda, ldb, ldc, ldd, strideA, strideB, strideC, strideD, beta, 0};
+    p.a_mn = a_major == GEMM_MN_MAJOR ? 1 : 0;
+    p.b_mn = b_major == GEMM_MN_MAJOR ? 1 : 0;
     return run(A, B, C, D, p, alpha, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -22,6 +22,7 @@ struct KParams {
     int32_t kb_total;          // number of 64-wide k-blocks, ceil(K/64)
     int32_t group_m;           // rasterisation group size along the tile rows
     int32_t zA, zB, zC, zD;    // batch coordinate multipliers (0 = operand not batched)
+    int32_t a_mn, b_mn;        // 1: the MMA operand is stored MN-major (rows contiguous), 0: K-major
     int64_t num_units;         // data-parallel units: whole tiles, or (tile, K slice) pairs when splits > 1
     // Problem view, for the epilogue.
     int32_t M, N;

@@ -256,11 +256,25 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_addr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: A and B fp16, both K-major, D fp32.
+// Descriptor of an MN-major operand tile stored as TMA lays out boxes of 64
+// MN-elements (128 bytes) x 64 K-rows with 128-byte swizzle, one box after the
+// other along MN: 64-element MN blocks are 8192 bytes apart (leading-dimension
+// byte offset) and 8-row K groups 1024 bytes apart (stride-dimension byte offset).
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t smem_addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(8192u >> 4) << 16;
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;
+    d |= static_cast<uint64_t>(1u) << 46;
+    d |= static_cast<uint64_t>(2u) << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: A and B fp16, D fp32; operand majors from the flags.
 //   bits 4-5: D format (1 = f32); bits 7-9 / 10-12: A / B format (0 = f16);
 //   bits 15 / 16: A / B major (0 = K); bits 17-22: N >> 3; bits 24-28: M >> 4.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
-    return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, uint32_t a_mn = 0, uint32_t b_mn = 0) {
+    return (1u << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 }  // namespace gtn

@@ -294,13 +294,28 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
                         const uint32_t dA = sA + stage * Cfg::A_BYTES;
                         const uint32_t dB = sB + stage * Cfg::B_BYTES;
-                        if constexpr (PAIR == 1) {
-                            tma_load_3d(dA, &tmA, fb, kb * Cfg::BK, rowA, w.b * p.zA);
-                            tma_load_3d(dB, &tmB, fb, kb * Cfg::BK, rowB, w.b * p.zB);
+                        // K-major operand: one box of 64 K x rows.  MN-major operand: boxes of
+                        // 64 rows (MN) x 64 K, 8 KB each, one after the other along MN.
+                        const uint32_t fl = (PAIR == 1) ? fb : map_to_cta(fb, 0);
+                        auto load = [&](uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z) {
+                            if constexpr (PAIR == 1) tma_load_3d(dst, map, fl, x, y, z);
+                            else tma_load_3d_pair(dst, map, fl, x, y, z);
+                        };
+                        if (!p.a_mn) {
+                            load(dA, &tmA, kb * Cfg::BK, rowA, w.b * p.zA);
                         } else {
-                            const uint32_t fl = map_to_cta(fb, 0);
-                            tma_load_3d_pair(dA, &tmA, fl, kb * Cfg::BK, rowA, w.b * p.zA);
-                            tma_load_3d_pair(dB, &tmB, fl, kb * Cfg::BK, rowB, w.b * p.zB);
+#pragma unroll
+                            for (int i = 0; i < Cfg::BM / 64; ++i)
+                                load(dA + 8192u * i, &tmA, rowA + 64 * i, kb * Cfg::BK, w.b * p.zA);
+                        }
+                        if (!p.b_mn) {
+                            load(dB, &tmB, kb * Cfg::BK, rowB, w.b * p.zB);
+                        } else {
+                            if constexpr (Cfg::BN_LOCAL % 64 == 0) {
+#pragma unroll
+                                for (int i = 0; i < Cfg::BN_LOCAL / 64; ++i)
+                                    load(dB + 8192u * i, &tmB, rowB + 64 * i, kb * Cfg::BK, w.b * p.zB);
+                            }
                         }
                     }
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -316,7 +331,10 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader CTA only)
         if (rank == 0 && lane == 0) {
-            constexpr uint32_t IDESC = idesc_f16_f32(Cfg::BM * PAIR, BN);
+            const uint32_t IDESC = idesc_f16_f32(Cfg::BM * PAIR, BN, p.a_mn ? 1u : 0u, p.b_mn ? 1u : 0u);
+            // Per 16-wide K step: +32 bytes inside a K-major 128-byte row, +2048 bytes
+            // (16 rows of 128 bytes) in an MN-major box.
+            const uint32_t a_step = p.a_mn ? 128u : 2u, b_step = p.b_mn ? 128u : 2u;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -334,12 +352,12 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t adesc = smem_desc_sw128(sA + stage * Cfg::A_BYTES);
-                    const uint64_t bdesc = smem_desc_sw128(sB + stage * Cfg::B_BYTES);
+                    const uint32_t a_addr = sA + stage * Cfg::A_BYTES, b_addr = sB + stage * Cfg::B_BYTES;
+                    const uint64_t adesc = p.a_mn ? smem_desc_mn_sw128(a_addr) : smem_desc_sw128(a_addr);
+                    const uint64_t bdesc = p.b_mn ? smem_desc_mn_sw128(b_addr) : smem_desc_sw128(b_addr);
 #pragma unroll
                     for (int k = 0; k < Cfg::BK / 16; ++k) {
-                        // +32 bytes per 16-wide K step inside the 128-byte swizzled row
-                        mma_f16<PAIR>(d_tmem, adesc + 2u * k, bdesc + 2u * k, IDESC,
+                        mma_f16<PAIR>(d_tmem, adesc + a_step * k, bdesc + b_step * k, IDESC,
                                       (kb > w.kb0 || k > 0) ? 1u : 0u);
                     }
                     if constexpr (PAIR == 1) mma_commit(empty_bar(stage));

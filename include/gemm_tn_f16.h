@@ -108,6 +108,33 @@ GEMM_TN_API gemm_status_t gemm_tn_f16_batched(const void* A, int64_t lda, int64_
                                   float alpha, float beta,
                                   gemm_stream_t stream);
 
+/*
+ * Operand storage for gemm_f16.  The product is always D = alpha * A . B^T + beta * C
+ * with A logically M x K and B logically N x K (TN is both K-major).
+ *   GEMM_K_MAJOR : A stored M x lda with K contiguous (lda >= K); B stored N x ldb.
+ *   GEMM_MN_MAJOR: A stored K x lda with M contiguous (lda >= M), i.e. A^T row-major;
+ *                  B stored K x ldb with N contiguous (ldb >= N).
+ */
+typedef enum { GEMM_K_MAJOR = 0, GEMM_MN_MAJOR = 1 } gemm_major_t;
+
+/*
+ * The GEMM with either operand in either storage order -- the stride-generic form
+ * of the "gemm_device 逐行解析" page, whose kernel takes A, B and C with arbitrary
+ * strides dA, dB, dC (section 1).  Batched like gemm_tn_f16_batched (batch >= 1;
+ * strideX between entries, 0 broadcasts A, B or C).  An MN-major operand is read by
+ * the tensor core through an MN-major shared-memory layout; operands are never
+ * swapped for small M in that case.  All other rules as gemm_tn_f16_batched;
+ * GEMM_ERR_INVALID_VALUE for an unknown a_major / b_major.
+ */
+GEMM_TN_API gemm_status_t gemm_f16(int32_t a_major, int32_t b_major,
+                                   const void* A, int64_t lda, int64_t strideA,
+                                   const void* B, int64_t ldb, int64_t strideB,
+                                   const void* C, int64_t ldc, int64_t strideC,
+                                   void* D, int64_t ldd, int64_t strideD,
+                                   int64_t M, int64_t N, int64_t K, int64_t batch,
+                                   float alpha, float beta,
+                                   gemm_stream_t stream);
+
 /* Static English text for a status code; never NULL. */
 GEMM_TN_API const char* gemm_status_string(gemm_status_t status);
 

@@ -197,3 +197,15 @@ def test_options_roundtrip_and_validation():
         G.gemm_tn_f16_set_option(12345, 1)
     with pytest.raises(G.GemmError):
         G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_WAIT_TIMEOUT_NS, 10)
+
+
+def test_gemm_f16_rejects_bad_majors_and_leading_dims():
+    # unknown major
+    assert G.gemm_f16(3, 0, 0x1000, 8, 0, 0x2000, 8, 0, None, 8, 0, 0x3000, 8, 0, 8, 8, 8, 1, 1.0, 0.0,
+                      check=False) == G.GEMM_ERR_INVALID_VALUE
+    # MN-major A needs lda >= M (A stored K x lda): M = 16 > lda = 8
+    assert G.gemm_f16(G.GEMM_MN_MAJOR, 0, 0x1000, 8, 0, 0x2000, 8, 0, None, 8, 0, 0x3000, 8, 0, 16, 8, 8, 1,
+                      1.0, 0.0, check=False) == G.GEMM_ERR_INVALID_VALUE
+    # MN-major B needs ldb >= N
+    assert G.gemm_f16(0, G.GEMM_MN_MAJOR, 0x1000, 8, 0, 0x2000, 8, 0, None, 16, 0, 0x3000, 16, 0, 8, 16, 8, 1,
+                      1.0, 0.0, check=False) == G.GEMM_ERR_INVALID_VALUE
