@@ -282,6 +282,39 @@ def dist_barrier(dist):
         dist.barrier()
 
 
+def time_transpose(G, device, flush_buf, read_buf, peaks, n=1024, steps=50):
+    """y = x^T for a 1024 x 1024 fp32 matrix (the transpose page's workload)."""
+    import torch
+    x = torch.rand((n, n), device=device)
+    y = torch.empty_like(x)
+    for _ in range(5):
+        G.transpose_f32(x, n, y, n, n, n)
+    torch.cuda.synchronize()
+    ts = []
+    for i in range(steps):
+        flush_l2(flush_buf, read_buf, i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        G.transpose_f32(x, n, y, n, n, n)
+        e1.record()
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    ms = statistics.median([a.elapsed_time(b) for a, b in ts])
+    gbs = 2 * n * n * 4 / (ms * 1e-3) / 1e9
+    # the same without the flush: the 4 MB matrix then stays in L2, as on the page's GPU
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        G.transpose_f32(x, n, y, n, n, n)
+    e1.record()
+    torch.cuda.synchronize()
+    hot_us = e0.elapsed_time(e1) / steps * 1e3
+    return {"workload": "transpose y = x^T, fp32 1024 x 1024", "us": ms * 1e3, "hbm_gbs": gbs,
+            "frac_of_hbm_roofline": gbs / peaks["hbm_gbs"], "l2": "flushed before every step",
+            "us_l2_resident_back_to_back": hot_us,
+            "page_context": "0.0039 ms best on an RTX 4090 (transpose page's table; other hardware)"}
+
+
 def roofline_tflops(w, peaks):
     tensor = peaks["bf16_tflops"]
     hbm = peaks["hbm_gbs"] * 1e9
@@ -443,6 +476,7 @@ def run_ours(args, rank, world, dist):
         st = G.gemm_tn_f16_last_device_error()
         if st != G.GEMM_OK:
             raise RuntimeError(f"device error in per-config timing: {G.gemm_status_string(st)}")
+        per_config["transpose_f32_1024"] = time_transpose(G, device, flush, read_buf, peaks)
 
     if rank != 0:
         return

@@ -42,4 +42,6 @@ from ._binding import (  # noqa: F401
     gemm_tn_f16_version,
     library_path,
     load_library,
+    transpose_f16,
+    transpose_f32,
 )

@@ -135,6 +135,20 @@ GEMM_TN_API gemm_status_t gemm_f16(int32_t a_major, int32_t b_major,
                                    float alpha, float beta,
                                    gemm_stream_t stream);
 
+/*
+ * Matrix transpose Y = X^T of the "10-mat-transpose-cute" page (y[c][r] = x[r][c]
+ * for a rows x cols row-major x; predicated at ragged edges): fp32 (the page's
+ * type) and fp16 elements, bits copied unchanged.
+ * X: rows x ldx (ldx >= cols), Y: cols x ldy (ldy >= rows), both device memory;
+ * they must not overlap (GEMM_ERR_INVALID_VALUE), elements must be naturally
+ * aligned (GEMM_ERR_MISALIGNED).  16-byte aligned matrices with leading dimensions
+ * that are multiples of 16 bytes take the vectorised path.  Asynchronous on stream.
+ */
+GEMM_TN_API gemm_status_t transpose_f32(const void* X, int64_t ldx, void* Y, int64_t ldy,
+                                        int64_t rows, int64_t cols, gemm_stream_t stream);
+GEMM_TN_API gemm_status_t transpose_f16(const void* X, int64_t ldx, void* Y, int64_t ldy,
+                                        int64_t rows, int64_t cols, gemm_stream_t stream);
+
 /* Static English text for a status code; never NULL. */
 GEMM_TN_API const char* gemm_status_string(gemm_status_t status);
 

@@ -71,6 +71,11 @@ def _bind(path):
                                          u16p, i64, i64, i64, i64, i64,
                                          ctypes.c_float, ctypes.c_float, i64, i64]
     lib.gto_gemm_f16_strided.restype = None
+    u32p = ctypes.POINTER(ctypes.c_uint32)
+    lib.gto_transpose_u32.argtypes = [u32p, i64, u32p, i64, i64, i64]
+    lib.gto_transpose_u32.restype = None
+    lib.gto_transpose_u16.argtypes = [u16p, i64, u16p, i64, i64, i64]
+    lib.gto_transpose_u16.restype = None
     return lib
 
 
@@ -123,6 +128,9 @@ class Oracle:
     def gemm_strided(self, *args, **kw):
         return _gemm_strided(self.lib, *args, **kw)
 
+    def transpose(self, *args, **kw):
+        return _transpose(self.lib, *args, **kw)
+
 
 def _u16ptr(a):
     if a is None:
@@ -149,6 +157,10 @@ def gemm_tn_entries(*args, **kw):
 
 def gemm_strided(*args, **kw):
     return _gemm_strided(_load(), *args, **kw)
+
+
+def transpose(*args, **kw):
+    return _transpose(_load(), *args, **kw)
 
 
 def default_threads() -> int:
@@ -247,3 +259,21 @@ def _gemm_strided(lib, A, a_strides, B, b_strides, C, M, N, K, alpha, beta, *, l
     with ThreadPoolExecutor(max_workers=nthr) as ex:
         list(ex.map(lambda s: lib.gto_gemm_f16_strided(*args_pre, s[0], s[1]), spans))
     return D
+
+
+def _transpose(lib, X, rows, cols, *, ldx=None, ldy=None, Y=None):
+    """y = x^T for a rows x cols row-major x of uint32 (fp32 bits) or uint16 (fp16 bits).
+    Returns Y, a flat array of cols * ldy elements unless Y is supplied."""
+    ldx = cols if ldx is None else ldx
+    ldy = rows if ldy is None else ldy
+    X = np.ascontiguousarray(X)
+    if Y is None:
+        Y = np.zeros(max(cols * ldy, 1), dtype=X.dtype)
+    if X.dtype == np.uint32:
+        p = ctypes.POINTER(ctypes.c_uint32)
+        lib.gto_transpose_u32(X.ctypes.data_as(p), ldx, Y.ctypes.data_as(p), ldy, rows, cols)
+    elif X.dtype == np.uint16:
+        lib.gto_transpose_u16(_u16ptr(X), ldx, _u16ptr(Y), ldy, rows, cols)
+    else:
+        raise TypeError("uint32 or uint16 bit patterns expected")
+    return Y

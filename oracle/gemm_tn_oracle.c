@@ -179,3 +179,15 @@ void gto_gemm_f16_strided(const uint16_t* A, int64_t a_rs, int64_t a_cs, int64_t
         }
     }
 }
+
+void gto_transpose_u32(const uint32_t* X, int64_t ldx, uint32_t* Y, int64_t ldy, int64_t rows, int64_t cols)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) Y[c * ldy + r] = X[r * ldx + c];
+}
+
+void gto_transpose_u16(const uint16_t* X, int64_t ldx, uint16_t* Y, int64_t ldy, int64_t rows, int64_t cols)
+{
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) Y[c * ldy + r] = X[r * ldx + c];
+}

@@ -85,6 +85,14 @@ void gto_gemm_f16_strided(const uint16_t* A, int64_t a_rs, int64_t a_cs, int64_t
                           float alpha, float beta,
                           int64_t r_begin, int64_t r_end);
 
+/*
+ * Matrix transpose y = x^T of the "10-mat-transpose-cute" page (each version
+ * computes y[c][r] = x[r][c] for an M x N row-major x, predicated at the edges):
+ * element bits are copied, 4-byte (fp32) or 2-byte (fp16) elements.
+ */
+void gto_transpose_u32(const uint32_t* X, int64_t ldx, uint32_t* Y, int64_t ldy, int64_t rows, int64_t cols);
+void gto_transpose_u16(const uint16_t* X, int64_t ldx, uint16_t* Y, int64_t ldy, int64_t rows, int64_t cols);
+
 #ifdef __cplusplus
 }
 #endif

@@ -342,8 +342,25 @@ def check_strided_layouts(o, seed=14):
             assert np.array_equal(bits_to_f64(got), want)
 
 
+def check_transpose(o, seed=15):
+    """y = x^T: equals numpy's transpose element for element, twice is the identity,
+    and padding beyond ld is neither read into nor written."""
+    rng = np.random.default_rng(seed)
+    for dt in (np.uint32, np.uint16):
+        rows, cols = 37, 53
+        x = rng.integers(0, np.iinfo(dt).max, (rows, cols), dtype=dt)
+        y = o.transpose(x, rows, cols).reshape(cols, rows)
+        assert np.array_equal(y, x.T)
+        assert np.array_equal(o.transpose(y, cols, rows).reshape(rows, cols), x)
+        xp = np.full((rows, cols + 5), 7, dtype=dt); xp[:, :cols] = x
+        yp = np.full(cols * (rows + 3), 9, dtype=dt)
+        o.transpose(xp, rows, cols, ldx=cols + 5, ldy=rows + 3, Y=yp)
+        yp = yp.reshape(cols, rows + 3)
+        assert np.array_equal(yp[:, :rows], x.T) and (yp[:, rows:] == 9).all()
+
+
 GEMM_CHECKS = [check_bruteforce_exact, check_strided_layouts, check_identity, check_permutation, check_all_ones,
                check_transpose_invariant, check_small_integers, check_beta_zero_does_not_read_c,
-               check_leading_dims, check_batched, check_entries_match_full, check_degenerate]
+               check_leading_dims, check_batched, check_entries_match_full, check_degenerate, check_transpose]
 CONVERSION_CHECKS = [check_decode_exhaustive, check_encode_specials, check_encode_random_vs_numpy,
                      check_encode_ties_and_neighbours, check_encode_roundtrip]

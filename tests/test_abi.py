@@ -209,3 +209,10 @@ def test_gemm_f16_rejects_bad_majors_and_leading_dims():
     # MN-major B needs ldb >= N
     assert G.gemm_f16(0, G.GEMM_MN_MAJOR, 0x1000, 8, 0, 0x2000, 8, 0, None, 16, 0, 0x3000, 16, 0, 8, 16, 8, 1,
                       1.0, 0.0, check=False) == G.GEMM_ERR_INVALID_VALUE
+
+
+def test_transpose_host_checks_without_a_gpu():
+    assert G.transpose_f32(None, 8, None, 8, 0, 8, check=False) == G.GEMM_OK
+    assert G.transpose_f32(0x1000, 4, 0x9000, 8, 8, 8, check=False) == G.GEMM_ERR_INVALID_VALUE
+    assert G.transpose_f16(0x1001, 8, 0x9000, 8, 8, 8, check=False) == G.GEMM_ERR_MISALIGNED
+    assert G.transpose_f32(0x1000, 8, 0x1010, 8, 8, 8, check=False) == G.GEMM_ERR_INVALID_VALUE

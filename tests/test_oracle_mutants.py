@@ -27,6 +27,8 @@ MUTANTS = [
     # (mutants stay inside the operand buffers: an out-of-range read would be undefined)
     ("strided_a_unit_k_stride", "A[b * strideA + m * a_rs + k * a_cs]", "A[b * strideA + m * a_rs + k]"),
     ("strided_b_unit_row_stride", "B[b * strideB + n * b_rs + k * b_cs]", "B[b * strideB + n + k * b_cs]"),
+    ("transpose_drops_last_row", "for (int64_t r = 0; r < rows; ++r)\n        for (int64_t c = 0; c < cols; ++c) Y[c * ldy + r] = X[r * ldx + c];\n}\n\nvoid gto_transpose_u16",
+     "for (int64_t r = 0; r + 1 < rows; ++r)\n        for (int64_t c = 0; c < cols; ++c) Y[c * ldy + r] = X[r * ldx + c];\n}\n\nvoid gto_transpose_u16"),
     ("flush_subnormals", "const int q = (E < -14) ? -24 : E - 10;", "const int q = (E < -14) ? 99 : E - 10;"),
 ]
 
