@@ -29,6 +29,7 @@ from ._binding import (  # noqa: F401
     GEMM_TN_STATIC_SCRATCH_BYTES,
     GemmError,
     gemm_f16,
+    gemm_f16_acc16,
     gemm_status_string,
     gemm_tn_f16,
     gemm_tn_f16_batched,

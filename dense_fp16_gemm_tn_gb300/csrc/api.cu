@@ -183,6 +183,7 @@ struct Problem {
     float beta;
     uint32_t align;  // bit i: operand i (A,B,C,D) base is 16-byte aligned
     int32_t a_mn = 0, b_mn = 0;  // 1: A stored K x lda (M contiguous) / B stored K x ldb (N contiguous)
+    int32_t acc16 = 0;           // 1: accumulate in fp16 on the tensor core
 };
 
 // Elements of an operand's rows in memory (its contiguous extent) and their count.
@@ -300,7 +301,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     bool swap = pr.M <= 64 && pr.N >= 128 && pr.N >= 2 * pr.M;
     const int64_t fs = g_opt_force_swap.load();
     if (fs > 0 && pr.M <= 64) swap = true;
-    if (fs < 0 || pr.a_mn || pr.b_mn) swap = false;
+    if (fs < 0 || pr.a_mn || pr.b_mn || pr.acc16) swap = false;
 
     int bn, pair;
     const int64_t slots = std::max(sms, 1);
@@ -334,14 +335,15 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     // few tiles is the stream-K split decided in plan_stream_k).
     int splits = 1;
     const int64_t fsplit = g_opt_force_splits.load();
-    if (fsplit >= 1 && !pr.a_mn && !pr.b_mn) {
+    if (fsplit >= 1 && !pr.a_mn && !pr.b_mn && !pr.acc16) {
         pair = 1;
         splits = static_cast<int>(std::min<int64_t>(fsplit, kb));
         if (!swap) bn = 128;  // the partial-sum variant exists at 128 columns
     }
 
     int epi;
-    if (splits > 1) epi = swap ? EPI_PARTIAL_SWAP : EPI_PARTIAL;
+    if (pr.acc16) epi = (pr.beta == 0.0f && d_ok && g_opt_force_generic.load() == 0) ? EPI_TMA_A16 : EPI_GENERIC_A16;
+    else if (splits > 1) epi = swap ? EPI_PARTIAL_SWAP : EPI_PARTIAL;
     else if (swap) epi = EPI_SWAP;
     else if (d_ok && c_ok && g_opt_force_generic.load() == 0) epi = pr.beta == 0.0f ? EPI_TMA : EPI_TMA_C;
     else epi = EPI_GENERIC;
@@ -370,7 +372,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     pub.swap_ab = swap ? 1 : 0;
     pub.splits = splits;
     pub.stages = v.stages;
-    pub.epi_tma = (epi == EPI_TMA || epi == EPI_TMA_C) ? 1 : 0;
+    pub.epi_tma = (epi_base(epi) == EPI_TMA || epi == EPI_TMA_C) ? 1 : 0;
 
     pl.ldo_a = round_up(a_len(pr), 8);
     pl.ldo_b = round_up(b_len(pr), 8);
@@ -454,14 +456,15 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
                                       64, boxB))
         pl.pub.pack_b = 1,
         pl.pack_b_bytes = round_up(((p.batch > 1 && p.sB != 0) ? p.batch : 1) * b_rows(p) * pl.ldo_b * 2, 256);
-    if ((pl.epi == EPI_TMA || pl.epi == EPI_TMA_C) &&
+    if ((epi_base(pl.epi) == EPI_TMA || pl.epi == EPI_TMA_C) &&
         (!encode_map(&mapD, D, p.N, p.M, p.batch, p.ldd, p.sD, p.batch > 1, 64, 32) ||
          (pl.epi == EPI_TMA_C &&
           !encode_map(&mapC, C, p.N, p.M, p.batch, p.ldc, p.sC, p.batch > 1 && p.sC != 0, 64, 32)))) {
         TcVariant v;
-        if (find_tc_variant(pl.var.bn, pl.var.pair, EPI_GENERIC, 0, &v)) {
+        const int generic = epi_acc16(pl.epi) ? EPI_GENERIC_A16 : EPI_GENERIC;
+        if (find_tc_variant(pl.var.bn, pl.var.pair, generic, 0, &v)) {
             pl.var = v;
-            pl.epi = EPI_GENERIC;
+            pl.epi = generic;
             pl.pub.epi_tma = 0;
         } else {
             return GEMM_ERR_UNSUPPORTED;
@@ -517,7 +520,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     }
     mapA_op = swap ? mapPB : mapPA;
     mapB_op = swap ? mapPA : mapPB;
-    if (pl.epi != EPI_TMA && pl.epi != EPI_TMA_C) mapD = mapA_op;  // unused by the kernel; any valid map
+    if (epi_base(pl.epi) != EPI_TMA && pl.epi != EPI_TMA_C) mapD = mapA_op;  // unused by the kernel; any valid map
     if (pl.epi != EPI_TMA_C) mapC = mapD;
 
     KParams kp;
@@ -605,6 +608,19 @@ gemm_status_t gemm_f16(int32_t a_major, int32_t b_major, const void* A, int64_t 
     Problem p = {M, N, K, batch, lda, ldb, ldc, ldd, strideA, strideB, strideC, strideD, beta, 0};
     p.a_mn = a_major == GEMM_MN_MAJOR ? 1 : 0;
     p.b_mn = b_major == GEMM_MN_MAJOR ? 1 : 0;
+    return run(A, B, C, D, p, alpha, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_f16_acc16(int32_t a_major, int32_t b_major, const void* A, int64_t lda, int64_t strideA,
+                             const void* B, int64_t ldb, int64_t strideB, const void* C, int64_t ldc, int64_t strideC,
+                             void* D, int64_t ldd, int64_t strideD, int64_t M, int64_t N, int64_t K, int64_t batch,
+                             float alpha, float beta, gemm_stream_t stream) {
+    if ((a_major != GEMM_K_MAJOR && a_major != GEMM_MN_MAJOR) || (b_major != GEMM_K_MAJOR && b_major != GEMM_MN_MAJOR))
+        return GEMM_ERR_INVALID_VALUE;
+    Problem p = {M, N, K, batch, lda, ldb, ldc, ldd, strideA, strideB, strideC, strideD, beta, 0};
+    p.a_mn = a_major == GEMM_MN_MAJOR ? 1 : 0;
+    p.b_mn = b_major == GEMM_MN_MAJOR ? 1 : 0;
+    p.acc16 = 1;
     return run(A, B, C, D, p, alpha, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -700,6 +716,7 @@ gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value) {
             if (value < -1 || value > 1) return GEMM_ERR_INVALID_VALUE;
             g_opt_stream_k = value;
             return GEMM_OK;
+
     }
     return GEMM_ERR_INVALID_VALUE;
 }
@@ -715,6 +732,7 @@ int64_t gemm_tn_f16_get_option(int32_t option) {
         case GEMM_TN_OPT_FORCE_GENERIC_EPI: return g_opt_force_generic.load();
         case GEMM_TN_OPT_FORCE_PACK: return g_opt_force_pack.load();
         case GEMM_TN_OPT_STREAM_K: return g_opt_stream_k.load();
+
     }
     return -1;
 }

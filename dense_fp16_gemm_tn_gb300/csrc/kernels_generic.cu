@@ -13,10 +13,13 @@ bool launch_family_generic(const TcVariant& v, const CUtensorMap& tmA, const CUt
     }
     GTN_CASE(256, 1, 4, EPI_GENERIC, 0)
     GTN_CASE(256, 1, 4, EPI_GENERIC, 1)
+    GTN_CASE(256, 1, 4, EPI_GENERIC_A16, 0)
     GTN_CASE(256, 2, 6, EPI_GENERIC, 0)
     GTN_CASE(256, 2, 6, EPI_GENERIC, 1)
+    GTN_CASE(256, 2, 6, EPI_GENERIC_A16, 0)
     GTN_CASE(128, 1, 6, EPI_GENERIC, 0)
     GTN_CASE(128, 1, 6, EPI_GENERIC, 1)
+    GTN_CASE(128, 1, 6, EPI_GENERIC_A16, 0)
     GTN_CASE(128, 1, 6, EPI_PARTIAL, 0)
 #undef GTN_CASE
     return false;
@@ -30,10 +33,13 @@ bool capacity_family_generic(const TcVariant& v, int sms, int64_t* cap) {
     }
     GTN_CASE(256, 1, 4, EPI_GENERIC, 0)
     GTN_CASE(256, 1, 4, EPI_GENERIC, 1)
+    GTN_CASE(256, 1, 4, EPI_GENERIC_A16, 0)
     GTN_CASE(256, 2, 6, EPI_GENERIC, 0)
     GTN_CASE(256, 2, 6, EPI_GENERIC, 1)
+    GTN_CASE(256, 2, 6, EPI_GENERIC_A16, 0)
     GTN_CASE(128, 1, 6, EPI_GENERIC, 0)
     GTN_CASE(128, 1, 6, EPI_GENERIC, 1)
+    GTN_CASE(128, 1, 6, EPI_GENERIC_A16, 0)
     GTN_CASE(128, 1, 6, EPI_PARTIAL, 0)
 #undef GTN_CASE
     return false;

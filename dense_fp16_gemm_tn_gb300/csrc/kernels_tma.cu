@@ -14,14 +14,17 @@ bool launch_family_tma(const TcVariant& v, const CUtensorMap& tmA, const CUtenso
     GTN_CASE(256, 1, 4, EPI_TMA, 0)
     GTN_CASE(256, 1, 4, EPI_TMA_C, 0)
     GTN_CASE(256, 1, 4, EPI_TMA, 1)
+    GTN_CASE(256, 1, 4, EPI_TMA_A16, 0)
     GTN_CASE(256, 1, 4, EPI_TMA_C, 1)
     GTN_CASE(256, 2, 6, EPI_TMA, 0)
     GTN_CASE(256, 2, 6, EPI_TMA_C, 0)
     GTN_CASE(256, 2, 6, EPI_TMA, 1)
+    GTN_CASE(256, 2, 6, EPI_TMA_A16, 0)
     GTN_CASE(256, 2, 6, EPI_TMA_C, 1)
     GTN_CASE(128, 1, 6, EPI_TMA, 0)
     GTN_CASE(128, 1, 6, EPI_TMA_C, 0)
     GTN_CASE(128, 1, 6, EPI_TMA, 1)
+    GTN_CASE(128, 1, 6, EPI_TMA_A16, 0)
     GTN_CASE(128, 1, 6, EPI_TMA_C, 1)
     GTN_CASE(128, 2, 8, EPI_TMA, 0)
     GTN_CASE(128, 2, 8, EPI_TMA_C, 0)
@@ -40,14 +43,17 @@ bool capacity_family_tma(const TcVariant& v, int sms, int64_t* cap) {
     GTN_CASE(256, 1, 4, EPI_TMA, 0)
     GTN_CASE(256, 1, 4, EPI_TMA_C, 0)
     GTN_CASE(256, 1, 4, EPI_TMA, 1)
+    GTN_CASE(256, 1, 4, EPI_TMA_A16, 0)
     GTN_CASE(256, 1, 4, EPI_TMA_C, 1)
     GTN_CASE(256, 2, 6, EPI_TMA, 0)
     GTN_CASE(256, 2, 6, EPI_TMA_C, 0)
     GTN_CASE(256, 2, 6, EPI_TMA, 1)
+    GTN_CASE(256, 2, 6, EPI_TMA_A16, 0)
     GTN_CASE(256, 2, 6, EPI_TMA_C, 1)
     GTN_CASE(128, 1, 6, EPI_TMA, 0)
     GTN_CASE(128, 1, 6, EPI_TMA_C, 0)
     GTN_CASE(128, 1, 6, EPI_TMA, 1)
+    GTN_CASE(128, 1, 6, EPI_TMA_A16, 0)
     GTN_CASE(128, 1, 6, EPI_TMA_C, 1)
     GTN_CASE(128, 2, 8, EPI_TMA, 0)
     GTN_CASE(128, 2, 8, EPI_TMA_C, 0)

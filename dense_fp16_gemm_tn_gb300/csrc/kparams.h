@@ -12,7 +12,21 @@ enum EpiMode : int {
     EPI_PARTIAL = 3,       // fp32 partial sums of one K slice -> workspace
     EPI_PARTIAL_SWAP = 4,  // same, accumulator holds D^T
     EPI_TMA_C = 5,         // D = alpha*acc + beta*C, C loaded and D stored by TMA (aligned C and D)
+    EPI_TMA_A16 = 6,       // EPI_TMA with an fp16 accumulator
+    EPI_GENERIC_A16 = 7,   // EPI_GENERIC with an fp16 accumulator
 };
+
+#ifdef __CUDACC__
+#define GTN_HD __host__ __device__
+#else
+#define GTN_HD
+#endif
+
+// Epilogue mode without the accumulator precision; true when the accumulator is fp16.
+GTN_HD constexpr int epi_base(int epi) {
+    return epi == EPI_TMA_A16 ? EPI_TMA : epi == EPI_GENERIC_A16 ? EPI_GENERIC : epi;
+}
+GTN_HD constexpr bool epi_acc16(int epi) { return epi == EPI_TMA_A16 || epi == EPI_GENERIC_A16; }
 
 struct KParams {
     // Tensor-core view: the MMA's A operand has rows_a rows, its B operand rows_b rows.

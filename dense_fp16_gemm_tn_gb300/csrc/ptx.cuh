@@ -231,6 +231,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
+// 32 consecutive columns holding 16-bit values, two adjacent columns packed per
+// register (the .num count is the number of destination registers).
+__device__ __forceinline__ void tmem_ld_32x32b_x32_pack16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.pack::16b.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -270,11 +282,13 @@ __device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t smem_addr) {
     return d;
 }
 
-// Instruction descriptor, kind::f16: A and B fp16, D fp32; operand majors from the flags.
+// Instruction descriptor, kind::f16: A and B fp16, D fp32 (d_f32 = 1) or fp16 (0);
+// operand majors from the flags.
 //   bits 4-5: D format (1 = f32); bits 7-9 / 10-12: A / B format (0 = f16);
 //   bits 15 / 16: A / B major (0 = K); bits 17-22: N >> 3; bits 24-28: M >> 4.
-__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, uint32_t a_mn = 0, uint32_t b_mn = 0) {
-    return (1u << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N, uint32_t a_mn = 0, uint32_t b_mn = 0,
+                                                     uint32_t d_f32 = 1) {
+    return (d_f32 << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 }  // namespace gtn

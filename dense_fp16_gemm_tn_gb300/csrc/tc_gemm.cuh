@@ -68,7 +68,8 @@ struct TileCfg {
     static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
     static constexpr int EPI_WARP_BYTES =
-        (EPI == EPI_TMA || EPI == EPI_TMA_C) ? 2 * 32 * 128 : (EPI == EPI_GENERIC || EPI == EPI_PARTIAL) ? 32 * 33 * 4 : 0;
+        (epi_base(EPI) == EPI_TMA || EPI == EPI_TMA_C) ? 2 * 32 * 128
+        : (epi_base(EPI) == EPI_GENERIC || EPI == EPI_PARTIAL) ? 32 * 33 * 4 : 0;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
@@ -81,7 +82,7 @@ struct TileCfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N in [16,256], N%16==0");
     static_assert(BN_LOCAL % 8 == 0, "B tile must hold whole 8-row swizzle atoms");
     static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "tiles must stay 1024-byte aligned");
-    static_assert((EPI != EPI_TMA && EPI != EPI_TMA_C) || BN % 64 == 0, "TMA epilogue stores 64-column chunks");
+    static_assert((epi_base(EPI) != EPI_TMA && EPI != EPI_TMA_C) || BN % 64 == 0, "TMA epilogue stores 64-column chunks");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory per CTA");
     static_assert(PAIR == 1 || PAIR == 2, "CTA pair or single CTA");
 };
@@ -223,6 +224,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                   const KParams p) {
     using Cfg = TileCfg<BN, PAIR, STAGES, EPI>;
+    constexpr int EB = epi_base(EPI);       // epilogue mode without the accumulator precision
+    constexpr bool ACC16 = epi_acc16(EPI);  // fp16 accumulator in tensor memory
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -261,7 +264,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
-        if constexpr (EPI == EPI_TMA || EPI == EPI_TMA_C) prefetch_tensormap(&tmD);
+        if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C) prefetch_tensormap(&tmD);
         if constexpr (EPI == EPI_TMA_C) prefetch_tensormap(&tmC);
     }
     if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -331,7 +334,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader CTA only)
         if (rank == 0 && lane == 0) {
-            const uint32_t IDESC = idesc_f16_f32(Cfg::BM * PAIR, BN, p.a_mn ? 1u : 0u, p.b_mn ? 1u : 0u);
+            const uint32_t IDESC = idesc_f16_f32(Cfg::BM * PAIR, BN, p.a_mn ? 1u : 0u, p.b_mn ? 1u : 0u, ACC16 ? 0u : 1u);
             // Per 16-wide K step: +32 bytes inside a K-major 128-byte row, +2048 bytes
             // (16 rows of 128 bytes) in an MN-major box.
             const uint32_t a_step = p.a_mn ? 128u : 2u, b_step = p.b_mn ? 128u : 2u;
@@ -378,7 +381,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t chunk_count = 0;
-        const bool use_c = (EPI == EPI_GENERIC || EPI == EPI_SWAP) && p.beta != 0.0f;
+        const bool use_c = (EB == EPI_GENERIC || EB == EPI_SWAP) && p.beta != 0.0f;
         // TMA epilogue with beta != 0: C boxes are fetched by TMA into the staging buffers.
         constexpr bool tma_c = EPI == EPI_TMA_C;
         uint32_t cphase = 0u;  // bit b: parity of the next C load into staging buffer b
@@ -407,7 +410,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 for (int r = 0; r < 32; ++r)
                     dst[r] = (col_ok && arow0 + r < p.M) ? src[(arow0 + r) * p.ldc] : __ushort_as_half(0);
             };
-            if constexpr (EPI == EPI_GENERIC) {
+            if constexpr (EB == EPI_GENERIC) {
                 if (use_c && !partial) load_c_chunk(0, cnext);
             }
             // TMA epilogue: request the C box (32 rows x 64 columns) of chunk c into staging
@@ -435,6 +438,25 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if (!ok) break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            // 32 accumulator columns of this thread's row as fp32 bits (fp16 accumulators widened).
+            auto acc_ld32 = [&](int col, uint32_t (&v)[32]) {
+                if constexpr (!ACC16) {
+                    tmem_ld_32x32b_x32(t_row + col, v);
+                    tmem_ld_wait();
+                } else {
+                    // an fp16 accumulator holds one element per 32-bit column; two
+                    // adjacent columns are packed into each register on the way out
+                    uint32_t h[16];
+                    tmem_ld_32x32b_x32_pack16(t_row + col, h);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h[q]));
+                        v[2 * q] = __float_as_uint(f.x);
+                        v[2 * q + 1] = __float_as_uint(f.y);
+                    }
+                }
+            };
 
             // Sum of all contributors' partials for this thread's row, columns
             // [col, col + NC), added in contributor order (deterministic).  Two
@@ -467,9 +489,12 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // (stream-K fixup, PARTS) from the sum of the contributors' partials.
             auto emit_tile = [&](auto parts_tag) {
                 constexpr bool PARTS = decltype(parts_tag)::value;
-                if constexpr (EPI == EPI_TMA || EPI == EPI_TMA_C) {
+                if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C) {
                     auto fetch64 = [&](int c, uint32_t (&v0)[32], uint32_t (&v1)[32]) {
-                        if constexpr (!PARTS) {
+                        if constexpr (!PARTS && ACC16) {
+                            acc_ld32(c * 64, v0);
+                            acc_ld32(c * 64 + 32, v1);
+                        } else if constexpr (!PARTS) {
                             tmem_ld_32x32b_x32(t_row + c * 64, v0);
                             tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
                             tmem_ld_wait();
@@ -562,18 +587,18 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             store_chunk(c, sb);
                         }
                     }
-                } else if constexpr (EPI == EPI_GENERIC || EPI == EPI_PARTIAL) {
+                } else if constexpr (EB == EPI_GENERIC || EB == EPI_PARTIAL) {
                     // Transpose each 32x32 block through padded shared memory so that a warp
                     // reads C and writes D along rows (coalesced), whatever the alignment.
                     float* T = reinterpret_cast<float*>(ebuf);
                     __half* Dp = static_cast<__half*>(p.D);
-                    if constexpr (EPI == EPI_GENERIC) {
+                    if constexpr (EB == EPI_GENERIC) {
                         if (use_c && PARTS) load_c_chunk(0, cnext);
                     }
 #pragma unroll 1
                     for (int c = 0; c < BN / 32; ++c) {
                         __half ccur[32];
-                        if constexpr (EPI == EPI_GENERIC) {
+                        if constexpr (EB == EPI_GENERIC) {
                             if (use_c) {
 #pragma unroll
                                 for (int r = 0; r < 32; ++r) ccur[r] = cnext[r];
@@ -584,8 +609,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         }
                         uint32_t v[32];
                         if constexpr (!PARTS) {
-                            tmem_ld_32x32b_x32(t_row + c * 32, v);
-                            tmem_ld_wait();
+                            acc_ld32(c * 32, v);
                         } else {
                             sum_parts(c * 32, v);
                         }
@@ -594,7 +618,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         __syncwarp();
                         const int64_t col = acol0 + c * 32 + lane;
                         if (col < p.N) {
-                            if constexpr (EPI == EPI_GENERIC) {
+                            if constexpr (EB == EPI_GENERIC) {
                                 __half* dst = Dp + static_cast<int64_t>(w.b) * p.strideD + col;
 #pragma unroll
                                 for (int r = 0; r < 32; ++r) {
@@ -631,7 +655,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             sum_parts(c * 16, v);
                         }
                         if (n < p.N) {
-                            if constexpr (EPI == EPI_SWAP) {
+                            if constexpr (EB == EPI_SWAP) {
                                 // all C loads of the chunk first, then the stores
                                 __half cv[16];
 #pragma unroll
@@ -706,7 +730,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             }
         }
-        if constexpr (EPI == EPI_TMA || EPI == EPI_TMA_C) {
+        if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C) {
             if (lane == 0) bulk_wait_group<0>();
             __syncwarp();
         }

@@ -18,14 +18,17 @@ static const TcVariant kVariants[] = {
     {256, 1, 4, EPI_TMA, 0, 0},
     {256, 1, 4, EPI_TMA_C, 0, 0},
     {256, 1, 4, EPI_TMA, 1, 0},
+    {256, 1, 4, EPI_TMA_A16, 0, 0},
     {256, 1, 4, EPI_TMA_C, 1, 0},
     {256, 2, 6, EPI_TMA, 0, 0},
     {256, 2, 6, EPI_TMA_C, 0, 0},
     {256, 2, 6, EPI_TMA, 1, 0},
+    {256, 2, 6, EPI_TMA_A16, 0, 0},
     {256, 2, 6, EPI_TMA_C, 1, 0},
     {128, 1, 6, EPI_TMA, 0, 0},
     {128, 1, 6, EPI_TMA_C, 0, 0},
     {128, 1, 6, EPI_TMA, 1, 0},
+    {128, 1, 6, EPI_TMA_A16, 0, 0},
     {128, 1, 6, EPI_TMA_C, 1, 0},
     {128, 2, 8, EPI_TMA, 0, 0},
     {128, 2, 8, EPI_TMA_C, 0, 0},
@@ -33,10 +36,13 @@ static const TcVariant kVariants[] = {
     {128, 2, 8, EPI_TMA_C, 1, 0},
     {256, 1, 4, EPI_GENERIC, 0, 0},
     {256, 1, 4, EPI_GENERIC, 1, 0},
+    {256, 1, 4, EPI_GENERIC_A16, 0, 0},
     {256, 2, 6, EPI_GENERIC, 0, 0},
     {256, 2, 6, EPI_GENERIC, 1, 0},
+    {256, 2, 6, EPI_GENERIC_A16, 0, 0},
     {128, 1, 6, EPI_GENERIC, 0, 0},
     {128, 1, 6, EPI_GENERIC, 1, 0},
+    {128, 1, 6, EPI_GENERIC_A16, 0, 0},
     {128, 1, 6, EPI_PARTIAL, 0, 0},
     {16, 1, 12, EPI_SWAP, 0, 0},
     {16, 1, 12, EPI_SWAP, 1, 0},

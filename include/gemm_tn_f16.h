@@ -136,6 +136,23 @@ GEMM_TN_API gemm_status_t gemm_f16(int32_t a_major, int32_t b_major,
                                    gemm_stream_t stream);
 
 /*
+ * gemm_f16 with the products accumulated in fp16 on the tensor core, as the
+ * "cute(8) smem_gemm" page's kernel does (GemmConfig: SM80_16x8x16_F16F16F16F16_TN).
+ * Faster on no shape here and far less accurate than gemm_f16 (every 16-wide K
+ * step rounds the running sum to fp16); provided for that page's semantics.
+ * alpha and beta are applied in fp32 to the fp16 accumulator, then D is rounded.
+ * Same arguments and rules as gemm_f16.
+ */
+GEMM_TN_API gemm_status_t gemm_f16_acc16(int32_t a_major, int32_t b_major,
+                                         const void* A, int64_t lda, int64_t strideA,
+                                         const void* B, int64_t ldb, int64_t strideB,
+                                         const void* C, int64_t ldc, int64_t strideC,
+                                         void* D, int64_t ldd, int64_t strideD,
+                                         int64_t M, int64_t N, int64_t K, int64_t batch,
+                                         float alpha, float beta,
+                                         gemm_stream_t stream);
+
+/*
  * Matrix transpose Y = X^T of the "10-mat-transpose-cute" page (y[c][r] = x[r][c]
  * for a rows x cols row-major x; predicated at ragged edges): fp32 (the page's
  * type) and fp16 elements, bits copied unchanged.
