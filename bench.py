@@ -64,11 +64,12 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(files):
+    """Hash of the CUDA sources the captured kernel is built from (names under csrc/)."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "dense_fp16_gemm_tn_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
-            h.update(os.path.basename(p).encode())
+    for name in sorted(files):
+        with open(os.path.join(ROOT, "dense_fp16_gemm_tn_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -83,7 +84,10 @@ def ncu_traffic(workload_key):
     except (OSError, ValueError):
         return None
     e = d.get(workload_key)
-    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+    try:
+        if not e or e.get("kernel_source_hash") != kernel_source_hash(e["sources"]):
+            return None
+    except (KeyError, OSError):
         return None
     return e.get("traffic_bytes_per_launch")
 
