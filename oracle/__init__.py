@@ -10,6 +10,9 @@ What it computes::
 
     D[b,m,n] = RNE_fp16(alpha * sum_k A[b,m,k] * B[b,n,k] + beta * C[b,m,n])
 
+and, for the fused score + softmax step, the softmax row statistics of
+S = alpha * Q K^T: m[b,i] = max_j S[b,i,j], l[b,i] = sum_j exp(S[b,i,j] - m[b,i]);
+
 in fp64 with one final rounding (see ``gemm_tn_oracle.h`` for the passages of
 the pages it follows: the TN inner product and ``axpby`` epilogue of the
 ``gemm_device`` walk-through, section 3, and the (M,K)/(N,K) stride-(K,1)
@@ -76,6 +79,10 @@ def _bind(path):
     lib.gto_transpose_u32.restype = None
     lib.gto_transpose_u16.argtypes = [u16p, i64, u16p, i64, i64, i64]
     lib.gto_transpose_u16.restype = None
+    f64p = ctypes.POINTER(ctypes.c_double)
+    lib.gto_score_softmax_stats.argtypes = [u16p, i64, i64, u16p, i64, i64, i64, i64, i64, ctypes.c_float,
+                                            f64p, f64p, i64, i64]
+    lib.gto_score_softmax_stats.restype = None
     return lib
 
 
@@ -131,6 +138,9 @@ class Oracle:
     def transpose(self, *args, **kw):
         return _transpose(self.lib, *args, **kw)
 
+    def score_softmax_stats(self, *args, **kw):
+        return _score_softmax_stats(self.lib, *args, **kw)
+
 
 def _u16ptr(a):
     if a is None:
@@ -161,6 +171,10 @@ def gemm_strided(*args, **kw):
 
 def transpose(*args, **kw):
     return _transpose(_load(), *args, **kw)
+
+
+def score_softmax_stats(*args, **kw):
+    return _score_softmax_stats(_load(), *args, **kw)
 
 
 def default_threads() -> int:
@@ -277,3 +291,34 @@ def _transpose(lib, X, rows, cols, *, ldx=None, ldy=None, Y=None):
     else:
         raise TypeError("uint32 or uint16 bit patterns expected")
     return Y
+
+
+def _score_softmax_stats(lib, Q, Kmat, M, N, d, alpha, *, ldq=None, ldk=None, batch=1, strideQ=None,
+                         strideK=None, rows=None, threads=None):
+    """Softmax row statistics of S = alpha * Q K^T per batch entry: returns (m, l), two
+    float64 arrays indexed r = b*M + i, with m = max_j S[i, j] and l = sum_j exp(S[i, j] - m).
+    Q, K are uint16 arrays of binary16 bits (M x d and N x d per batch entry, leading
+    dimensions ldq / ldk, batch strides strideQ / strideK).  ``rows`` = (r_begin, r_end)
+    restricts the work to those flattened rows (the others stay NaN)."""
+    ldq = d if ldq is None else ldq
+    ldk = d if ldk is None else ldk
+    strideQ = M * ldq if strideQ is None else strideQ
+    strideK = N * ldk if strideK is None else strideK
+    total = batch * M
+    m = np.full(max(total, 1), np.nan)
+    l = np.full(max(total, 1), np.nan)
+    r0, r1 = (0, total) if rows is None else rows
+    if r1 <= r0:
+        return m[:total], l[:total]
+    f64p = ctypes.POINTER(ctypes.c_double)
+    args_pre = (_u16ptr(Q), ldq, strideQ, _u16ptr(Kmat), ldk, strideK, M, N, d, float(alpha),
+                m.ctypes.data_as(f64p), l.ctypes.data_as(f64p))
+    nthr = default_threads() if threads is None else threads
+    if nthr <= 1 or (r1 - r0) * max(N, 1) * max(d, 1) < (1 << 21):
+        lib.gto_score_softmax_stats(*args_pre, r0, r1)
+        return m[:total], l[:total]
+    chunk = max(1, (r1 - r0 + 4 * nthr - 1) // (4 * nthr))
+    spans = [(r, min(r1, r + chunk)) for r in range(r0, r1, chunk)]
+    with ThreadPoolExecutor(max_workers=nthr) as ex:
+        list(ex.map(lambda sp: lib.gto_score_softmax_stats(*args_pre, sp[0], sp[1]), spans))
+    return m[:total], l[:total]

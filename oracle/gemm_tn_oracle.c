@@ -191,3 +191,40 @@ void gto_transpose_u16(const uint16_t* X, int64_t ldx, uint16_t* Y, int64_t ldy,
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < cols; ++c) Y[c * ldy + r] = X[r * ldx + c];
 }
+
+/* alpha * (k-ordered fp64 dot of one query row with one key row) */
+static double score(const uint16_t* q_row, const uint16_t* k_row, int64_t d, double alpha)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < d; ++k) acc += g_decode[q_row[k]] * g_decode[k_row[k]];
+    return alpha * acc;
+}
+
+/* Two passes over the keys: the maximum, then the sum of exp(s_j - max). */
+void gto_score_softmax_stats(const uint16_t* Q, int64_t ldq, int64_t strideQ,
+                             const uint16_t* K, int64_t ldk, int64_t strideK,
+                             int64_t M, int64_t N, int64_t d, float alpha,
+                             double* row_max, double* row_sum,
+                             int64_t r_begin, int64_t r_end)
+{
+    decode_table_init();
+    if (M <= 0) return;
+    const double al = (double)alpha;
+    for (int64_t r = r_begin; r < r_end; ++r) {
+        const int64_t b = r / M;
+        const int64_t i = r % M;
+        const uint16_t* q_row = Q + b * strideQ + i * ldq;
+        const uint16_t* k_base = K + b * strideK;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < N; ++j) {
+            const double s = score(q_row, k_base + j * ldk, d, al);
+            if (s > m) m = s;
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            l += exp(score(q_row, k_base + j * ldk, d, al) - m);
+        }
+        row_max[r] = m;
+        row_sum[r] = l;
+    }
+}

@@ -93,6 +93,28 @@ void gto_gemm_f16_strided(const uint16_t* A, int64_t a_rs, int64_t a_cs, int64_t
 void gto_transpose_u32(const uint32_t* X, int64_t ldx, uint32_t* Y, int64_t ldy, int64_t rows, int64_t cols);
 void gto_transpose_u16(const uint16_t* X, int64_t ldx, uint16_t* Y, int64_t ldy, int64_t rows, int64_t cols);
 
+/*
+ * Softmax row statistics of the scaled score matrix, the step that follows the
+ * score GEMM score = Q @ K.T of "为什么 cutlass_cute_tutorial_zh.md 中要用
+ * retile_D" (section 1: Q is the MMA's A operand, K its B operand, head_dim
+ * 64).  The pages stop at the score; the statistics are the textbook softmax
+ * normaliser, for batch entry b and query row i:
+ *
+ *   s_j      = alpha * sum_{k<d} Q[b][i][k] * K[b][j][k]      (fp64, k order)
+ *   m[b][i]  = max_{j<N} s_j
+ *   l[b][i]  = sum_{j<N} exp(s_j - m[b][i])                     (fp64, j order)
+ *
+ * so that softmax(s)_j = exp(s_j - m) / l and logsumexp(s) = m + log(l).
+ * Q is M x d (leading dimension ldq), K is N x d (ldk), batch strides strideQ,
+ * strideK; outputs are indexed r = b*M + i for rows r in [r_begin, r_end).
+ * N == 0 gives m = -inf and l = 0.  Inputs are finite.
+ */
+void gto_score_softmax_stats(const uint16_t* Q, int64_t ldq, int64_t strideQ,
+                             const uint16_t* K, int64_t ldk, int64_t strideK,
+                             int64_t M, int64_t N, int64_t d, float alpha,
+                             double* row_max, double* row_sum,
+                             int64_t r_begin, int64_t r_end);
+
 #ifdef __cplusplus
 }
 #endif

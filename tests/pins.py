@@ -11,7 +11,11 @@ and the mathematics of the TN GEMM fix:
 - identity and permutation matrices, the all-ones closed form, the transpose
   invariant D(A,B)^T = D(B,A), small-integer exactness against numpy's
   integer matmul, beta == 0 not reading C, leading-dimension padding never
-  being read, batched == per-batch.
+  being read, batched == per-batch;
+- softmax row statistics: exact scores from integer matmul with math.fsum of
+  math.exp, scipy's logsumexp, equal keys (l = N), the shift invariance of
+  softmax, dominant keys whose rivals underflow (l counts them), degenerate
+  sizes.
 
 The same checks run against deliberately broken copies of the oracle
 (tests/test_oracle_mutants.py) to show that each plausible slip fails at
@@ -358,6 +362,120 @@ def check_transpose(o, seed=15):
         yp = yp.reshape(cols, rows + 3)
         assert np.array_equal(yp[:, :rows], x.T) and (yp[:, rows:] == 9).all()
 
+
+# ------------------------------------------------- softmax row statistics
+
+def _small_ints(rng, shape, lo=-2, hi=2):
+    return rng.integers(lo, hi + 1, shape).astype(np.int64)
+
+
+def _padded_bits(x_int, ld):
+    """Rows of small integers as binary16 bits with NaN (0x7E00) padding up to ld."""
+    rows, cols = x_int.shape
+    out = np.full((rows, ld), 0x7E00, dtype=np.uint16)
+    out[:, :cols] = half_bits(x_int.astype(np.float64))
+    return out
+
+
+def check_softmax_exact_small_int(o, seed=21):
+    """Small integers, power-of-two alpha: every score is exact, so m must equal
+    alpha * max of numpy's integer matmul exactly, and l the correctly rounded sum
+    of exp over those exact scores (math.fsum of math.exp) to fp64 summation error.
+    Batched, with NaN-padded leading dimensions that must never be read."""
+    import math
+    rng = np.random.default_rng(seed)
+    batch, M, N, d = 2, 7, 29, 23
+    ldq, ldk = d + 3, d + 5
+    for alpha in (0.25, -0.5, 2.0):
+        Qi = _small_ints(rng, (batch, M, d))
+        Ki = _small_ints(rng, (batch, N, d))
+        Q = np.concatenate([_padded_bits(Qi[b], ldq).ravel() for b in range(batch)])
+        K = np.concatenate([_padded_bits(Ki[b], ldk).ravel() for b in range(batch)])
+        m, l = o.score_softmax_stats(Q, K, M, N, d, alpha, ldq=ldq, ldk=ldk, batch=batch)
+        for b in range(batch):
+            S = Qi[b] @ Ki[b].T  # exact integers
+            for i in range(M):
+                row = [alpha * float(v) for v in S[i]]
+                mref = max(row)
+                assert m[b * M + i] == mref, (b, i, m[b * M + i], mref)
+                lref = math.fsum(math.exp(v - mref) for v in row)
+                assert abs(l[b * M + i] - lref) <= 1e-13 * lref, (b, i, l[b * M + i], lref)
+
+
+def check_softmax_logsumexp(o, seed=22):
+    """N(0,1) fp16 inputs at the head width of the retile_D page (64): m against the
+    row maximum of numpy's fp64 matmul and m + log(l) against scipy's logsumexp."""
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(seed)
+    M, N, d, alpha = 6, 333, 64, 0.125
+    Q = half_bits(rng.standard_normal((M, d)))
+    K = half_bits(rng.standard_normal((N, d)))
+    S = alpha * (bits_to_f64(Q).reshape(M, d) @ bits_to_f64(K).reshape(N, d).T)
+    m, l = o.score_softmax_stats(Q, K, M, N, d, alpha)
+    assert np.allclose(m, S.max(axis=1), rtol=1e-13, atol=1e-13)
+    assert np.allclose(m + np.log(l), logsumexp(S, axis=1), rtol=1e-13, atol=1e-13)
+    # every term is at most 1 and the largest is 1
+    assert (l >= 1.0).all() and (l <= N).all()
+
+
+def check_softmax_equal_keys(o, seed=23):
+    """All keys equal: every score of a row is the same, so l = N exactly and m is
+    that score (rows of both signs, so an m started at 0 instead of -inf shows)."""
+    rng = np.random.default_rng(seed)
+    M, N, d, alpha = 9, 41, 16, 0.5
+    Qi = _small_ints(rng, (M, d))
+    v = _small_ints(rng, (d,))
+    Ki = np.tile(v, (N, 1))
+    m, l = o.score_softmax_stats(half_bits(Qi.astype(float)), half_bits(Ki.astype(float)), M, N, d, alpha)
+    s = alpha * (Qi @ v).astype(np.float64)
+    assert (s < 0).any() and (s > 0).any()
+    assert np.array_equal(m, s)
+    assert np.array_equal(l, np.full(M, float(N)))
+
+
+def check_softmax_shift_invariance(o, seed=24):
+    """Adding one vector c to every key shifts each row's scores by alpha*q.c:
+    m moves by exactly that and l does not change (all exact with small integers)."""
+    rng = np.random.default_rng(seed)
+    M, N, d, alpha = 8, 37, 19, 0.25
+    Qi = _small_ints(rng, (M, d))
+    Ki = _small_ints(rng, (N, d))
+    c = _small_ints(rng, (d,))
+    m0, l0 = o.score_softmax_stats(half_bits(Qi.astype(float)), half_bits(Ki.astype(float)), M, N, d, alpha)
+    m1, l1 = o.score_softmax_stats(half_bits(Qi.astype(float)), half_bits((Ki + c).astype(float)), M, N, d, alpha)
+    assert np.array_equal(m1, m0 + alpha * (Qi @ c).astype(np.float64))
+    assert np.array_equal(l1, l0)
+
+
+def check_softmax_dominant_keys(o):
+    """Keys are +v or -v with q.v = 1024: the -v terms underflow to exactly 0 in
+    exp, so l counts the +v keys, wherever they sit (first and last included)."""
+    M, N, d = 3, 50, 16
+    Q = np.full((M, d), 8.0)
+    hot = np.zeros(N, bool)
+    hot[[0, 7, 8, 23, N - 1]] = True
+    K = np.where(hot[:, None], 8.0, -8.0) * np.ones((N, d))
+    m, l = o.score_softmax_stats(half_bits(Q), half_bits(K), M, N, d, 1.0)
+    assert np.array_equal(m, np.full(M, 1024.0))
+    assert np.array_equal(l, np.full(M, float(hot.sum())))
+
+
+def check_softmax_degenerate(o):
+    """N = 1: l = 1, m = the score.  N = 0: m = -inf, l = 0.  d = 0: all scores 0."""
+    Q = half_bits(np.array([[1.0, 2.0, -3.0]]))
+    K = half_bits(np.array([[0.5, 0.25, 1.0]]))
+    m, l = o.score_softmax_stats(Q, K, 1, 1, 3, 2.0)
+    assert m[0] == 2.0 * (0.5 + 0.5 - 3.0) and l[0] == 1.0
+    m, l = o.score_softmax_stats(Q, K, 1, 0, 3, 2.0)
+    assert m[0] == -np.inf and l[0] == 0.0
+    m, l = o.score_softmax_stats(Q, np.zeros(4, np.uint16), 1, 4, 0, 2.0, ldq=3, ldk=1)
+    assert m[0] == 0.0 and l[0] == 4.0
+    m, l = o.score_softmax_stats(Q, K, 0, 1, 3, 2.0)
+    assert m.size == 0 and l.size == 0
+
+
+SOFTMAX_CHECKS = [check_softmax_exact_small_int, check_softmax_logsumexp, check_softmax_equal_keys,
+                  check_softmax_shift_invariance, check_softmax_dominant_keys, check_softmax_degenerate]
 
 GEMM_CHECKS = [check_bruteforce_exact, check_strided_layouts, check_identity, check_permutation, check_all_ones,
                check_transpose_invariant, check_small_integers, check_beta_zero_does_not_read_c,

@@ -29,6 +29,16 @@ MUTANTS = [
     ("strided_b_unit_row_stride", "B[b * strideB + n * b_rs + k * b_cs]", "B[b * strideB + n + k * b_cs]"),
     ("transpose_drops_last_row", "for (int64_t r = 0; r < rows; ++r)\n        for (int64_t c = 0; c < cols; ++c) Y[c * ldy + r] = X[r * ldx + c];\n}\n\nvoid gto_transpose_u16",
      "for (int64_t r = 0; r + 1 < rows; ++r)\n        for (int64_t c = 0; c < cols; ++c) Y[c * ldy + r] = X[r * ldx + c];\n}\n\nvoid gto_transpose_u16"),
+    ("softmax_sum_drops_last_key", "for (int64_t j = 0; j < N; ++j) {\n            l += exp(",
+     "for (int64_t j = 0; j + 1 < N; ++j) {\n            l += exp("),
+    ("softmax_max_skips_last_key", "for (int64_t j = 0; j < N; ++j) {\n            const double s =",
+     "for (int64_t j = 0; j + 1 < N; ++j) {\n            const double s ="),
+    ("softmax_exp_sign", "l += exp(score(q_row, k_base + j * ldk, d, al) - m);", "l += exp(m - score(q_row, k_base + j * ldk, d, al));"),
+    ("softmax_max_starts_at_zero", "double m = -INFINITY;", "double m = 0.0;"),
+    ("softmax_drops_alpha", "return alpha * acc;", "return acc;"),
+    ("softmax_key_uses_ldq", "const double s = score(q_row, k_base + j * ldk, d, al);", "const double s = score(q_row, k_base + j * ldq, d, al);"),
+    ("softmax_dot_skips_last", "for (int64_t k = 0; k < d; ++k) acc +=", "for (int64_t k = 0; k + 1 < d; ++k) acc +="),
+    ("softmax_key_batch_stride", "const uint16_t* k_base = K + b * strideK;", "const uint16_t* k_base = K + b * strideQ;"),
     ("flush_subnormals", "const int q = (E < -14) ? -24 : E - 10;", "const int q = (E < -14) ? 99 : E - 10;"),
 ]
 
@@ -43,7 +53,7 @@ def test_pins_catch_mutant(tmp_path, name, old, new):
     lib = oracle.compile_source(str(path), str(tmp_path / f"lib_{name}.so"))
     o = oracle.Oracle.from_path(lib)
     failures = []
-    for check in pins.CONVERSION_CHECKS[:3] + pins.GEMM_CHECKS:
+    for check in pins.CONVERSION_CHECKS[:3] + pins.GEMM_CHECKS + pins.SOFTMAX_CHECKS:
         try:
             check(o)
         except AssertionError:
