@@ -319,6 +319,63 @@ def time_transpose(G, device, flush_buf, read_buf, peaks, n=1024, steps=50):
             "page_context": "0.0039 ms best on an RTX 4090 (transpose page's table; other hardware)"}
 
 
+MUFU_EX2_PER_CLK_SM = 16  # special-function unit: exp2 results per clock per SM
+
+
+def time_score_softmax(G, device, flush_buf, read_buf, peaks, sms, steps=10):
+    """Fused score + softmax statistics on the score workload (128 heads, Q, K 4096 x 64,
+    N(0,1), alpha 1/8): the 4 GiB score matrix is never stored.  The bound is the exp2
+    rate of the special-function units (one exp per score), derived from the unit
+    count and the maximum SM clock."""
+    import torch
+    from dense_fp16_gemm_tn_gb300 import inputs
+    w = inputs.WORKLOADS["score_qk"]
+    g = torch.Generator(device=device)
+    g.manual_seed(3000)
+    Q = torch.randn((w.batch, w.M, w.K), generator=g, device=device).half()
+    K = torch.randn((w.batch, w.N, w.K), generator=g, device=device).half()
+    m = torch.empty((w.batch * w.M,), dtype=torch.float32, device=device)
+    l = torch.empty_like(m)
+
+    def call():
+        G.score_softmax_stats_f16(Q, w.K, w.M * w.K, K, w.K, w.N * w.K, m, l, w.M, w.N, w.K, w.batch, w.alpha)
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    ts = []
+    for i in range(steps):
+        flush_l2(flush_buf, read_buf, i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    st = G.gemm_tn_f16_last_device_error()
+    if st != G.GEMM_OK:
+        raise RuntimeError(f"device error in score+softmax timing: {G.gemm_status_string(st)}")
+    ms = statistics.median([a.elapsed_time(b) for a, b in ts])
+    scores = w.batch * w.M * w.N
+    try:
+        max_mhz = float(subprocess.run(["nvidia-smi", "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits",
+                                        "-i", str(device.index or 0)], capture_output=True, text=True,
+                                       timeout=10).stdout.split()[0])
+    except (OSError, ValueError, IndexError, subprocess.TimeoutExpired):
+        max_mhz = 2070.0
+    exp_peak = sms * MUFU_EX2_PER_CLK_SM * max_mhz * 1e6  # exp2 per second
+    achieved = scores / (ms * 1e-3)
+    return {"workload": "fused score + scale + online softmax statistics, 128 heads, Q,K [4096,64] N(0,1), "
+                        "alpha=1/8; outputs row max and row sum (fp32)",
+            "ms": ms, "tflops": w.flops / (ms * 1e-3) / 1e12,
+            "scores_per_s": achieved,
+            "roofline": {"bound": "alu", "achieved": achieved / 1e9, "peak": exp_peak / 1e9, "unit": "Gexp/s",
+                         "frac": achieved / exp_peak,
+                         "peak_source": f"{sms} SMs x {MUFU_EX2_PER_CLK_SM} exp2/clk x {max_mhz:.0f} MHz"},
+            "hbm_gbs": (2 * (w.M + w.N) * w.K * w.batch + 8 * w.batch * w.M) / (ms * 1e-3) / 1e9,
+            "l2": "flushed before every step"}
+
+
 def roofline_tflops(w, peaks):
     tensor = peaks["bf16_tflops"]
     hbm = peaks["hbm_gbs"] * 1e9
@@ -481,6 +538,7 @@ def run_ours(args, rank, world, dist):
         if st != G.GEMM_OK:
             raise RuntimeError(f"device error in per-config timing: {G.gemm_status_string(st)}")
         per_config["transpose_f32_1024"] = time_transpose(G, device, flush, read_buf, peaks)
+        per_config["score_softmax"] = time_score_softmax(G, device, flush, read_buf, peaks, sms)
 
     if rank != 0:
         return

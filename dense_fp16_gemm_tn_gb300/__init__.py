@@ -38,6 +38,7 @@ from ._binding import (  # noqa: F401
     gemm_tn_f16_last_device_error,
     gemm_tn_f16_plan,
     gemm_tn_f16_set_option,
+    score_softmax_stats_f16,
     gemm_tn_f16_shutdown,
     gemm_tn_f16_splitk_static,
     gemm_tn_f16_version,

@@ -36,7 +36,8 @@ GEMM_TN_OPT_STREAM_K = 9
 
 EXPORTED = ["gemm_tn_f16", "gemm_tn_f16_batched", "gemm_status_string", "gemm_tn_f16_last_device_error",
             "gemm_tn_f16_last_cuda_error", "gemm_tn_f16_shutdown", "gemm_tn_f16_version", "gemm_tn_f16_plan",
-            "gemm_tn_f16_set_option", "gemm_tn_f16_get_option", "gemm_tn_f16_splitk_static", "gemm_f16", "transpose_f32", "transpose_f16", "gemm_f16_acc16"]
+            "gemm_tn_f16_set_option", "gemm_tn_f16_get_option", "gemm_tn_f16_splitk_static", "gemm_f16", "transpose_f32", "transpose_f16", "gemm_f16_acc16",
+            "score_softmax_stats_f16"]
 
 GEMM_K_MAJOR = 0
 GEMM_MN_MAJOR = 1
@@ -113,6 +114,8 @@ def load_library(build_if_missing: bool = True):
         lib.gemm_f16.restype = ctypes.c_int
         lib.gemm_f16_acc16.argtypes = lib.gemm_f16.argtypes
         lib.gemm_f16_acc16.restype = ctypes.c_int
+        lib.score_softmax_stats_f16.argtypes = [vp, i64, i64, vp, i64, i64, vp, vp, i64, i64, i64, i64, f32, vp]
+        lib.score_softmax_stats_f16.restype = ctypes.c_int
         for name in ("transpose_f32", "transpose_f16"):
             getattr(lib, name).argtypes = [vp, i64, vp, i64, i64, i64, vp]
             getattr(lib, name).restype = ctypes.c_int
@@ -170,6 +173,14 @@ def gemm_f16_acc16(a_major, b_major, A, lda, strideA, B, ldb, strideB, C, ldc, s
                                        _ptr(C), ldc, strideC, _ptr(D), ldd, strideD, M, N, K, batch,
                                        float(alpha), float(beta), _stream(stream))
     return _check(st, "gemm_f16_acc16", check)
+
+
+def score_softmax_stats_f16(Q, ldq, strideQ, K, ldk, strideK, row_max, row_sum, M, N, d, batch, alpha,
+                            stream=None, *, check=True):
+    """Softmax row statistics of S = alpha * Q K^T (fp32 row_max, row_sum); S is never stored."""
+    st = load_library().score_softmax_stats_f16(_ptr(Q), ldq, strideQ, _ptr(K), ldk, strideK, _ptr(row_max),
+                                                _ptr(row_sum), M, N, d, batch, float(alpha), _stream(stream))
+    return _check(st, "score_softmax_stats_f16", check)
 
 
 def transpose_f32(X, ldx, Y, ldy, rows, cols, stream=None, *, check=True):

@@ -15,6 +15,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <limits>
 #include <mutex>
 
 #include "gemm_tn_f16.h"
@@ -577,6 +578,109 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     return GEMM_OK;
 }
 
+// Fused score + softmax statistics: validation, optional repack of operands TMA
+// cannot fetch as they are, tensor maps, launch.
+gemm_status_t run_softmax(const void* Q, int64_t ldq, int64_t strideQ, const void* K, int64_t ldk, int64_t strideK,
+                          float* row_max, float* row_sum, int64_t M, int64_t N, int64_t d, int64_t batch, float alpha,
+                          cudaStream_t stream) {
+    if (M < 0 || N < 0 || d < 0 || batch < 0) return GEMM_ERR_INVALID_VALUE;
+    const int64_t lim = int64_t(1) << 31;
+    if (M >= lim || N >= lim || batch >= lim) return GEMM_ERR_UNSUPPORTED;
+    if (d > 256) return GEMM_ERR_UNSUPPORTED;
+    if (M == 0 || batch == 0) return GEMM_OK;
+    if (!row_max || !row_sum) return GEMM_ERR_INVALID_VALUE;
+    if ((reinterpret_cast<uintptr_t>(row_max) & 3u) || (reinterpret_cast<uintptr_t>(row_sum) & 3u))
+        return GEMM_ERR_MISALIGNED;
+    const int64_t rows = batch * M;
+    if (ranges_overlap(row_max, 4 * rows, row_sum, 4 * rows)) return GEMM_ERR_INVALID_VALUE;
+    const bool live = N > 0 && d > 0;  // otherwise the statistics are constants
+    if (live) {
+        if (!Q || !K || ldq < d || ldk < d) return GEMM_ERR_INVALID_VALUE;
+        if (batch > 1 && (strideQ < 0 || strideK < 0)) return GEMM_ERR_INVALID_VALUE;
+        if ((reinterpret_cast<uintptr_t>(Q) & 1u) || (reinterpret_cast<uintptr_t>(K) & 1u)) return GEMM_ERR_MISALIGNED;
+        const int64_t q_bytes = extent_bytes(M, d, ldq, strideQ, batch);
+        const int64_t k_bytes = extent_bytes(N, d, ldk, strideK, batch);
+        if (ranges_overlap(row_max, 4 * rows, Q, q_bytes) || ranges_overlap(row_sum, 4 * rows, Q, q_bytes) ||
+            ranges_overlap(row_max, 4 * rows, K, k_bytes) || ranges_overlap(row_sum, 4 * rows, K, k_bytes))
+            return GEMM_ERR_INVALID_VALUE;
+    }
+
+    DeviceState* dev = nullptr;
+    gemm_status_t st = device_state(&dev);
+    if (st != GEMM_OK) return st;
+    cudaError_t e;
+    if (!live) {
+        // N == 0: empty maximum and sum.  d == 0: every score is 0, so m = 0 and l = N.
+        const float mv = N == 0 ? -std::numeric_limits<float>::infinity() : 0.0f;
+        const float lv = static_cast<float>(N);
+        e = launch_fill_stats(row_max, row_sum, rows, mv, lv, dev->sms, stream);
+        return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+    }
+
+    const bool q_batched = batch > 1 && strideQ != 0;
+    const bool k_batched = batch > 1 && strideK != 0;
+    const int kq = d <= 64 ? 1 : d <= 128 ? 2 : 4;
+    CUtensorMap mapQ, mapK;
+    bool pack_q = !operand_tma_ok(aligned16(Q), ldq, strideQ, q_batched ? batch : 1) ||
+                  !encode_map(&mapQ, Q, d, M, batch, ldq, strideQ, q_batched, 64, 128);
+    bool pack_k = !operand_tma_ok(aligned16(K), ldk, strideK, k_batched ? batch : 1) ||
+                  !encode_map(&mapK, K, d, N, batch, ldk, strideK, k_batched, 64, 256);
+    const int64_t ldo = round_up(d, 8);
+    const int64_t q_pack_bytes = pack_q ? round_up((q_batched ? batch : 1) * M * ldo * 2, 256) : 0;
+    const int64_t k_pack_bytes = pack_k ? round_up((k_batched ? batch : 1) * N * ldo * 2, 256) : 0;
+    uint8_t* ws = nullptr;
+    if (q_pack_bytes + k_pack_bytes > 0) {
+        e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), static_cast<size_t>(q_pack_bytes + k_pack_bytes),
+                                    dev->pool, stream);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return GEMM_ERR_WORKSPACE;
+        }
+    }
+    auto release = [&]() {
+        if (ws) cudaFreeAsync(ws, stream);
+    };
+    RepackArgs jobs[2];
+    int njobs = 0;
+    if (pack_q) {
+        jobs[njobs++] = {Q, ldq, strideQ, ws, ldo, M, d, q_batched ? batch : 1};
+        if (!encode_map(&mapQ, ws, d, M, batch, ldo, M * ldo, q_batched, 64, 128)) {
+            release();
+            return GEMM_ERR_UNSUPPORTED;
+        }
+    }
+    if (pack_k) {
+        jobs[njobs++] = {K, ldk, strideK, ws + q_pack_bytes, ldo, N, d, k_batched ? batch : 1};
+        if (!encode_map(&mapK, ws + q_pack_bytes, d, N, batch, ldo, N * ldo, k_batched, 64, 256)) {
+            release();
+            return GEMM_ERR_UNSUPPORTED;
+        }
+    }
+    if (njobs > 0) {
+        e = launch_repack(jobs, njobs, dev->sms, stream);
+        if (e != cudaSuccess) { release(); return cuda_fail(e); }
+    }
+
+    SoftmaxParams sp;
+    std::memset(&sp, 0, sizeof(sp));
+    sp.M = static_cast<int32_t>(M);
+    sp.N = static_cast<int32_t>(N);
+    sp.mblocks = static_cast<int32_t>(ceil_div(M, 128));
+    sp.ntiles = static_cast<int32_t>(ceil_div(N, 256));
+    sp.num_units = batch * sp.mblocks;
+    sp.alpha = alpha;
+    sp.sc = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634074);  // alpha * log2(e)
+    sp.row_max = row_max;
+    sp.row_sum = row_sum;
+    sp.err = dev->err;
+    sp.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
+    sp.zq = q_batched ? 1 : 0;
+    sp.zk = k_batched ? 1 : 0;
+    e = launch_score_softmax(mapQ, mapK, sp, kq, dev->sms, stream);
+    release();
+    return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+}
+
 }  // namespace
 }  // namespace gtn
 
@@ -622,6 +726,13 @@ gemm_status_t gemm_f16_acc16(int32_t a_major, int32_t b_major, const void* A, in
     p.b_mn = b_major == GEMM_MN_MAJOR ? 1 : 0;
     p.acc16 = 1;
     return run(A, B, C, D, p, alpha, reinterpret_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t score_softmax_stats_f16(const void* Q, int64_t ldq, int64_t strideQ, const void* K, int64_t ldk,
+                                      int64_t strideK, float* row_max, float* row_sum, int64_t M, int64_t N, int64_t d,
+                                      int64_t batch, float alpha, gemm_stream_t stream) {
+    return run_softmax(Q, ldq, strideQ, K, ldk, strideK, row_max, row_sum, M, N, d, batch, alpha,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char* gemm_status_string(gemm_status_t s) {

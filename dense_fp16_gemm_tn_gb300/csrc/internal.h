@@ -52,4 +52,24 @@ cudaError_t launch_splitk_reduce(const float* W, int32_t splits, int64_t M, int6
 cudaError_t launch_scale(int64_t M, int64_t N, int64_t batch, float beta, const void* C, int64_t ldc,
                          int64_t strideC, void* D, int64_t ldd, int64_t strideD, int sms, cudaStream_t stream);
 
+// Fused score + softmax statistics kernel (score_softmax.cu).
+struct SoftmaxParams {
+    int32_t M, N;           // query rows and keys per batch entry
+    int32_t mblocks;        // ceil(M / 128)
+    int32_t ntiles;         // ceil(N / 256)
+    int64_t num_units;      // batch * mblocks
+    float alpha;            // score scale
+    float sc;               // alpha * log2(e)
+    float* row_max;         // [batch * M]
+    float* row_sum;         // [batch * M]
+    uint32_t* err;          // device error word
+    uint64_t timeout_ns;    // bound on every wait
+    int32_t zq, zk;         // 1: operand has a batch dimension in its tensor map
+};
+// kq = number of 64-wide blocks of the head dimension (1, 2 or 4).
+cudaError_t launch_score_softmax(const CUtensorMap& tmQ, const CUtensorMap& tmK, const SoftmaxParams& p, int kq,
+                                 int sms, cudaStream_t stream);
+// m[i] = mv, l[i] = lv for i < n.
+cudaError_t launch_fill_stats(float* m, float* l, int64_t n, float mv, float lv, int sms, cudaStream_t stream);
+
 }  // namespace gtn

@@ -153,6 +153,36 @@ GEMM_TN_API gemm_status_t gemm_f16_acc16(int32_t a_major, int32_t b_major,
                                          gemm_stream_t stream);
 
 /*
+ * Fused score GEMM + scale + softmax statistics.  The score is the Q @ K.T of the
+ * "为什么 cutlass_cute_tutorial_zh.md 中要用 retile_D" page (section 1: Q is the
+ * MMA's A operand, K its B operand; head_dim 64 there); the pages stop at the
+ * score, and this call continues with the softmax normaliser of each score row,
+ * computed online so that the score matrix is never stored:
+ *
+ *   s_ij          = alpha * sum_{k<d} Q[b][i][k] * K[b][j][k]   (fp32 accumulate)
+ *   row_max[b*M+i] = max_j s_ij
+ *   row_sum[b*M+i] = sum_j exp(s_ij - row_max[b*M+i])
+ *
+ * so softmax(s_i)_j = exp(s_ij - row_max) / row_sum and logsumexp = row_max + log(row_sum).
+ * Q: M x d per batch entry, row-major with leading dimension ldq >= d; K: N x d,
+ * ldk >= d; strideQ / strideK between batch entries (0 broadcasts one operand).
+ * row_max, row_sum: batch * M fp32 each, device memory, 4-byte aligned, written
+ * only (they must not overlap each other or Q, K: GEMM_ERR_INVALID_VALUE).
+ * d <= 256 (GEMM_ERR_UNSUPPORTED above).  Q and K need only 2-byte alignment:
+ * operands whose rows are not 16-byte aligned are first copied to an aligned
+ * scratch copy from the library's stream-ordered pool (GEMM_ERR_WORKSPACE if that
+ * fails).  M == 0 or batch == 0 does nothing; N == 0 gives row_max = -inf,
+ * row_sum = 0; d == 0 gives row_max = 0, row_sum = N.  Inputs are finite.
+ * Asynchronous on `stream`; a device-side wait that times out is reported by
+ * gemm_tn_f16_last_device_error().
+ */
+GEMM_TN_API gemm_status_t score_softmax_stats_f16(const void* Q, int64_t ldq, int64_t strideQ,
+                                                  const void* K, int64_t ldk, int64_t strideK,
+                                                  float* row_max, float* row_sum,
+                                                  int64_t M, int64_t N, int64_t d, int64_t batch,
+                                                  float alpha, gemm_stream_t stream);
+
+/*
  * Matrix transpose Y = X^T of the "10-mat-transpose-cute" page (y[c][r] = x[r][c]
  * for a rows x cols row-major x; predicated at ragged edges): fp32 (the page's
  * type) and fp16 elements, bits copied unchanged.

@@ -216,3 +216,25 @@ def test_transpose_host_checks_without_a_gpu():
     assert G.transpose_f32(0x1000, 4, 0x9000, 8, 8, 8, check=False) == G.GEMM_ERR_INVALID_VALUE
     assert G.transpose_f16(0x1001, 8, 0x9000, 8, 8, 8, check=False) == G.GEMM_ERR_MISALIGNED
     assert G.transpose_f32(0x1000, 8, 0x1010, 8, 8, 8, check=False) == G.GEMM_ERR_INVALID_VALUE
+
+
+def test_score_softmax_host_checks_without_a_gpu():
+    f = G.score_softmax_stats_f16
+    Q, K, m, l = 0x100000, 0x200000, 0x300000, 0x400000
+    # empty problems: nothing to do, no CUDA call
+    assert f(None, 64, 0, None, 64, 0, None, None, 0, 16, 64, 1, 0.125, check=False) == G.GEMM_OK
+    assert f(None, 64, 0, None, 64, 0, None, None, 16, 16, 64, 0, 0.125, check=False) == G.GEMM_OK
+    # negative sizes, missing outputs, short leading dimensions
+    assert f(Q, 64, 0, K, 64, 0, m, l, -1, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_INVALID_VALUE
+    assert f(Q, 64, 0, K, 64, 0, None, l, 16, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_INVALID_VALUE
+    assert f(Q, 32, 0, K, 64, 0, m, l, 16, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_INVALID_VALUE
+    assert f(Q, 64, 0, K, 32, 0, m, l, 16, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_INVALID_VALUE
+    assert f(None, 64, 0, K, 64, 0, m, l, 16, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_INVALID_VALUE
+    # head dimension limit and output alignment
+    assert f(Q, 512, 0, K, 512, 0, m, l, 16, 16, 257, 1, 0.125, check=False) == G.GEMM_ERR_UNSUPPORTED
+    assert f(Q, 64, 0, K, 64, 0, m + 2, l, 16, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_MISALIGNED
+    assert f(Q + 1, 64, 0, K, 64, 0, m, l, 16, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_MISALIGNED
+    # outputs overlapping each other or an input
+    assert f(Q, 64, 0, K, 64, 0, m, m + 32, 16, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_INVALID_VALUE
+    assert f(Q, 64, 0, K, 64, 0, Q + 64, l, 16, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_INVALID_VALUE
+    assert f(Q, 64, 0, K, 64, 0, m, K + 128, 16, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_INVALID_VALUE
