@@ -319,7 +319,7 @@ def time_transpose(G, device, flush_buf, read_buf, peaks, n=1024, steps=50):
             "page_context": "0.0039 ms best on an RTX 4090 (transpose page's table; other hardware)"}
 
 
-MUFU_EX2_PER_CLK_SM = 16  # special-function unit: exp2 results per clock per SM
+MUFU_EX2_PER_CLK_SM = 32  # special-function unit: exp2 results per clock per SM on this part
 
 
 def time_score_softmax(G, device, flush_buf, read_buf, peaks, sms, steps=10):

@@ -622,9 +622,10 @@ gemm_status_t run_softmax(const void* Q, int64_t ldq, int64_t strideQ, const voi
     const int kq = d <= 64 ? 1 : d <= 128 ? 2 : 4;
     CUtensorMap mapQ, mapK;
     bool pack_q = !operand_tma_ok(aligned16(Q), ldq, strideQ, q_batched ? batch : 1) ||
-                  !encode_map(&mapQ, Q, d, M, batch, ldq, strideQ, q_batched, 64, 128);
+                  !encode_map(&mapQ, Q, d, M, batch, ldq, strideQ, q_batched, 64, kSoftmaxTileM);
+    const uint32_t key_box = static_cast<uint32_t>(softmax_tile_n());
     bool pack_k = !operand_tma_ok(aligned16(K), ldk, strideK, k_batched ? batch : 1) ||
-                  !encode_map(&mapK, K, d, N, batch, ldk, strideK, k_batched, 64, 256);
+                  !encode_map(&mapK, K, d, N, batch, ldk, strideK, k_batched, 64, key_box);
     const int64_t ldo = round_up(d, 8);
     const int64_t q_pack_bytes = pack_q ? round_up((q_batched ? batch : 1) * M * ldo * 2, 256) : 0;
     const int64_t k_pack_bytes = pack_k ? round_up((k_batched ? batch : 1) * N * ldo * 2, 256) : 0;
@@ -644,14 +645,14 @@ gemm_status_t run_softmax(const void* Q, int64_t ldq, int64_t strideQ, const voi
     int njobs = 0;
     if (pack_q) {
         jobs[njobs++] = {Q, ldq, strideQ, ws, ldo, M, d, q_batched ? batch : 1};
-        if (!encode_map(&mapQ, ws, d, M, batch, ldo, M * ldo, q_batched, 64, 128)) {
+        if (!encode_map(&mapQ, ws, d, M, batch, ldo, M * ldo, q_batched, 64, kSoftmaxTileM)) {
             release();
             return GEMM_ERR_UNSUPPORTED;
         }
     }
     if (pack_k) {
         jobs[njobs++] = {K, ldk, strideK, ws + q_pack_bytes, ldo, N, d, k_batched ? batch : 1};
-        if (!encode_map(&mapK, ws + q_pack_bytes, d, N, batch, ldo, N * ldo, k_batched, 64, 256)) {
+        if (!encode_map(&mapK, ws + q_pack_bytes, d, N, batch, ldo, N * ldo, k_batched, 64, key_box)) {
             release();
             return GEMM_ERR_UNSUPPORTED;
         }
@@ -665,8 +666,8 @@ gemm_status_t run_softmax(const void* Q, int64_t ldq, int64_t strideQ, const voi
     std::memset(&sp, 0, sizeof(sp));
     sp.M = static_cast<int32_t>(M);
     sp.N = static_cast<int32_t>(N);
-    sp.mblocks = static_cast<int32_t>(ceil_div(M, 128));
-    sp.ntiles = static_cast<int32_t>(ceil_div(N, 256));
+    sp.mblocks = static_cast<int32_t>(ceil_div(M, kSoftmaxTileM));
+    sp.ntiles = static_cast<int32_t>(ceil_div(N, softmax_tile_n()));
     sp.num_units = batch * sp.mblocks;
     sp.alpha = alpha;
     sp.sc = static_cast<float>(static_cast<double>(alpha) * 1.4426950408889634074);  // alpha * log2(e)

@@ -53,10 +53,13 @@ cudaError_t launch_scale(int64_t M, int64_t N, int64_t batch, float beta, const 
                          int64_t strideC, void* D, int64_t ldd, int64_t strideD, int sms, cudaStream_t stream);
 
 // Fused score + softmax statistics kernel (score_softmax.cu).
+constexpr int kSoftmaxTileM = 128;  // query rows per work unit
+// Keys per score tile of the compiled kernel (the row count of its key boxes).
+int softmax_tile_n();
 struct SoftmaxParams {
     int32_t M, N;           // query rows and keys per batch entry
-    int32_t mblocks;        // ceil(M / 128)
-    int32_t ntiles;         // ceil(N / 256)
+    int32_t mblocks;        // ceil(M / kSoftmaxTileM)
+    int32_t ntiles;         // ceil(N / softmax_tile_n())
     int64_t num_units;      // batch * mblocks
     float alpha;            // score scale
     float sc;               // alpha * log2(e)

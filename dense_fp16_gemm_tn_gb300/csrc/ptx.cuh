@@ -75,6 +75,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same with an explicit bound on how long the thread may be suspended inside
+// the instruction (nanoseconds).  Without one the suspension limit is the
+// system's, and a waiter can observe a completed phase hundreds of cycles late.
+__device__ __forceinline__ bool mbar_try_wait_ns(uint32_t bar, uint32_t parity, uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // ------------------------------------------------------------------ fences / cluster barrier
 
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -17,11 +17,13 @@
 //   warp 1      tcgen05.mma issuer: S tile (128 x 256, fp32) into one of two
 //               tensor-memory buffers (2 x 256 columns);
 //   warps 2-9   softmax: warp w reads tensor-memory lanes 32*(w%4).. (one query
-//               row per thread) and one half (128 columns) of each S tile; it
-//               keeps the row's running extreme of the raw scores and the sum of
-//               2^(t - t_max) in base-2 units (t = s * log2 e), rescaling the sum
-//               when the maximum grows; the two column halves of a row are merged
-//               through shared memory at the end of the unit.
+//               row per thread) of every other S tile (the tiles of buffer
+//               (w-2)/4), so the two warps sharing a lane quarter alternate between
+//               loading and folding; each keeps the row's running extreme of the
+//               raw scores and the sum of 2^(t - t_max) in base-2 units
+//               (t = s * log2 e), rescaling the sum when the maximum grows; the two
+//               partial states of a row are merged through shared memory at the
+//               end of the unit.
 // Every wait is bounded (same error word and abort protocol as the GEMM).
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -34,8 +36,8 @@
 namespace gtn {
 namespace {
 
-constexpr int SM_BM = 128;         // query rows per unit
-constexpr int SM_BN = 256;         // keys per S tile
+constexpr int SM_BM = kSoftmaxTileM;  // query rows per unit
+constexpr int SM_BN = 256;            // keys per S tile
 constexpr int SM_BK = 64;          // halves per box row (128 bytes)
 constexpr int SM_EPI_WARPS = 8;
 constexpr int SM_THREADS = 32 * (2 + SM_EPI_WARPS);
@@ -58,6 +60,7 @@ struct SmCfg {
     static constexpr uint32_t OFF_ABORT = OFF_TMEM_SLOT + 8;
     static constexpr uint32_t SMEM = OFF_ABORT + 8 + 1024;  // + alignment slack
     static_assert(STAGES >= 2, "key ring too shallow");
+    static_assert(SM_BM == 128 && SM_BN == 256, "one tensor-memory lane per query row; two 128-column halves");
     static_assert(SMEM <= 232448, "shared memory budget");
 };
 
@@ -92,11 +95,15 @@ __device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32]) {
         : "memory");
 }
 
+// Waits here sit on the critical path of a tight producer/consumer chain: a short
+// suspension bound lets a waiter see a completed phase promptly.
+constexpr uint32_t kSuspendNs = 32;
+
 static __device__ __noinline__ bool sm_wait_slow(uint32_t bar, uint32_t parity, uint32_t* err, uint64_t timeout_ns,
                                                  volatile int* abort_flag, uint32_t who) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_ns(bar, parity, kSuspendNs)) return true;
         if ((i & 15u) == 0) {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > timeout_ns) {
@@ -116,18 +123,21 @@ __device__ __forceinline__ void sm_spin_ns(uint64_t ns) {
 
 __device__ __forceinline__ bool sm_wait(uint32_t bar, uint32_t parity, uint32_t* err, uint64_t timeout_ns,
                                         volatile int* abort_flag, uint32_t who) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_ns(bar, parity, kSuspendNs)) return true;
     return sm_wait_slow(bar, parity, err, timeout_ns, abort_flag, who);
 }
 
-// Running state of one query row over one column half: the extreme (maximum for
-// alpha >= 0, minimum for alpha < 0) of the raw fp32 scores seen so far, and the
-// sum of 2^(t - t_ext) over them, t = score * sc with sc = alpha * log2(e).
+// Running state of one query row over the columns one warp has folded: the
+// extreme (maximum for alpha >= 0, minimum for alpha < 0) of the raw fp32 scores,
+// and the sum of 2^(t - ref), t = score * sc with sc = alpha * log2(e), where the
+// reference ref is the base-2 running maximum ext * sc.
 struct RowState {
     float ext;  // raw score extreme (+-inf before the first column)
-    float mt;   // ext * sc, the base-2 running maximum (-inf before the first column)
-    float l;    // sum of 2^(t_j - mt)
+    float ref;  // ext * sc (-inf before the first column)
+    float l;    // sum of 2^(t_j - ref)
 };
+
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
 
 // Folds 32 consecutive scores (the first `valid` of them real columns) into the state.
 template <bool NEG, bool MASKED>
@@ -150,35 +160,108 @@ __device__ __forceinline__ void fold_chunk(const uint32_t (&r)[32], int valid, f
     float b3 = NEG ? min3f(a[9], a[10], st.ext) : max3f(a[9], a[10], st.ext);
     const float e2 = NEG ? fminf(fminf(b0, b1), fminf(b2, b3)) : fmaxf(fmaxf(b0, b1), fmaxf(b2, b3));
     const float mt2 = e2 * sc;
-    // rescale the sum when the maximum moved (2^(-inf) = 0 clears the empty start)
-    const float f = ex2_approx(st.mt - mt2);
-    st.l = (mt2 == st.mt) ? st.l : st.l * f;
-    st.mt = mt2;
+    // move the reference to the running maximum, rescaling the sum (2^(-inf) = 0
+    // clears the empty start)
+    const float f = ex2_approx(st.ref - mt2);
+    st.l = (mt2 == st.ref) ? st.l : st.l * f;
+    st.ref = mt2;
     st.ext = e2;
-    const float nm = -mt2;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    const float2 sc2 = f2(sc), nm2 = f2(-mt2);
+    float2 s0 = f2(0.f), s1 = f2(0.f);
 #pragma unroll
-    for (int k = 0; k < 32; k += 4) {
-        float x0 = fmaf(v[k + 0], sc, nm), x1 = fmaf(v[k + 1], sc, nm);
-        float x2 = fmaf(v[k + 2], sc, nm), x3 = fmaf(v[k + 3], sc, nm);
+    for (int k = 0; k < 32; k += 2) {
+        // exponent arguments t - t_max, two columns per instruction
+        float2 x = __ffma2_rn(make_float2(v[k], v[k + 1]), sc2, nm2);
+        float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
         if (MASKED) {
-            const float ninf = __int_as_float(0xff800000);
-            if (k + 0 >= valid) x0 = ninf;
-            if (k + 1 >= valid) x1 = ninf;
-            if (k + 2 >= valid) x2 = ninf;
-            if (k + 3 >= valid) x3 = ninf;
+            if (k >= valid) e.x = 0.f;
+            if (k + 1 >= valid) e.y = 0.f;
         }
-        s0 += ex2_approx(x0);
-        s1 += ex2_approx(x1);
-        s2 += ex2_approx(x2);
-        s3 += ex2_approx(x3);
+        if ((k >> 1) & 1) s1 = __fadd2_rn(s1, e);
+        else s0 = __fadd2_rn(s0, e);
     }
-    st.l += (s0 + s1) + (s2 + s3);
+    const float2 s = __fadd2_rn(s0, s1);
+    st.l += s.x + s.y;
 }
 
+// Orders later uses of the registers after the preceding tcgen05.wait::ld.
+__device__ __forceinline__ void regs_after_wait(uint32_t (&r)[32]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// The 128 columns of one half tile, one tensor-memory lane (query row) per thread.
+__device__ __forceinline__ void load_half(uint32_t taddr, uint32_t (&r)[4][32]) {
+    tmem_ld_32x32b_x32(taddr, r[0]);
+    tmem_ld_32x32b_x32(taddr + 32u, r[1]);
+    tmem_ld_32x32b_x32(taddr + 64u, r[2]);
+    tmem_ld_32x32b_x32(taddr + 96u, r[3]);
+    tmem_ld_wait_regs(r[0]);
+    regs_after_wait(r[1]);
+    regs_after_wait(r[2]);
+    regs_after_wait(r[3]);
+}
+
+// sum over the 128 columns of 2^(score * sc - ref), in four packed partial sums
+__device__ __forceinline__ float2 sum_exp2_128(const uint32_t (&r)[4][32], float sc, float ref) {
+    const float2 sc2 = f2(sc), nm2 = f2(-ref);
+    float2 s[4] = {f2(0.f), f2(0.f), f2(0.f), f2(0.f)};
+#pragma unroll
+    for (int k = 0; k < 128; k += 2) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[k >> 5][k & 31]),
+                                                __uint_as_float(r[k >> 5][(k + 1) & 31])), sc2, nm2);
+        const float2 e = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        s[(k >> 1) & 3] = __fadd2_rn(s[(k >> 1) & 3], e);
+    }
+    return __fadd2_rn(__fadd2_rn(s[0], s[1]), __fadd2_rn(s[2], s[3]));
+}
+
+// Folds a full half tile (128 real columns) into the state: one extreme over the
+// 128 scores, the reference moved to the new running maximum (the sum rescaled),
+// then 128 exponentials.
 template <bool NEG>
-__device__ __forceinline__ void fold_half(uint32_t taddr, int valid, float sc, RowState& st) {
-    // valid: real columns in this 128-column half (warp-uniform)
+__device__ __forceinline__ void fold_full_half(const uint32_t (&r)[4][32], float sc, RowState& st) {
+    float a[43];
+#pragma unroll
+    for (int i = 0; i < 42; ++i) {
+        const int k = 3 * i;
+        const float x0 = __uint_as_float(r[k >> 5][k & 31]);
+        const float x1 = __uint_as_float(r[(k + 1) >> 5][(k + 1) & 31]);
+        const float x2 = __uint_as_float(r[(k + 2) >> 5][(k + 2) & 31]);
+        a[i] = NEG ? min3f(x0, x1, x2) : max3f(x0, x1, x2);
+    }
+    a[42] = NEG ? min3f(__uint_as_float(r[3][30]), __uint_as_float(r[3][31]), st.ext)
+                : max3f(__uint_as_float(r[3][30]), __uint_as_float(r[3][31]), st.ext);
+    float b[15];
+#pragma unroll
+    for (int i = 0; i < 14; ++i) b[i] = NEG ? min3f(a[3 * i], a[3 * i + 1], a[3 * i + 2])
+                                           : max3f(a[3 * i], a[3 * i + 1], a[3 * i + 2]);
+    b[14] = a[42];
+    float c[5];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) c[i] = NEG ? min3f(b[3 * i], b[3 * i + 1], b[3 * i + 2])
+                                          : max3f(b[3 * i], b[3 * i + 1], b[3 * i + 2]);
+    const float e2 = NEG ? fminf(min3f(c[0], c[1], c[2]), fminf(c[3], c[4]))
+                         : fmaxf(max3f(c[0], c[1], c[2]), fmaxf(c[3], c[4]));
+    const float mt = e2 * sc;
+    const float f = ex2_approx(st.ref - mt);  // 2^(-inf) = 0 on the row's first columns
+    st.l = (mt == st.ref) ? st.l : st.l * f;
+    st.ref = mt;
+    st.ext = e2;
+    const float2 s = sum_exp2_128(r, sc, mt);
+    st.l += s.x + s.y;
+}
+
+// Folds a partial half tile (the ragged last tile: 0 < valid < 128 real columns,
+// warp-uniform) chunk by chunk, masking the columns past the last key.
+template <bool NEG>
+__device__ __forceinline__ void fold_partial_half(uint32_t taddr, int valid, float sc, RowState& st) {
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
         const int vc = valid - 32 * c;
@@ -227,7 +310,7 @@ score_softmax_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             mbar_init(qfull(b), 1);
             mbar_init(qempty(b), 1);
             mbar_init(tfull(b), 1);
-            mbar_init(tempty(b), SM_EPI_WARPS);
+            mbar_init(tempty(b), SM_EPI_WARPS / 2);
             mbar_init(mfull(b), 4 * 32);
             mbar_init(mempty(b), 4 * 32);
         }
@@ -328,10 +411,11 @@ score_softmax_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
     } else {
         // ------------------------------------------------------------ softmax warps
         const int q = warp & 3;             // tensor-memory lane quarter
-        const int h = (warp - 2) >> 2;      // column half of each S tile
+        const int h = (warp - 2) >> 2;      // this warp folds the S tiles held in buffer h
         const bool neg = p.sc < 0.f;
-        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
-        uint32_t abuf = 0, aphase = 0;
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(h * SM_BN);
+        uint32_t tphase = 0;                // phase of tfull(h)
+        uint64_t g = 0;                     // S tiles of this CTA before the current unit
         uint32_t ui = 0;
         bool ok = true;
         for (int64_t u = blockIdx.x; ok && u < p.num_units; u += G, ++ui) {
@@ -339,30 +423,52 @@ score_softmax_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_const
             const int32_t mb = static_cast<int32_t>(u % p.mblocks);
             RowState st;
             st.ext = neg ? __int_as_float(0x7f800000) : __int_as_float(0xff800000);
-            st.mt = __int_as_float(0xff800000);
+            st.ref = __int_as_float(0xff800000);
             st.l = 0.f;
-            for (int32_t t = 0; t < ntiles; ++t) {
+            // tiles alternate between the two buffers across the CTA's whole tile sequence;
+            // the two warps of a lane quarter take every other tile, so that one folds
+            // while the other loads
+            for (int32_t t = static_cast<int32_t>((g & 1u) ^ static_cast<uint32_t>(h)); t < ntiles; t += 2) {
                 uint32_t got = 0;
                 if (lane == 0)
-                    got = sm_wait(tfull(static_cast<int>(abuf)), aphase, p.err, p.timeout_ns, abort_flag, 0x25) ? 1u : 0u;
+                    got = sm_wait(tfull(h), tphase, p.err, p.timeout_ns, abort_flag, 0x25) ? 1u : 0u;
                 got = __shfl_sync(0xffffffffu, got, 0);
                 if (!got) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const int valid = p.N - t * SM_BN - h * (SM_BN / 2);
-                const uint32_t taddr = tmem_base + lane_base + abuf * SM_BN + static_cast<uint32_t>(h * (SM_BN / 2));
-                if (neg) fold_half<true>(taddr, valid, p.sc, st);
-                else fold_half<false>(taddr, valid, p.sc, st);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty(static_cast<int>(abuf)));
-                abuf ^= 1u;
-                if (abuf == 0) aphase ^= 1u;
+                auto release = [&]() {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty(h));
+                };
+                const int valid = p.N - t * SM_BN;  // real columns in this tile
+                if (valid >= SM_BN) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t r[4][32];
+                        load_half(tbase + static_cast<uint32_t>(hh * (SM_BN / 2)), r);
+                        if (hh == 1) release();  // the MMA may refill the buffer during the fold
+                        if (neg) fold_full_half<true>(r, p.sc, st);
+                        else fold_full_half<false>(r, p.sc, st);
+                    }
+                } else {
+                    const int v0 = valid < SM_BN / 2 ? valid : SM_BN / 2;
+                    if (neg) {
+                        fold_partial_half<true>(tbase, v0, p.sc, st);
+                        fold_partial_half<true>(tbase + SM_BN / 2, valid - v0, p.sc, st);
+                    } else {
+                        fold_partial_half<false>(tbase, v0, p.sc, st);
+                        fold_partial_half<false>(tbase + SM_BN / 2, valid - v0, p.sc, st);
+                    }
+                    release();
+                }
+                tphase ^= 1u;
             }
+            g += static_cast<uint64_t>(ntiles);
             if (!ok) break;
-            // merge the two column halves of each row
+            // merge the two partial states of each row
             const int mbuf = static_cast<int>(ui & 1u);
             const uint32_t mpar = (ui >> 1) & 1u;
             const int row_local = 32 * q + lane;
@@ -436,6 +542,8 @@ cudaError_t launch_score_softmax(const CUtensorMap& tmQ, const CUtensorMap& tmK,
     }
     return cudaErrorInvalidValue;
 }
+
+int softmax_tile_n() { return SM_BN; }
 
 cudaError_t launch_fill_stats(float* m, float* l, int64_t n, float mv, float lv, int sms, cudaStream_t stream) {
     int64_t blocks = (n + 255) / 256;

@@ -179,11 +179,14 @@ __device__ __forceinline__ bool seg_next(const KParams& p, SegIter& it, Seg& s) 
 
 // Slow path of a bounded wait.  Returns false (and raises the abort flag) when
 // the wait gave up; records the first failure in the device error word.
+// Bound on a waiter's suspension inside mbarrier.try_wait (see mbar_try_wait_ns).
+constexpr uint32_t kWaitSuspendNs = 32;
+
 static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uint32_t* err, uint64_t timeout_ns,
                                               volatile int* abort_flag, uint32_t who) {
     const uint64_t t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_ns(bar, parity, kWaitSuspendNs)) return true;
         if ((i & 15u) == 0) {
             if (*abort_flag) return false;
             if (global_timer_ns() - t0 > timeout_ns) {
@@ -197,7 +200,7 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uin
 
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint32_t* err, uint64_t timeout_ns,
                                              volatile int* abort_flag, uint32_t who) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_ns(bar, parity, kWaitSuspendNs)) return true;
     return wait_slow(bar, parity, err, timeout_ns, abort_flag, who);
 }
 

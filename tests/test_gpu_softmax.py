@@ -11,7 +11,7 @@ accumulation of the score, base-2 exponent with ex2.approx, fp32 running sums):
     its value by ln2 dx + 2^-21 (ex2.approx) relative;
   - the running sum: one rescale per 32-column chunk at most (each 2^-21 +
     2^-23 + ln2 2^-23 T relative) and (chunks + 12) fp32 additions of positive
-    terms (2^-24 each), plus the merge of the two column halves (2 * 2^-21).
+    terms (2^-24 each), plus the merge of the two partial states (2 * 2^-21).
 Rows whose statistics are fixed by structure (equal keys, dominant keys, small
 integers) are checked much more tightly."""
 import math
@@ -129,6 +129,24 @@ def test_softmax_parity(name, M, N, d, batch, alpha, ldq, ldk, dist, bk):
     em, el = check_rows(Q, K, m, l, M, N, d, batch, alpha, ldq, ldk, strideQ, strideK, what=name)
     # tripwire well inside the worst-case bound: a correct kernel's typical row_sum error is ~1e-6
     assert np.median(el) < 2e-5, f"{name}: median row_sum error {np.median(el):.3g}"
+
+
+@pytest.mark.parametrize("order", ["increasing", "decreasing"])
+def test_softmax_monotone_scores(order):
+    """Scores that grow (or shrink) steadily along the keys by about 16 base-2 units
+    per 256-key tile: growing ones move the row maximum on every tile, so every
+    reference move and rescale is taken; shrinking ones never move it after the
+    first tile."""
+    from pins import half_bits
+    M, N, d = 200, 4096, 64
+    rng = np.random.default_rng(9)
+    Q = half_bits(0.5 + 0.01 * rng.standard_normal((M, d)))
+    ramp = 8.0 * np.arange(N) / N
+    if order == "decreasing":
+        ramp = ramp[::-1]
+    K = half_bits(ramp[:, None] * np.ones((N, d)))
+    m, l = run_softmax(Q, K, M, N, d, 1, 1.0, d, d, M * d, N * d)
+    check_rows(Q, K, m, l, M, N, d, 1, 1.0, d, d, M * d, N * d, what=order)
 
 
 def test_softmax_equal_keys_sum_is_the_key_count():
