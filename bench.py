@@ -322,7 +322,7 @@ def time_transpose(G, device, flush_buf, read_buf, peaks, n=1024, steps=50):
 MUFU_EX2_PER_CLK_SM = 32  # special-function unit: exp2 results per clock per SM on this part
 
 
-def time_score_softmax(G, device, flush_buf, read_buf, peaks, sms, steps=10):
+def time_score_softmax(G, device, flush_buf, read_buf, peaks, sms, steps=10, heads=None):
     """Fused score + softmax statistics on the score workload (128 heads, Q, K 4096 x 64,
     N(0,1), alpha 1/8): the 4 GiB score matrix is never stored.  The bound is the exp2
     rate of the special-function units (one exp per score), derived from the unit
@@ -330,15 +330,16 @@ def time_score_softmax(G, device, flush_buf, read_buf, peaks, sms, steps=10):
     import torch
     from dense_fp16_gemm_tn_gb300 import inputs
     w = inputs.WORKLOADS["score_qk"]
+    nb = w.batch if heads is None else heads
     g = torch.Generator(device=device)
     g.manual_seed(3000)
-    Q = torch.randn((w.batch, w.M, w.K), generator=g, device=device).half()
-    K = torch.randn((w.batch, w.N, w.K), generator=g, device=device).half()
-    m = torch.empty((w.batch * w.M,), dtype=torch.float32, device=device)
+    Q = torch.randn((nb, w.M, w.K), generator=g, device=device).half()
+    K = torch.randn((nb, w.N, w.K), generator=g, device=device).half()
+    m = torch.empty((nb * w.M,), dtype=torch.float32, device=device)
     l = torch.empty_like(m)
 
     def call():
-        G.score_softmax_stats_f16(Q, w.K, w.M * w.K, K, w.K, w.N * w.K, m, l, w.M, w.N, w.K, w.batch, w.alpha)
+        G.score_softmax_stats_f16(Q, w.K, w.M * w.K, K, w.K, w.N * w.K, m, l, w.M, w.N, w.K, nb, w.alpha)
 
     for _ in range(3):
         call()
@@ -356,7 +357,7 @@ def time_score_softmax(G, device, flush_buf, read_buf, peaks, sms, steps=10):
     if st != G.GEMM_OK:
         raise RuntimeError(f"device error in score+softmax timing: {G.gemm_status_string(st)}")
     ms = statistics.median([a.elapsed_time(b) for a, b in ts])
-    scores = w.batch * w.M * w.N
+    scores = nb * w.M * w.N
     try:
         max_mhz = float(subprocess.run(["nvidia-smi", "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits",
                                         "-i", str(device.index or 0)], capture_output=True, text=True,
@@ -365,14 +366,14 @@ def time_score_softmax(G, device, flush_buf, read_buf, peaks, sms, steps=10):
         max_mhz = 2070.0
     exp_peak = sms * MUFU_EX2_PER_CLK_SM * max_mhz * 1e6  # exp2 per second
     achieved = scores / (ms * 1e-3)
-    return {"workload": "fused score + scale + online softmax statistics, 128 heads, Q,K [4096,64] N(0,1), "
+    return {"workload": f"fused score + scale + online softmax statistics, {nb} heads, Q,K [4096,64] N(0,1), "
                         "alpha=1/8; outputs row max and row sum (fp32)",
-            "ms": ms, "tflops": w.flops / (ms * 1e-3) / 1e12,
+            "ms": ms, "tflops": w.flops * nb / w.batch / (ms * 1e-3) / 1e12,
             "scores_per_s": achieved,
             "roofline": {"bound": "alu", "achieved": achieved / 1e9, "peak": exp_peak / 1e9, "unit": "Gexp/s",
                          "frac": achieved / exp_peak,
                          "peak_source": f"{sms} SMs x {MUFU_EX2_PER_CLK_SM} exp2/clk x {max_mhz:.0f} MHz"},
-            "hbm_gbs": (2 * (w.M + w.N) * w.K * w.batch + 8 * w.batch * w.M) / (ms * 1e-3) / 1e9,
+            "hbm_gbs": (2 * (w.M + w.N) * w.K * nb + 8 * nb * w.M) / (ms * 1e-3) / 1e9,
             "l2": "flushed before every step"}
 
 
@@ -562,6 +563,20 @@ def run_ours(args, rank, world, dist):
     print(json.dumps(line), flush=True)
 
 
+def run_softmax_only(args):
+    import torch
+    import dense_fp16_gemm_tn_gb300 as G
+    device = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(device)
+    G.load_library()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    peaks, _ = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    read_buf = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    r = time_score_softmax(G, device, flush, read_buf, peaks, sms, steps=args.steps, heads=args.softmax_only)
+    print(json.dumps({"score_softmax": r}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -571,6 +586,9 @@ def main():
     ap.add_argument("--workload", default=MAIN_WORKLOAD)
     ap.add_argument("--skip-per-config", action="store_true")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--softmax-only", type=int, default=0, metavar="HEADS",
+                    help="time only the fused score + softmax call on HEADS heads and print its entry "
+                         "(a small case for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -579,6 +597,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.softmax_only:
+        run_softmax_only(args)
         return
     dist = None
     if world > 1:
