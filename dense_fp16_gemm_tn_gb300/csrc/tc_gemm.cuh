@@ -341,6 +341,10 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // Per 16-wide K step: +32 bytes inside a K-major 128-byte row, +2048 bytes
             // (16 rows of 128 bytes) in an MN-major box.
             const uint32_t a_step = p.a_mn ? 128u : 2u, b_step = p.b_mn ? 128u : 2u;
+            // Descriptors of stage 0; a stage's descriptors differ only in the start-address
+            // field (address >> 4, 14 bits: shared memory stays below 256 KB).
+            const uint64_t adesc0 = p.a_mn ? smem_desc_mn_sw128(sA) : smem_desc_sw128(sA);
+            const uint64_t bdesc0 = p.b_mn ? smem_desc_mn_sw128(sB) : smem_desc_sw128(sB);
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -353,14 +357,14 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
+                    // The stage was written by TMA (async proxy) and completed through the
+                    // mbarrier's transaction count: the wait alone orders the MMA's reads.
                     if (!wait_bounded(full_bar(stage), phase, p.err, p.timeout_ns, abort_flag, 4)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
-                    const uint32_t a_addr = sA + stage * Cfg::A_BYTES, b_addr = sB + stage * Cfg::B_BYTES;
-                    const uint64_t adesc = p.a_mn ? smem_desc_mn_sw128(a_addr) : smem_desc_sw128(a_addr);
-                    const uint64_t bdesc = p.b_mn ? smem_desc_mn_sw128(b_addr) : smem_desc_sw128(b_addr);
+                    const uint64_t adesc = adesc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
+                    const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
 #pragma unroll
                     for (int k = 0; k < Cfg::BK / 16; ++k) {
                         mma_f16<PAIR>(d_tmem, adesc + a_step * k, bdesc + b_step * k, IDESC,
