@@ -54,6 +54,18 @@ gemm_status_t cuda_fail(cudaError_t e) {
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// A fresh 56-bit tag for each stream-K launch: splitmix64 of a process-wide
+// sequence number (a bijection, so no two launches share a tag), never zero.
+unsigned long long next_sk_epoch() {
+    static std::atomic<unsigned long long> seq{0};
+    unsigned long long z = seq.fetch_add(1) + 0x9e3779b97f4a7c15ull;
+    z = (z ^ (z >> 30)) * 0xbf58476d1ce4e5b9ull;
+    z = (z ^ (z >> 27)) * 0x94d049bb133111ebull;
+    z ^= z >> 31;
+    z &= (1ull << 56) - 1;
+    return z == 0 ? 1 : z;
+}
 int64_t round_up(int64_t a, int64_t b) { return ceil_div(a, b) * b; }
 
 // ------------------------------------------------------------------ per-device state
@@ -268,7 +280,7 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
             pub.sk_tiles = sk;
             pl.sk_iters = I;
             pl.sk_w_bytes = round_up(sk * maxc * pair * 128 * static_cast<int64_t>(pub.tile_n) * 4, 256);
-            pl.sk_ctr_bytes = round_up(sk * pair * 4 * 4, 256);
+            pl.sk_ctr_bytes = round_up(sk * pair * 4 * 8, 256);
         }
     }
     find_tc_variant(pl.var.bn, pl.var.pair, pl.epi, pub.stream_k, &pl.var);
@@ -562,9 +574,8 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
         kp.sk_iters = pl.sk_iters;
         kp.sk_maxc = pl.pub.sk_maxc;
         kp.sk_W = reinterpret_cast<float*>(sk_base);
-        kp.sk_counters = reinterpret_cast<uint32_t*>(sk_base + pl.sk_w_bytes);
-        e = cudaMemsetAsync(kp.sk_counters, 0, static_cast<size_t>(pl.sk_ctr_bytes), stream);
-        if (e != cudaSuccess) { release(); return cuda_fail(e); }
+        kp.sk_counters = reinterpret_cast<unsigned long long*>(sk_base + pl.sk_w_bytes);
+        kp.sk_epoch = next_sk_epoch();
     }
     int64_t grid = 0;
     e = launch_tc_variant(pl.var, mapA_op, mapB_op, mapC, mapD, kp, pl.pub.grid, stream, &grid);

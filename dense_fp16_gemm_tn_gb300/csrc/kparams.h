@@ -54,7 +54,11 @@ struct KParams {
     int64_t sk_iters;          // I; 0 = no stream-K phase
     int32_t sk_maxc;           // partial slots per stream-K tile (>= contributors of any tile)
     float* sk_W;               // [sk_tile][sk_maxc][PAIR][128][BN] fp32 partial accumulators
-    uint32_t* sk_counters;     // [sk_tile][PAIR][4 epilogue warps] arrivals; zero before the launch
+    // [sk_tile][PAIR][4 epilogue warps] arrival words: (sk_epoch << 8) | count.  A word
+    // whose tag is not this launch's epoch counts as zero, so the scratch needs no
+    // clearing (a stale or arbitrary word matches a 56-bit epoch with probability 2^-56).
+    unsigned long long* sk_counters;
+    unsigned long long sk_epoch;  // unique per launch, nonzero, < 2^56
     uint32_t* err;
     uint64_t timeout_ns;
     int32_t debug_skip_first_load;  // test hook: CTA 0 never issues its first load

@@ -728,8 +728,20 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 __threadfence();
                 __syncwarp();
                 uint32_t prev = 0;
-                if (lane == 0)
-                    prev = atomicAdd(p.sk_counters + (static_cast<int64_t>(w.sk_tile) * PAIR + rank) * 4 + quarter, 1u);
+                if (lane == 0) {
+                    unsigned long long* ctr =
+                        p.sk_counters + (static_cast<int64_t>(w.sk_tile) * PAIR + rank) * 4 + quarter;
+                    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr);
+                    // at most sk_n contributors race on a word, so the loop is short; the
+                    // bound only guards against a word no contributor of this launch wrote
+                    for (int attempt = 0; attempt < 4096; ++attempt) {
+                        prev = ((old >> 8) == p.sk_epoch) ? static_cast<uint32_t>(old & 0xffu) : 0u;
+                        const unsigned long long want = (p.sk_epoch << 8) | (prev + 1u);
+                        const unsigned long long seen = atomicCAS(ctr, old, want);
+                        if (seen == old) break;
+                        old = seen;
+                    }
+                }
                 prev = __shfl_sync(0xffffffffu, prev, 0);
                 if (prev == static_cast<uint32_t>(w.sk_n - 1)) {
                     __threadfence();
