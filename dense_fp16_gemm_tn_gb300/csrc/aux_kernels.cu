@@ -38,49 +38,65 @@ __device__ __forceinline__ uint4 window16(const uint32_t (&w)[8], uint32_t shift
 }
 
 // dst[b][r][0..ldo) = src[b][r][0..K) followed by zeros, for up to two operands in one
-// launch; ldo % 8 == 0 and dst 16-byte aligned.  A thread writes 16-byte groups of 8
-// halves.  Their source halves start at any 2-byte boundary: the thread loads the
+// launch; ldo % 8 == 0 and dst 16-byte aligned.  A lane writes 16-byte groups of 8
+// halves.  Their source halves start at any 2-byte boundary: the lane loads the
 // aligned 16-byte block holding the first one and, when the group straddles into the
 // next block and that block holds a half of the row, that block too, then shifts
 // the 32-byte window into place.  No load leaves the blocks that hold row data.
-// One row per block iteration (row index arithmetic once per row); each thread
-// keeps two groups in flight.
-__global__ void repack_rows_kernel(RepackJob j0, RepackJob j1) {
+// A warp takes a span of 32 x kRepackGroups groups of one row at a time (the index
+// arithmetic once per span); a lane takes kRepackGroups groups 32 apart, so a warp's
+// stores cover 512 contiguous bytes and each lane has up to 2 x kRepackGroups loads
+// in flight.
+constexpr int kRepackGroups = 4;
+
+__global__ void __launch_bounds__(256, 4) repack_rows_kernel(RepackJob j0, RepackJob j1) {
+    constexpr int32_t kSpan = 32 * kRepackGroups;  // groups of one work item
     const int64_t rows0 = j0.batch * j0.rows;
-    const int64_t rows_total = rows0 + j1.batch * j1.rows;
-    for (int64_t row = blockIdx.x; row < rows_total; row += gridDim.x) {
-        const bool second = row >= rows0;
+    const int64_t cpr0 = (j0.ldo / 8 + kSpan - 1) / kSpan, cpr1 = (j1.ldo / 8 + kSpan - 1) / kSpan;
+    const int64_t items0 = rows0 * cpr0;
+    const int64_t items_total = items0 + j1.batch * j1.rows * cpr1;
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    // work item = (row, span of kSpan groups): a warp takes items w, w + nwarps, ...
+    for (int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; item < items_total;
+         item += nwarps) {
+        const bool second = item >= items0;
         const RepackJob& jb = second ? j1 : j0;
-        const int64_t rb = second ? row - rows0 : row;  // b * rows + r
-        const int64_t b = rb / jb.rows;
-        const int64_t r = rb - b * jb.rows;
-        const __half* src_row = jb.src + b * jb.stride_src + r * jb.ld_src;
+        const int64_t it = second ? item - items0 : item;
+        const int64_t cpr = second ? cpr1 : cpr0;
+        const int64_t rb = it / cpr;  // b * rows + r
+        const int32_t span0 = static_cast<int32_t>(it - rb * cpr) * kSpan;
+        const int64_t bi = jb.batch > 1 ? rb / jb.rows : 0;
+        const int64_t r = rb - bi * jb.rows;
+        const __half* src_row = jb.src + bi * jb.stride_src + r * jb.ld_src;
         __half* dst_row = jb.dst + rb * jb.ldo;
         const int32_t groups = static_cast<int32_t>(jb.ldo / 8);
         const int32_t K = static_cast<int32_t>(jb.K);
         const uint32_t shift = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src_row) & 15u);  // bytes, even
         const uint4* row_blk = reinterpret_cast<const uint4*>(reinterpret_cast<uintptr_t>(src_row) - shift);
-        for (int32_t g0 = threadIdx.x; g0 < groups; g0 += 2 * blockDim.x) {
-            uint32_t w[2][8];
+        // a group's window reaches into the following block when element k0 + (16 - shift) / 2 < K
+        const int32_t reach = static_cast<int32_t>((16u - shift) / 2u);
+        {
+            const int32_t g0 = span0;
+            uint32_t w[kRepackGroups][8];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int32_t g = g0 + u * blockDim.x;
+            for (int u = 0; u < kRepackGroups; ++u) {
+                const int32_t g = g0 + u * 32 + lane;
                 const int32_t k0 = g * 8;
 #pragma unroll
                 for (int t = 0; t < 8; ++t) w[u][t] = 0;
                 if (g < groups && k0 < K) {
                     const uint4 v0 = __ldg(row_blk + g);
                     w[u][0] = v0.x; w[u][1] = v0.y; w[u][2] = v0.z; w[u][3] = v0.w;
-                    // first half held by the next block: element k0 + (16 - shift) / 2
-                    if (shift != 0 && k0 + static_cast<int32_t>((16u - shift) / 2u) < K) {
+                    if (shift != 0 && k0 + reach < K) {
                         const uint4 v1 = __ldg(row_blk + g + 1);
                         w[u][4] = v1.x; w[u][5] = v1.y; w[u][6] = v1.z; w[u][7] = v1.w;
                     }
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int32_t g = g0 + u * blockDim.x;
+            for (int u = 0; u < kRepackGroups; ++u) {
+                const int32_t g = g0 + u * 32 + lane;
                 if (g >= groups) break;
                 const int32_t k0 = g * 8;
                 uint4 out = make_uint4(0, 0, 0, 0);
@@ -159,8 +175,12 @@ cudaError_t launch_repack(const RepackArgs* ops, int count, int sms, cudaStream_
     }
     const int64_t rows = jobs[0].batch * jobs[0].rows + jobs[1].batch * jobs[1].rows;
     if (rows == 0) return cudaSuccess;
-    // one 256-thread block per row (enough for a 2048-half row in one pass), 8 per SM
-    int64_t blocks = rows < static_cast<int64_t>(sms) * 8 ? rows : static_cast<int64_t>(sms) * 8;
+    // a warp per span: 256-thread blocks, up to 4 blocks per SM (all resident)
+    constexpr int64_t kSpan = 32 * kRepackGroups;
+    const int64_t items = jobs[0].batch * jobs[0].rows * ((jobs[0].ldo / 8 + kSpan - 1) / kSpan) +
+                          jobs[1].batch * jobs[1].rows * ((jobs[1].ldo / 8 + kSpan - 1) / kSpan);
+    const int64_t want = (items + 7) / 8;
+    int64_t blocks = want < static_cast<int64_t>(sms) * 4 ? want : static_cast<int64_t>(sms) * 4;
     repack_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(jobs[0], jobs[1]);
     return cudaGetLastError();
 }
