@@ -34,6 +34,7 @@ from ._binding import (  # noqa: F401
     gemm_tn_f16,
     gemm_tn_f16_batched,
     gemm_tn_f16_get_option,
+    gemm_tn_f16_host,
     gemm_tn_f16_last_cuda_error,
     gemm_tn_f16_last_device_error,
     gemm_tn_f16_plan,

@@ -37,7 +37,7 @@ GEMM_TN_OPT_STREAM_K = 9
 EXPORTED = ["gemm_tn_f16", "gemm_tn_f16_batched", "gemm_status_string", "gemm_tn_f16_last_device_error",
             "gemm_tn_f16_last_cuda_error", "gemm_tn_f16_shutdown", "gemm_tn_f16_version", "gemm_tn_f16_plan",
             "gemm_tn_f16_set_option", "gemm_tn_f16_get_option", "gemm_tn_f16_splitk_static", "gemm_f16", "transpose_f32", "transpose_f16", "gemm_f16_acc16",
-            "score_softmax_stats_f16"]
+            "score_softmax_stats_f16", "gemm_tn_f16_host"]
 
 GEMM_K_MAJOR = 0
 GEMM_MN_MAJOR = 1
@@ -116,6 +116,8 @@ def load_library(build_if_missing: bool = True):
         lib.gemm_f16_acc16.restype = ctypes.c_int
         lib.score_softmax_stats_f16.argtypes = [vp, i64, i64, vp, i64, i64, vp, vp, i64, i64, i64, i64, f32, vp]
         lib.score_softmax_stats_f16.restype = ctypes.c_int
+        lib.gemm_tn_f16_host.argtypes = lib.gemm_tn_f16.argtypes
+        lib.gemm_tn_f16_host.restype = ctypes.c_int
         for name in ("transpose_f32", "transpose_f16"):
             getattr(lib, name).argtypes = [vp, i64, vp, i64, i64, i64, vp]
             getattr(lib, name).restype = ctypes.c_int
@@ -128,6 +130,8 @@ def _ptr(x):
         return None
     if hasattr(x, "data_ptr"):
         return x.data_ptr()
+    if hasattr(x, "ctypes"):  # numpy array (host memory)
+        return x.ctypes.data
     return int(x)
 
 
@@ -173,6 +177,14 @@ def gemm_f16_acc16(a_major, b_major, A, lda, strideA, B, ldb, strideB, C, ldc, s
                                        _ptr(C), ldc, strideC, _ptr(D), ldd, strideD, M, N, K, batch,
                                        float(alpha), float(beta), _stream(stream))
     return _check(st, "gemm_f16_acc16", check)
+
+
+def gemm_tn_f16_host(A, lda, B, ldb, C, ldc, D, ldd, M, N, K, alpha, beta, stream=None, *, check=True):
+    """gemm_tn_f16 on host buffers (numpy arrays or CPU tensors; page-locked memory overlaps
+    the copies).  Asynchronous on `stream`: synchronize before reading D."""
+    st = load_library().gemm_tn_f16_host(_ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, _ptr(D), ldd, M, N, K,
+                                         float(alpha), float(beta), _stream(stream))
+    return _check(st, "gemm_tn_f16_host", check)
 
 
 def score_softmax_stats_f16(Q, ldq, strideQ, K, ldk, strideK, row_max, row_sum, M, N, d, batch, alpha,

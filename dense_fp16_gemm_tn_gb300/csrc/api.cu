@@ -17,6 +17,7 @@
 #include <cstring>
 #include <limits>
 #include <mutex>
+#include <vector>
 
 #include "gemm_tn_f16.h"
 #include "internal.h"
@@ -77,6 +78,8 @@ struct DeviceState {
     uint32_t* err = nullptr;
     cudaMemPool_t pool = nullptr;
     int64_t capacity[kMaxVariants];  // resident CTAs per variant, 0 = not queried yet
+    cudaStream_t copy_in = nullptr;   // host -> device copies of gemm_tn_f16_host
+    cudaStream_t copy_out = nullptr;  // device -> host copies of gemm_tn_f16_host
 };
 
 constexpr int kMaxDevices = 64;
@@ -589,6 +592,117 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     return GEMM_OK;
 }
 
+// ------------------------------------------------------------------ host-buffer GEMM
+
+// D = alpha A B^T + beta C with every matrix in host memory.  B (N x K) goes to the
+// device first; A, C and D travel in blocks of rows, so that block j's GEMM runs while
+// block j+1's A and C come in and block j-1's D goes out.  Copies use two library
+// streams joined to the caller's stream by events; device buffers come from the pool.
+gemm_status_t run_host(const void* A, int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc, void* D,
+                       int64_t ldd, int64_t M, int64_t N, int64_t K, float alpha, float beta, cudaStream_t stream) {
+    Problem pr = {M, N, K, 1, lda, ldb, ldc, ldd, 0, 0, 0, 0, beta, 0};
+    gemm_status_t st = validate(pr);
+    if (st != GEMM_OK) return st;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!D || (K > 0 && (!A || !B)) || (beta != 0.0f && !C)) return GEMM_ERR_INVALID_VALUE;
+    auto odd = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 1u) != 0; };
+    if (odd(D) || (K > 0 && (odd(A) || odd(B))) || (beta != 0.0f && odd(C))) return GEMM_ERR_MISALIGNED;
+    DeviceState* dev = nullptr;
+    if ((st = device_state(&dev)) != GEMM_OK) return st;
+    cudaError_t e;
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mu);
+        if (!dev->copy_in && (e = cudaStreamCreateWithFlags(&dev->copy_in, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e);
+        if (!dev->copy_out && (e = cudaStreamCreateWithFlags(&dev->copy_out, cudaStreamNonBlocking)) != cudaSuccess)
+            return cuda_fail(e);
+    }
+    const bool use_c = beta != 0.0f;
+    const int64_t a_bytes = K > 0 ? 2 * ((M - 1) * lda + K) : 0;
+    const int64_t b_bytes = K > 0 ? 2 * ((N - 1) * ldb + K) : 0;
+    const int64_t c_bytes = use_c ? 2 * ((M - 1) * ldc + N) : 0;
+    const int64_t d_bytes = 2 * ((M - 1) * ldd + N);
+    const int64_t a_off = 0, b_off = round_up(a_bytes, 256), c_off = b_off + round_up(b_bytes, 256),
+                  d_off = c_off + round_up(c_bytes, 256), total = d_off + round_up(d_bytes, 256);
+    uint8_t* buf = nullptr;
+    if ((e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&buf), static_cast<size_t>(total), dev->pool, stream)) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_WORKSPACE;
+    }
+    // row blocks: about four, at least 512 rows each (multiples of the 256-row tile)
+    const int64_t rows_blk = std::max<int64_t>(512, round_up(ceil_div(M, 4), 256));
+    const int64_t nblk = ceil_div(M, rows_blk);
+    std::vector<cudaEvent_t> evs;
+    auto new_event = [&](cudaEvent_t* ev) {
+        cudaError_t r = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        if (r == cudaSuccess) evs.push_back(*ev);
+        return r;
+    };
+    auto finish = [&](gemm_status_t status) {
+        for (cudaEvent_t ev : evs) cudaEventDestroy(ev);  // released once pending work completes
+        return status;
+    };
+    auto fail = [&](cudaError_t r) {
+        // join the copy streams before the buffer goes back to the pool
+        cudaEvent_t ev_in = nullptr, ev_out = nullptr;
+        if (new_event(&ev_in) == cudaSuccess && cudaEventRecord(ev_in, dev->copy_in) == cudaSuccess)
+            cudaStreamWaitEvent(stream, ev_in, 0);
+        if (new_event(&ev_out) == cudaSuccess && cudaEventRecord(ev_out, dev->copy_out) == cudaSuccess)
+            cudaStreamWaitEvent(stream, ev_out, 0);
+        cudaFreeAsync(buf, stream);
+        return finish(cuda_fail(r));
+    };
+    cudaEvent_t ev_start;
+    if ((e = new_event(&ev_start)) != cudaSuccess || (e = cudaEventRecord(ev_start, stream)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(dev->copy_in, ev_start, 0)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(dev->copy_out, ev_start, 0)) != cudaSuccess)
+        return fail(e);
+    uint8_t* dA = buf + a_off;
+    uint8_t* dB = buf + b_off;
+    uint8_t* dC = buf + c_off;
+    uint8_t* dD = buf + d_off;
+    // rows x width halves of a row-major matrix with leading dimension ld: only the
+    // elements travel, never the padding between rows
+    auto copy_rows = [&](void* dst, const void* src, int64_t ld, int64_t width, int64_t rows, cudaMemcpyKind kind,
+                         cudaStream_t s_) {
+        return cudaMemcpy2DAsync(dst, static_cast<size_t>(2 * ld), src, static_cast<size_t>(2 * ld),
+                                 static_cast<size_t>(2 * width), static_cast<size_t>(rows), kind, s_);
+    };
+    if (K > 0 && (e = copy_rows(dB, B, ldb, K, N, cudaMemcpyHostToDevice, dev->copy_in)) != cudaSuccess) return fail(e);
+    for (int64_t j = 0; j < nblk; ++j) {
+        const int64_t r0 = j * rows_blk, rows = std::min(rows_blk, M - r0);
+        if (K > 0 && (e = copy_rows(dA + 2 * r0 * lda, static_cast<const uint8_t*>(A) + 2 * r0 * lda, lda, K, rows,
+                                    cudaMemcpyHostToDevice, dev->copy_in)) != cudaSuccess)
+            return fail(e);
+        if (use_c && (e = copy_rows(dC + 2 * r0 * ldc, static_cast<const uint8_t*>(C) + 2 * r0 * ldc, ldc, N, rows,
+                                    cudaMemcpyHostToDevice, dev->copy_in)) != cudaSuccess)
+            return fail(e);
+        cudaEvent_t ev_in, ev_done;
+        if ((e = new_event(&ev_in)) != cudaSuccess || (e = cudaEventRecord(ev_in, dev->copy_in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(stream, ev_in, 0)) != cudaSuccess)
+            return fail(e);
+        Problem pj = {rows, N, K, 1, lda, ldb, ldc, ldd, 0, 0, 0, 0, beta, 0};
+        st = run(dA + 2 * r0 * lda, dB, use_c ? dC + 2 * r0 * ldc : nullptr, dD + 2 * r0 * ldd, pj, alpha, stream);
+        if (st != GEMM_OK) {
+            fail(cudaSuccess);
+            return st;
+        }
+        if ((e = new_event(&ev_done)) != cudaSuccess || (e = cudaEventRecord(ev_done, stream)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(dev->copy_out, ev_done, 0)) != cudaSuccess)
+            return fail(e);
+        if ((e = copy_rows(static_cast<uint8_t*>(D) + 2 * r0 * ldd, dD + 2 * r0 * ldd, ldd, N, rows,
+                           cudaMemcpyDeviceToHost, dev->copy_out)) != cudaSuccess)
+            return fail(e);
+    }
+    cudaEvent_t ev_end;
+    if ((e = new_event(&ev_end)) != cudaSuccess || (e = cudaEventRecord(ev_end, dev->copy_out)) != cudaSuccess ||
+        (e = cudaStreamWaitEvent(stream, ev_end, 0)) != cudaSuccess)
+        return fail(e);
+    if ((e = cudaFreeAsync(buf, stream)) != cudaSuccess) return finish(cuda_fail(e));
+    return finish(GEMM_OK);
+}
+
 // Fused score + softmax statistics: validation, optional repack of operands TMA
 // cannot fetch as they are, tensor maps, launch.
 gemm_status_t run_softmax(const void* Q, int64_t ldq, int64_t strideQ, const void* K, int64_t ldk, int64_t strideK,
@@ -740,6 +854,12 @@ gemm_status_t gemm_f16_acc16(int32_t a_major, int32_t b_major, const void* A, in
     return run(A, B, C, D, p, alpha, reinterpret_cast<cudaStream_t>(stream));
 }
 
+gemm_status_t gemm_tn_f16_host(const void* A, int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc,
+                               void* D, int64_t ldd, int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                               gemm_stream_t stream) {
+    return run_host(A, lda, B, ldb, C, ldc, D, ldd, M, N, K, alpha, beta, reinterpret_cast<cudaStream_t>(stream));
+}
+
 gemm_status_t score_softmax_stats_f16(const void* Q, int64_t ldq, int64_t strideQ, const void* K, int64_t ldk,
                                       int64_t strideK, float* row_max, float* row_sum, int64_t M, int64_t N, int64_t d,
                                       int64_t batch, float alpha, gemm_stream_t stream) {
@@ -789,6 +909,9 @@ void gemm_tn_f16_shutdown(void) {
             cudaDeviceSynchronize();
             cudaMemPoolDestroy(d.pool);
             d.pool = nullptr;
+            if (d.copy_in) cudaStreamDestroy(d.copy_in);
+            if (d.copy_out) cudaStreamDestroy(d.copy_out);
+            d.copy_in = d.copy_out = nullptr;
             d.ready = false;
         }
     }

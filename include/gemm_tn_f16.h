@@ -153,6 +153,26 @@ GEMM_TN_API gemm_status_t gemm_f16_acc16(int32_t a_major, int32_t b_major,
                                          gemm_stream_t stream);
 
 /*
+ * gemm_tn_f16 with A, B, C and D in HOST memory: the same product, rules and
+ * layouts, with the host <-> device traffic handled by the library.  B goes to the
+ * device first; A, C and D travel in blocks of rows on two library streams, so that
+ * one block's GEMM overlaps the next block's A and C coming in and the previous
+ * block's D going out.  Only the matrix elements are copied (never the padding
+ * between rows; D's padding in host memory is left untouched).  Page-locked host
+ * memory (cudaHostAlloc / cudaHostRegister) lets the copies run asynchronously and
+ * overlap; pageable memory works but the copies then block the calling thread.
+ * Asynchronous on `stream`: the host buffers must stay valid and A, B, C unmodified
+ * until the stream has passed the call, and D is complete only then (synchronize on
+ * `stream` before reading it).  Device staging buffers come from the library's
+ * stream-ordered pool (GEMM_ERR_WORKSPACE if that fails).  The pages move data to the
+ * device before their kernels and show no such call.
+ */
+GEMM_TN_API gemm_status_t gemm_tn_f16_host(const void* A, int64_t lda, const void* B, int64_t ldb,
+                                           const void* C, int64_t ldc, void* D, int64_t ldd,
+                                           int64_t M, int64_t N, int64_t K, float alpha, float beta,
+                                           gemm_stream_t stream);
+
+/*
  * Fused score GEMM + scale + softmax statistics.  The score is the Q @ K.T of the
  * "为什么 cutlass_cute_tutorial_zh.md 中要用 retile_D" page (section 1: Q is the
  * MMA's A operand, K its B operand; head_dim 64 there); the pages stop at the

@@ -238,3 +238,12 @@ def test_score_softmax_host_checks_without_a_gpu():
     assert f(Q, 64, 0, K, 64, 0, m, m + 32, 16, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_INVALID_VALUE
     assert f(Q, 64, 0, K, 64, 0, Q + 64, l, 16, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_INVALID_VALUE
     assert f(Q, 64, 0, K, 64, 0, m, K + 128, 16, 16, 64, 1, 0.125, check=False) == G.GEMM_ERR_INVALID_VALUE
+
+
+def test_host_gemm_checks_without_a_gpu():
+    f = G.gemm_tn_f16_host
+    assert f(None, 8, None, 8, None, 8, None, 8, 0, 8, 8, 1.0, 0.0, check=False) == G.GEMM_OK
+    assert f(0x1000, 8, 0x2000, 8, None, 8, 0x3000, 8, -1, 8, 8, 1.0, 0.0, check=False) == G.GEMM_ERR_INVALID_VALUE
+    assert f(0x1000, 4, 0x2000, 8, None, 8, 0x3000, 8, 8, 8, 8, 1.0, 0.0, check=False) == G.GEMM_ERR_INVALID_VALUE
+    assert f(0x1000, 8, 0x2000, 8, None, 8, None, 8, 8, 8, 8, 1.0, 0.0, check=False) == G.GEMM_ERR_INVALID_VALUE
+    assert f(0x1001, 8, 0x2000, 8, None, 8, 0x3000, 8, 8, 8, 8, 1.0, 0.0, check=False) == G.GEMM_ERR_MISALIGNED
