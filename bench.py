@@ -291,6 +291,22 @@ def time_e2e(prob, G, steps, warmup):
     return ms, h2d, d2h
 
 
+def slowest_rank_ms(total_ms, dist, device=None):
+    """The timed region's length on the slowest rank (replicas: the job ends with it)."""
+    if dist is None:
+        return total_ms
+    import torch
+    on = device if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([total_ms], device=on, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_step, steps, total_ms):
+    """Whole-job throughput: every rank runs the same problem `steps` times."""
+    return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
+
+
 def dist_barrier(dist):
     if dist is not None:
         dist.barrier()
@@ -504,13 +520,9 @@ def run_ours(args, rank, world, dist):
     st = G.gemm_tn_f16_last_device_error()
     if st != G.GEMM_OK:
         raise RuntimeError(f"device error during the timed region: {G.gemm_status_string(st)}")
-    total_ms = sum(times)
-    if dist is not None:
-        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = slowest_rank_ms(sum(times), dist, device)
     ms_step = total_ms / args.steps
-    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(world, w.flops, args.steps, total_ms)
 
     # dominant kernel: the tensor-core GEMM; for the main workload it is the only launch of a step
     roof, bound = roofline_tflops(w, peaks)
