@@ -607,6 +607,13 @@ gemm_status_t run_host(const void* A, int64_t lda, const void* B, int64_t ldb, c
     if (!D || (K > 0 && (!A || !B)) || (beta != 0.0f && !C)) return GEMM_ERR_INVALID_VALUE;
     auto odd = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 1u) != 0; };
     if (odd(D) || (K > 0 && (odd(A) || odd(B))) || (beta != 0.0f && odd(C))) return GEMM_ERR_MISALIGNED;
+    // same aliasing rules as the device call: D overlaps no input, except C exactly
+    const int64_t d_ext = extent_bytes(M, N, ldd, 0, 1);
+    if (K > 0 && (ranges_overlap(D, d_ext, A, extent_bytes(M, K, lda, 0, 1)) ||
+                  ranges_overlap(D, d_ext, B, extent_bytes(N, K, ldb, 0, 1))))
+        return GEMM_ERR_INVALID_VALUE;
+    if (beta != 0.0f && (C == D ? ldc != ldd : ranges_overlap(D, d_ext, C, extent_bytes(M, N, ldc, 0, 1))))
+        return GEMM_ERR_INVALID_VALUE;
     DeviceState* dev = nullptr;
     if ((st = device_state(&dev)) != GEMM_OK) return st;
     cudaError_t e;

@@ -247,3 +247,10 @@ def test_host_gemm_checks_without_a_gpu():
     assert f(0x1000, 4, 0x2000, 8, None, 8, 0x3000, 8, 8, 8, 8, 1.0, 0.0, check=False) == G.GEMM_ERR_INVALID_VALUE
     assert f(0x1000, 8, 0x2000, 8, None, 8, None, 8, 8, 8, 8, 1.0, 0.0, check=False) == G.GEMM_ERR_INVALID_VALUE
     assert f(0x1001, 8, 0x2000, 8, None, 8, 0x3000, 8, 8, 8, 8, 1.0, 0.0, check=False) == G.GEMM_ERR_MISALIGNED
+
+
+def test_host_gemm_rejects_overlapping_buffers_without_a_gpu():
+    f = G.gemm_tn_f16_host
+    # D overlapping A, and C overlapping D without being D
+    assert f(0x1000, 8, 0x8000, 8, None, 8, 0x1010, 8, 8, 8, 8, 1.0, 0.0, check=False) == G.GEMM_ERR_INVALID_VALUE
+    assert f(0x1000, 8, 0x8000, 8, 0x20010, 8, 0x20000, 8, 8, 8, 8, 1.0, 1.0, check=False) == G.GEMM_ERR_INVALID_VALUE
