@@ -57,7 +57,8 @@ class gemm_tn_plan_t(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("epi_tma", ctypes.c_int32), ("pack_a", ctypes.c_int32),
                 ("pack_b", ctypes.c_int32), ("units", ctypes.c_int64), ("grid", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("stream_k", ctypes.c_int32), ("sk_maxc", ctypes.c_int32),
-                ("dp_tiles", ctypes.c_int64), ("sk_tiles", ctypes.c_int64)]
+                ("dp_tiles", ctypes.c_int64), ("sk_tiles", ctypes.c_int64), ("stage_cd", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

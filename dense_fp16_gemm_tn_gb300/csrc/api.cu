@@ -56,6 +56,9 @@ gemm_status_t cuda_fail(cudaError_t e) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Elements of D from which misaligned C / D are staged through aligned copies.
+constexpr int64_t kStageMinElems = int64_t(1) << 20;
+
 // A fresh 56-bit tag for each stream-K launch: splitmix64 of a process-wide
 // sequence number (a bijection, so no two launches share a tag), never zero.
 unsigned long long next_sk_epoch() {
@@ -217,6 +220,8 @@ struct Plan {
     int64_t ldo_a, ldo_b;        // leading dims of the packed copies
     int64_t pack_a_bytes, pack_b_bytes, partial_bytes;
     int64_t sk_w_bytes, sk_ctr_bytes;  // stream-K partial slots and arrival counters
+    int64_t ldo_cd;                    // leading dimension of the staged C / D copies
+    int64_t stage_c_bytes, stage_d_bytes;
     int64_t sk_iters;
     int group_m;
 };
@@ -289,7 +294,8 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
     find_tc_variant(pl.var.bn, pl.var.pair, pl.epi, pub.stream_k, &pl.var);
     pub.units = pub.stream_k ? pub.dp_tiles : tiles * pub.splits;
     pub.grid = pub.stream_k ? std::min<int64_t>(G, tiles * kb) * pair : std::min<int64_t>(pub.units, G) * pair;
-    pub.workspace_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes;
+    pub.workspace_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes +
+                          pl.stage_c_bytes + pl.stage_d_bytes;
 }
 
 // Tensor-core tile plan; pure host arithmetic, no CUDA calls.
@@ -357,12 +363,29 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
         if (!swap) bn = 128;  // the partial-sum variant exists at 128 columns
     }
 
+    // A large problem whose C or D rows TMA cannot address goes through aligned copies
+    // (C repacked first, D written by TMA to scratch and moved into place after): two
+    // streaming passes cost less than the predicated epilogue's element accesses.
+    const bool force_generic = g_opt_force_generic.load() != 0;
+    const bool stage = !pr.acc16 && splits == 1 && !swap && !force_generic && (!d_ok || !c_ok) &&
+                       pr.M * pr.N * pr.batch >= kStageMinElems;
     int epi;
-    if (pr.acc16) epi = (pr.beta == 0.0f && d_ok && g_opt_force_generic.load() == 0) ? EPI_TMA_A16 : EPI_GENERIC_A16;
+    if (pr.acc16) epi = (pr.beta == 0.0f && d_ok && !force_generic) ? EPI_TMA_A16 : EPI_GENERIC_A16;
     else if (splits > 1) epi = swap ? EPI_PARTIAL_SWAP : EPI_PARTIAL;
     else if (swap) epi = EPI_SWAP;
-    else if (d_ok && c_ok && g_opt_force_generic.load() == 0) epi = pr.beta == 0.0f ? EPI_TMA : EPI_TMA_C;
+    else if ((d_ok && c_ok && !force_generic) || stage) epi = pr.beta == 0.0f ? EPI_TMA : EPI_TMA_C;
     else epi = EPI_GENERIC;
+    if (stage) {
+        pl.ldo_cd = round_up(pr.N, 8);
+        if (pr.beta != 0.0f && !c_ok) {
+            pub.stage_cd |= 1;
+            pl.stage_c_bytes = round_up(((pr.batch > 1 && pr.sC != 0) ? pr.batch : 1) * pr.M * pl.ldo_cd * 2, 256);
+        }
+        if (!d_ok) {
+            pub.stage_cd |= 2;
+            pl.stage_d_bytes = round_up(pr.batch * pr.M * pl.ldo_cd * 2, 256);
+        }
+    }
 
     TcVariant v;
     if (!find_tc_variant(bn, pair, epi, 0, &v)) {
@@ -472,9 +495,11 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
                                       64, boxB))
         pl.pub.pack_b = 1,
         pl.pack_b_bytes = round_up(((p.batch > 1 && p.sB != 0) ? p.batch : 1) * b_rows(p) * pl.ldo_b * 2, 256);
+    // staged C / D get their maps once the scratch copies exist
+    const bool stage_c = (pl.pub.stage_cd & 1) != 0, stage_d = (pl.pub.stage_cd & 2) != 0;
     if ((epi_base(pl.epi) == EPI_TMA || pl.epi == EPI_TMA_C) &&
-        (!encode_map(&mapD, D, p.N, p.M, p.batch, p.ldd, p.sD, p.batch > 1, 64, 32) ||
-         (pl.epi == EPI_TMA_C &&
+        ((!stage_d && !encode_map(&mapD, D, p.N, p.M, p.batch, p.ldd, p.sD, p.batch > 1, 64, 32)) ||
+         (pl.epi == EPI_TMA_C && !stage_c &&
           !encode_map(&mapC, C, p.N, p.M, p.batch, p.ldc, p.sC, p.batch > 1 && p.sC != 0, 64, 32)))) {
         TcVariant v;
         const int generic = epi_acc16(pl.epi) ? EPI_GENERIC_A16 : EPI_GENERIC;
@@ -482,6 +507,8 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
             pl.var = v;
             pl.epi = generic;
             pl.pub.epi_tma = 0;
+            pl.pub.stage_cd = 0;
+            pl.stage_c_bytes = pl.stage_d_bytes = 0;
         } else {
             return GEMM_ERR_UNSUPPORTED;
         }
@@ -495,7 +522,8 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     }
     plan_stream_k(p, pl, cap / pl.var.pair);
 
-    const int64_t ws_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes;
+    const int64_t ws_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes +
+                             pl.stage_c_bytes + pl.stage_d_bytes;
     uint8_t* ws = nullptr;
     if (ws_bytes > 0) {
         e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), static_cast<size_t>(ws_bytes), dev->pool, stream);
@@ -510,7 +538,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
 
     const bool a_batched = p.batch > 1 && p.sA != 0;
     const bool b_batched = p.batch > 1 && p.sB != 0;
-    RepackArgs jobs[2];
+    RepackArgs jobs[3];
     int njobs = 0;
     if (pl.pub.pack_a) {
         void* dst = ws;
@@ -529,6 +557,22 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
             release();
             return GEMM_ERR_UNSUPPORTED;
         }
+    }
+    uint8_t* const stage_base = ws + pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes +
+                                pl.sk_ctr_bytes;
+    void* const Cs = stage_c ? static_cast<void*>(stage_base) : nullptr;
+    void* const Ds = stage_d ? static_cast<void*>(stage_base + pl.stage_c_bytes) : nullptr;
+    if (stage_c) {
+        const bool c_batched = p.batch > 1 && p.sC != 0;
+        jobs[njobs++] = {C, p.ldc, p.sC, Cs, pl.ldo_cd, p.M, p.N, c_batched ? p.batch : 1};
+        if (!encode_map(&mapC, Cs, p.N, p.M, p.batch, pl.ldo_cd, p.M * pl.ldo_cd, c_batched, 64, 32)) {
+            release();
+            return GEMM_ERR_UNSUPPORTED;
+        }
+    }
+    if (stage_d && !encode_map(&mapD, Ds, p.N, p.M, p.batch, pl.ldo_cd, p.M * pl.ldo_cd, p.batch > 1, 64, 32)) {
+        release();
+        return GEMM_ERR_UNSUPPORTED;
     }
     if (njobs > 0) {
         e = launch_repack(jobs, njobs, dev->sms, stream);
@@ -586,6 +630,10 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     if (pl.pub.splits > 1) {
         e = launch_splitk_reduce(kp.W, pl.pub.splits, p.M, p.N, p.batch, alpha, p.beta, C, p.ldc, p.sC, D, p.ldd,
                                  p.sD, dev->sms, stream);
+        if (e != cudaSuccess) { release(); return cuda_fail(e); }
+    }
+    if (stage_d) {
+        e = launch_unpack(Ds, pl.ldo_cd, D, p.ldd, p.sD, p.M, p.N, p.batch, dev->sms, stream);
         if (e != cudaSuccess) { release(); return cuda_fail(e); }
     }
     release();

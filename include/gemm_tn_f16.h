@@ -261,6 +261,10 @@ typedef struct {
     int32_t sk_maxc;         /* stream-K: largest number of CTA groups contributing to one tile */
     int64_t dp_tiles;        /* tiles computed whole (data-parallel), before the stream-K tiles */
     int64_t sk_tiles;        /* tiles shared out by k-block */
+    int32_t stage_cd;        /* bit 0: C copied to an aligned scratch copy first; bit 1: D written
+                                to an aligned scratch copy by tensor copies, then moved into place
+                                (large problems whose C or D rows are not 16-byte aligned) */
+    int32_t reserved;
 } gemm_tn_plan_t;
 
 GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int64_t batch,

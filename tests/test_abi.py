@@ -154,10 +154,16 @@ def test_plan_forced_splits_use_the_reduction_kernel():
     assert p["workspace_bytes"] >= 4 * 16 * 8192 * 4
 
 
-def test_plan_ragged_packed_ld_repacks_operands():
+def test_plan_ragged_packed_ld_repacks_operands_and_stages_c_d():
     p = plan(4095, 3073, 2047, lda=2047, ldb=2047, ldc=3073, ldd=3073, beta=1.5)
-    assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["epi_tma"] == 0
-    assert p["workspace_bytes"] >= 2 * (4095 + 3073) * 2048
+    assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["epi_tma"] == 1 and p["stage_cd"] == 3
+    assert p["workspace_bytes"] >= 2 * (4095 + 3073) * 2048 + 2 * 2 * 4095 * 3080
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_GENERIC_EPI, 1)
+    try:
+        p = plan(4095, 3073, 2047, lda=2047, ldb=2047, ldc=3073, ldd=3073, beta=1.5)
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_GENERIC_EPI, 0)
+    assert p["epi_tma"] == 0 and p["stage_cd"] == 0
 
 
 def test_plan_score_batched_short_k():
@@ -166,9 +172,15 @@ def test_plan_score_batched_short_k():
     assert p["units"] == 32 * 16 * 128
 
 
-def test_plan_misaligned_pointer_forces_pack_and_generic_epilogue():
+def test_plan_misaligned_pointer_forces_pack_and_stages_c_d():
+    # large: A, B repacked; D (and C) staged through aligned copies, TMA epilogue
     p = plan(1024, 1024, 1024, align=0)
-    assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["epi_tma"] == 0
+    assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["epi_tma"] == 1 and p["stage_cd"] == 2
+    p = plan(1024, 1024, 1024, align=0, beta=1.0)
+    assert p["epi_tma"] == 1 and p["stage_cd"] == 3
+    # small: the predicated epilogue reads C and writes D where they are
+    p = plan(256, 256, 1024, align=0, beta=1.0)
+    assert p["epi_tma"] == 0 and p["stage_cd"] == 0
 
 
 def test_plan_k_zero_and_empty():

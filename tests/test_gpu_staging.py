@@ -1,0 +1,86 @@
+"""Large problems whose C or D rows TMA cannot address: C is repacked and D written
+to an aligned scratch copy, then moved into place (plan field stage_cd).  Against the
+oracle element by element, with guard bands around D, and against the predicated
+epilogue the same problems took before."""
+import numpy as np
+import pytest
+
+import dense_fp16_gemm_tn_gb300 as G
+import oracle
+from dense_fp16_gemm_tn_gb300 import inputs
+from gpu_util import SENTINEL, assert_close, assert_device_ok, options, run_problem, to_dev, to_host, torch
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # name, M, N, K, batch, ldc, ldd, beta
+    ("d_odd_ld_beta0", 1100, 1000, 320, 1, 1000, 1003, 0.0),
+    ("cd_odd_ld_beta", 1100, 1000, 320, 1, 1001, 1003, 1.5),
+    ("c_odd_ld_only", 1030, 1040, 200, 1, 1043, 1040, -0.5),
+    ("d_odd_ld_only_beta", 1030, 1040, 200, 1, 1040, 1047, 2.0),
+    ("batched_odd_ld", 600, 900, 256, 3, 905, 907, 0.75),
+    ("packed_everything", 1500, 1003, 777, 1, 1003, 1003, 1.5),
+]
+
+
+@pytest.mark.parametrize("name,M,N,K,batch,ldc,ldd,beta", CASES, ids=[c[0] for c in CASES])
+def test_staged_c_d(name, M, N, K, batch, ldc, ldd, beta):
+    run_problem(M, N, K, batch=batch, ldc=ldc, ldd=ldd, alpha=0.5, beta=beta, seed=len(name), d_pad_rows=2)
+
+
+def test_staged_plan_is_taken():
+    p = G.gemm_tn_f16_plan(1100, 1000, 320, 1, 320, 320, 1001, 1003, 0, 0, 0, 0, 1.5, 15, 152)
+    assert p["stage_cd"] == 3 and p["epi_tma"] == 1
+
+
+def test_staged_small_integers_bit_exact():
+    run_problem(1100, 1000, 256, ldc=1001, ldd=1003, beta=1.0, dist="int", compare="exact", seed=5, d_pad_rows=2)
+
+
+def test_staged_matches_predicated_epilogue_bitwise():
+    """Both epilogues compute alpha*acc + beta*c in fp32 and round once: same bits."""
+    t = torch()
+    M, N, K, ldc, ldd = 1100, 1000, 384, 1001, 1003
+    A = t.randn((M, K), device="cuda").half()
+    B = t.randn((N, K), device="cuda").half()
+    C = t.randn((M * ldc,), device="cuda").half()
+    D1 = t.zeros((M * ldd,), device="cuda", dtype=t.float16)
+    D2 = t.zeros((M * ldd,), device="cuda", dtype=t.float16)
+    G.gemm_tn_f16(A, K, B, K, C, ldc, D1, ldd, M, N, K, 0.5, 1.5)
+    with options(force_generic=1):
+        G.gemm_tn_f16(A, K, B, K, C, ldc, D2, ldd, M, N, K, 0.5, 1.5)
+    t.cuda.synchronize()
+    assert_device_ok()
+    assert t.equal(D1, D2)
+
+
+def test_staged_in_place_and_misaligned_base():
+    """D == C (same odd leading dimension), and a D whose base is 2 bytes off 16."""
+    t = torch()
+    M, N, K, ld = 1024, 1027, 256, 1027
+    A = inputs.uniform_half(11, M, K)
+    B = inputs.uniform_half(12, N, K)
+    C = inputs.with_ld(inputs.uniform_half(13, M, N), ld)
+    ref = oracle.gemm_tn(A, B, C, M, N, K, 0.5, 1.0, ldc=ld, ldd=ld).reshape(M, ld)
+    dCD = to_dev(C.reshape(-1))
+    G.gemm_tn_f16(to_dev(A), K, to_dev(B), K, dCD, ld, dCD, ld, M, N, K, 0.5, 1.0)
+    t.cuda.synchronize()
+    assert_device_ok()
+    got = to_host(dCD).reshape(M, ld)
+    assert_close(got[:, :N], ref[:, :N], K, what="in place")
+    # misaligned base: D starts one half into a buffer of sentinels
+    M2, N2, ld2 = 1100, 1000, 1000
+    buf = t.full((M2 * ld2 + 16,), 0, dtype=t.int16, device="cuda")
+    buf.fill_(np.int16(np.uint16(SENTINEL).view(np.int16)))
+    bufh = buf.view(t.float16)
+    A2 = inputs.uniform_half(14, M2, K)
+    B2 = inputs.uniform_half(15, N2, K)
+    plan = G.gemm_tn_f16_plan(M2, N2, K, 1, K, K, N2, ld2, 0, 0, 0, 0, 0.0, 0b0111, 152)
+    assert plan["stage_cd"] == 2
+    G.gemm_tn_f16(to_dev(A2), K, to_dev(B2), K, None, N2, bufh[1:], ld2, M2, N2, K, 1.0, 0.0)
+    t.cuda.synchronize()
+    assert_device_ok()
+    got = to_host(bufh)
+    assert got[0] == SENTINEL and (got[1 + M2 * ld2:] == SENTINEL).all()
+    ref2 = oracle.gemm_tn(A2, B2, None, M2, N2, K, 1.0, 0.0, ldd=ld2)
+    assert_close(got[1:1 + M2 * ld2], ref2, K, what="misaligned base")
