@@ -165,10 +165,17 @@ __device__ __forceinline__ bool seg_next(const KParams& p, SegIter& it, Seg& s) 
     if (it.dp_next < p.num_units) {
         const int64_t u = it.dp_next;
         it.dp_next += it.G;
-        s.split = static_cast<int32_t>(u % p.splits);
-        tile_coords(p, u / p.splits, s);
-        s.kb0 = static_cast<int32_t>((static_cast<int64_t>(s.split) * p.kb_total) / p.splits);
-        s.kb1 = static_cast<int32_t>((static_cast<int64_t>(s.split + 1) * p.kb_total) / p.splits);
+        if (p.splits == 1) {  // whole tiles: no K-slice arithmetic
+            s.split = 0;
+            tile_coords(p, u, s);
+            s.kb0 = 0;
+            s.kb1 = p.kb_total;
+        } else {
+            s.split = static_cast<int32_t>(u % p.splits);
+            tile_coords(p, u / p.splits, s);
+            s.kb0 = static_cast<int32_t>((static_cast<int64_t>(s.split) * p.kb_total) / p.splits);
+            s.kb1 = static_cast<int32_t>((static_cast<int64_t>(s.split + 1) * p.kb_total) / p.splits);
+        }
         s.sk_tile = -1;
         s.sk_j = 0;
         s.sk_n = 1;
