@@ -220,8 +220,8 @@ struct Plan {
     int64_t ldo_a, ldo_b;        // leading dims of the packed copies
     int64_t pack_a_bytes, pack_b_bytes, partial_bytes;
     int64_t sk_w_bytes, sk_ctr_bytes;  // stream-K partial slots and arrival counters
-    int64_t ldo_cd;                    // leading dimension of the staged C / D copies
-    int64_t stage_c_bytes, stage_d_bytes;
+    int64_t ldo_cd;                    // leading dimension of the staged D copy
+    int64_t stage_d_bytes;
     int64_t sk_iters;
     int group_m;
 };
@@ -260,14 +260,15 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
     pub.sk_tiles = 0;
     pl.sk_iters = 0;
     pl.sk_w_bytes = pl.sk_ctr_bytes = 0;
-    const bool sk_epi = pl.epi == EPI_TMA || pl.epi == EPI_TMA_C || pl.epi == EPI_GENERIC || pl.epi == EPI_SWAP;
+    const bool sk_epi = pl.epi == EPI_TMA || pl.epi == EPI_TMA_C || pl.epi == EPI_TMA_CG || pl.epi == EPI_GENERIC ||
+                        pl.epi == EPI_SWAP;
     // Automatic stream-K when whole tiles would leave much of the machine idle.  At
     // full occupancy the GEMM runs at the power limit, so a partly empty last wave
     // costs less than its share; with the TMA epilogue the fixup is cheap enough
     // to pay from 10% idle, with the predicated one only from 40%.  Forced on, it
     // applies whenever the tiles do not divide evenly.
     const int64_t mode = g_opt_stream_k.load();
-    const double threshold = mode > 0 ? 1.0 : ((pl.epi == EPI_TMA || pl.epi == EPI_TMA_C) ? 0.9 : 0.6);
+    const double threshold = mode > 0 ? 1.0 : ((pl.epi == EPI_TMA || pl.epi == EPI_TMA_C || pl.epi == EPI_TMA_CG) ? 0.9 : 0.6);
     if (mode >= 0 && sk_epi && pub.splits == 1 && kb >= 8 && tiles % G != 0) {
         const double dp_eff = static_cast<double>(tiles) / static_cast<double>(ceil_div(tiles, G) * G);
         // Every group must get at least one iteration (contributors to a tile are
@@ -295,7 +296,7 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
     pub.units = pub.stream_k ? pub.dp_tiles : tiles * pub.splits;
     pub.grid = pub.stream_k ? std::min<int64_t>(G, tiles * kb) * pair : std::min<int64_t>(pub.units, G) * pair;
     pub.workspace_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes +
-                          pl.stage_c_bytes + pl.stage_d_bytes;
+                          pl.stage_d_bytes;
 }
 
 // Tensor-core tile plan; pure host arithmetic, no CUDA calls.
@@ -363,9 +364,10 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
         if (!swap) bn = 128;  // the partial-sum variant exists at 128 columns
     }
 
-    // A large problem whose C or D rows TMA cannot address goes through aligned copies
-    // (C repacked first, D written by TMA to scratch and moved into place after): two
-    // streaming passes cost less than the predicated epilogue's element accesses.
+    // A large problem whose D rows TMA cannot address writes D by TMA to an aligned
+    // scratch copy that is moved into place after (two streaming passes cost less than
+    // the predicated epilogue's element accesses).  C at any alignment is read by the
+    // epilogue itself (EPI_TMA_CG) whenever D can take the TMA path, staged or not.
     const bool force_generic = g_opt_force_generic.load() != 0;
     const bool stage = !pr.acc16 && splits == 1 && !swap && !force_generic && (!d_ok || !c_ok) &&
                        pr.M * pr.N * pr.batch >= kStageMinElems;
@@ -373,14 +375,10 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     if (pr.acc16) epi = (pr.beta == 0.0f && d_ok && !force_generic) ? EPI_TMA_A16 : EPI_GENERIC_A16;
     else if (splits > 1) epi = swap ? EPI_PARTIAL_SWAP : EPI_PARTIAL;
     else if (swap) epi = EPI_SWAP;
-    else if ((d_ok && c_ok && !force_generic) || stage) epi = pr.beta == 0.0f ? EPI_TMA : EPI_TMA_C;
+    else if ((d_ok && !force_generic) || stage) epi = pr.beta == 0.0f ? EPI_TMA : (c_ok ? EPI_TMA_C : EPI_TMA_CG);
     else epi = EPI_GENERIC;
     if (stage) {
         pl.ldo_cd = round_up(pr.N, 8);
-        if (pr.beta != 0.0f && !c_ok) {
-            pub.stage_cd |= 1;
-            pl.stage_c_bytes = round_up(((pr.batch > 1 && pr.sC != 0) ? pr.batch : 1) * pr.M * pl.ldo_cd * 2, 256);
-        }
         if (!d_ok) {
             pub.stage_cd |= 2;
             pl.stage_d_bytes = round_up(pr.batch * pr.M * pl.ldo_cd * 2, 256);
@@ -411,7 +409,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     pub.swap_ab = swap ? 1 : 0;
     pub.splits = splits;
     pub.stages = v.stages;
-    pub.epi_tma = (epi_base(epi) == EPI_TMA || epi == EPI_TMA_C) ? 1 : 0;
+    pub.epi_tma = (epi_base(epi) == EPI_TMA || epi == EPI_TMA_C || epi == EPI_TMA_CG) ? 1 : 0;
 
     pl.ldo_a = round_up(a_len(pr), 8);
     pl.ldo_b = round_up(b_len(pr), 8);
@@ -496,10 +494,10 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
         pl.pub.pack_b = 1,
         pl.pack_b_bytes = round_up(((p.batch > 1 && p.sB != 0) ? p.batch : 1) * b_rows(p) * pl.ldo_b * 2, 256);
     // staged C / D get their maps once the scratch copies exist
-    const bool stage_c = (pl.pub.stage_cd & 1) != 0, stage_d = (pl.pub.stage_cd & 2) != 0;
-    if ((epi_base(pl.epi) == EPI_TMA || pl.epi == EPI_TMA_C) &&
+    const bool stage_d = (pl.pub.stage_cd & 2) != 0;
+    if ((epi_base(pl.epi) == EPI_TMA || pl.epi == EPI_TMA_C || pl.epi == EPI_TMA_CG) &&
         ((!stage_d && !encode_map(&mapD, D, p.N, p.M, p.batch, p.ldd, p.sD, p.batch > 1, 64, 32)) ||
-         (pl.epi == EPI_TMA_C && !stage_c &&
+         (pl.epi == EPI_TMA_C &&
           !encode_map(&mapC, C, p.N, p.M, p.batch, p.ldc, p.sC, p.batch > 1 && p.sC != 0, 64, 32)))) {
         TcVariant v;
         const int generic = epi_acc16(pl.epi) ? EPI_GENERIC_A16 : EPI_GENERIC;
@@ -508,7 +506,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
             pl.epi = generic;
             pl.pub.epi_tma = 0;
             pl.pub.stage_cd = 0;
-            pl.stage_c_bytes = pl.stage_d_bytes = 0;
+            pl.stage_d_bytes = 0;
         } else {
             return GEMM_ERR_UNSUPPORTED;
         }
@@ -523,7 +521,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     plan_stream_k(p, pl, cap / pl.var.pair);
 
     const int64_t ws_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes +
-                             pl.stage_c_bytes + pl.stage_d_bytes;
+                             pl.stage_d_bytes;
     uint8_t* ws = nullptr;
     if (ws_bytes > 0) {
         e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), static_cast<size_t>(ws_bytes), dev->pool, stream);
@@ -560,16 +558,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     }
     uint8_t* const stage_base = ws + pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes +
                                 pl.sk_ctr_bytes;
-    void* const Cs = stage_c ? static_cast<void*>(stage_base) : nullptr;
-    void* const Ds = stage_d ? static_cast<void*>(stage_base + pl.stage_c_bytes) : nullptr;
-    if (stage_c) {
-        const bool c_batched = p.batch > 1 && p.sC != 0;
-        jobs[njobs++] = {C, p.ldc, p.sC, Cs, pl.ldo_cd, p.M, p.N, c_batched ? p.batch : 1};
-        if (!encode_map(&mapC, Cs, p.N, p.M, p.batch, pl.ldo_cd, p.M * pl.ldo_cd, c_batched, 64, 32)) {
-            release();
-            return GEMM_ERR_UNSUPPORTED;
-        }
-    }
+    void* const Ds = stage_d ? static_cast<void*>(stage_base) : nullptr;
     if (stage_d && !encode_map(&mapD, Ds, p.N, p.M, p.batch, pl.ldo_cd, p.M * pl.ldo_cd, p.batch > 1, 64, 32)) {
         release();
         return GEMM_ERR_UNSUPPORTED;
@@ -580,7 +569,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     }
     mapA_op = swap ? mapPB : mapPA;
     mapB_op = swap ? mapPA : mapPB;
-    if (epi_base(pl.epi) != EPI_TMA && pl.epi != EPI_TMA_C) mapD = mapA_op;  // unused by the kernel; any valid map
+    if (epi_base(pl.epi) != EPI_TMA && pl.epi != EPI_TMA_C && pl.epi != EPI_TMA_CG) mapD = mapA_op;  // unused by the kernel; any valid map
     if (pl.epi != EPI_TMA_C) mapC = mapD;
 
     KParams kp;

@@ -1,4 +1,5 @@
-// Variants whose epilogue writes D with TMA stores (aligned D; with EPI_TMA_C, C is read by TMA too).
+// Variants whose epilogue writes D with TMA stores (aligned D; with EPI_TMA_C, C is read by TMA too,
+// with EPI_TMA_CG straight from global memory at any alignment).
 #include "tc_launch.cuh"
 
 namespace gtn {
@@ -13,23 +14,31 @@ bool launch_family_tma(const TcVariant& v, const CUtensorMap& tmA, const CUtenso
     }
     GTN_CASE(256, 1, 4, EPI_TMA, 0)
     GTN_CASE(256, 1, 4, EPI_TMA_C, 0)
+    GTN_CASE(256, 1, 4, EPI_TMA_CG, 0)
     GTN_CASE(256, 1, 4, EPI_TMA, 1)
     GTN_CASE(256, 1, 4, EPI_TMA_A16, 0)
     GTN_CASE(256, 1, 4, EPI_TMA_C, 1)
+    GTN_CASE(256, 1, 4, EPI_TMA_CG, 1)
     GTN_CASE(256, 2, 6, EPI_TMA, 0)
     GTN_CASE(256, 2, 6, EPI_TMA_C, 0)
+    GTN_CASE(256, 2, 6, EPI_TMA_CG, 0)
     GTN_CASE(256, 2, 6, EPI_TMA, 1)
     GTN_CASE(256, 2, 6, EPI_TMA_A16, 0)
     GTN_CASE(256, 2, 6, EPI_TMA_C, 1)
+    GTN_CASE(256, 2, 6, EPI_TMA_CG, 1)
     GTN_CASE(128, 1, 6, EPI_TMA, 0)
     GTN_CASE(128, 1, 6, EPI_TMA_C, 0)
+    GTN_CASE(128, 1, 6, EPI_TMA_CG, 0)
     GTN_CASE(128, 1, 6, EPI_TMA, 1)
     GTN_CASE(128, 1, 6, EPI_TMA_A16, 0)
     GTN_CASE(128, 1, 6, EPI_TMA_C, 1)
+    GTN_CASE(128, 1, 6, EPI_TMA_CG, 1)
     GTN_CASE(128, 2, 8, EPI_TMA, 0)
     GTN_CASE(128, 2, 8, EPI_TMA_C, 0)
+    GTN_CASE(128, 2, 8, EPI_TMA_CG, 0)
     GTN_CASE(128, 2, 8, EPI_TMA, 1)
     GTN_CASE(128, 2, 8, EPI_TMA_C, 1)
+    GTN_CASE(128, 2, 8, EPI_TMA_CG, 1)
 #undef GTN_CASE
     return false;
 }
@@ -42,23 +51,31 @@ bool capacity_family_tma(const TcVariant& v, int sms, int64_t* cap) {
     }
     GTN_CASE(256, 1, 4, EPI_TMA, 0)
     GTN_CASE(256, 1, 4, EPI_TMA_C, 0)
+    GTN_CASE(256, 1, 4, EPI_TMA_CG, 0)
     GTN_CASE(256, 1, 4, EPI_TMA, 1)
     GTN_CASE(256, 1, 4, EPI_TMA_A16, 0)
     GTN_CASE(256, 1, 4, EPI_TMA_C, 1)
+    GTN_CASE(256, 1, 4, EPI_TMA_CG, 1)
     GTN_CASE(256, 2, 6, EPI_TMA, 0)
     GTN_CASE(256, 2, 6, EPI_TMA_C, 0)
+    GTN_CASE(256, 2, 6, EPI_TMA_CG, 0)
     GTN_CASE(256, 2, 6, EPI_TMA, 1)
     GTN_CASE(256, 2, 6, EPI_TMA_A16, 0)
     GTN_CASE(256, 2, 6, EPI_TMA_C, 1)
+    GTN_CASE(256, 2, 6, EPI_TMA_CG, 1)
     GTN_CASE(128, 1, 6, EPI_TMA, 0)
     GTN_CASE(128, 1, 6, EPI_TMA_C, 0)
+    GTN_CASE(128, 1, 6, EPI_TMA_CG, 0)
     GTN_CASE(128, 1, 6, EPI_TMA, 1)
     GTN_CASE(128, 1, 6, EPI_TMA_A16, 0)
     GTN_CASE(128, 1, 6, EPI_TMA_C, 1)
+    GTN_CASE(128, 1, 6, EPI_TMA_CG, 1)
     GTN_CASE(128, 2, 8, EPI_TMA, 0)
     GTN_CASE(128, 2, 8, EPI_TMA_C, 0)
+    GTN_CASE(128, 2, 8, EPI_TMA_CG, 0)
     GTN_CASE(128, 2, 8, EPI_TMA, 1)
     GTN_CASE(128, 2, 8, EPI_TMA_C, 1)
+    GTN_CASE(128, 2, 8, EPI_TMA_CG, 1)
 #undef GTN_CASE
     return false;
 }

@@ -14,6 +14,7 @@ enum EpiMode : int {
     EPI_TMA_C = 5,         // D = alpha*acc + beta*C, C loaded and D stored by TMA (aligned C and D)
     EPI_TMA_A16 = 6,       // EPI_TMA with an fp16 accumulator
     EPI_GENERIC_A16 = 7,   // EPI_GENERIC with an fp16 accumulator
+    EPI_TMA_CG = 8,        // EPI_TMA_C with C read straight from global memory at any 2-byte alignment
 };
 
 #ifdef __CUDACC__

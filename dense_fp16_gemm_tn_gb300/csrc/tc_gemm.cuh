@@ -68,7 +68,7 @@ struct TileCfg {
     static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
     static constexpr int EPI_WARP_BYTES =
-        (epi_base(EPI) == EPI_TMA || EPI == EPI_TMA_C) ? 2 * 32 * 128
+        (epi_base(EPI) == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) ? 2 * 32 * 128
         : (epi_base(EPI) == EPI_GENERIC || EPI == EPI_PARTIAL) ? 32 * 33 * 4 : 0;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
@@ -82,7 +82,8 @@ struct TileCfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N in [16,256], N%16==0");
     static_assert(BN_LOCAL % 8 == 0, "B tile must hold whole 8-row swizzle atoms");
     static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "tiles must stay 1024-byte aligned");
-    static_assert((epi_base(EPI) != EPI_TMA && EPI != EPI_TMA_C) || BN % 64 == 0, "TMA epilogue stores 64-column chunks");
+    static_assert((epi_base(EPI) != EPI_TMA && EPI != EPI_TMA_C && EPI != EPI_TMA_CG) || BN % 64 == 0,
+                  "TMA epilogue stores 64-column chunks");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory per CTA");
     static_assert(PAIR == 1 || PAIR == 2, "CTA pair or single CTA");
 };
@@ -222,6 +223,42 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// Misaligned C: the 16-byte-aligned words that cover halves src[0..63] of one row
+// (src only 2-byte aligned).  Only words that hold at least one of the first `valid`
+// halves are read, so no read leaves the pages the real elements live on; the rest
+// stay zero.
+__device__ __forceinline__ void load_cover64(const __half* src, int valid, uint32_t (&v)[36]) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(src);
+    const uintptr_t base = a & ~uintptr_t(15);
+    const bool any = valid > 0;
+    const uintptr_t end = a + 2u * static_cast<uint32_t>(any ? valid : 0);
+#pragma unroll
+    for (int q = 0; q < 9; ++q) {
+        const uintptr_t wa = base + 16u * q;
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (any && wa < end) x = __ldg(reinterpret_cast<const uint4*>(wa));
+        v[4 * q] = x.x;
+        v[4 * q + 1] = x.y;
+        v[4 * q + 2] = x.z;
+        v[4 * q + 3] = x.w;
+    }
+}
+
+// The 64 halves starting `sh` halves (0..7, per lane) into the covering words, as 32
+// words of two halves (low half first): word-granular selects by 2 and by 1 words,
+// then a 16-bit funnel shift for an odd `sh` — no divergence, no indexed registers.
+__device__ __forceinline__ void align_cover64(const uint32_t (&v)[36], uint32_t sh, uint32_t (&w)[32]) {
+    const bool by2 = (sh & 4u) != 0, by1 = (sh & 2u) != 0, odd = (sh & 1u) != 0;
+    uint32_t t[34];
+#pragma unroll
+    for (int i = 0; i < 34; ++i) t[i] = by2 ? v[i + 2] : v[i];
+    uint32_t u[33];
+#pragma unroll
+    for (int i = 0; i < 33; ++i) u[i] = by1 ? t[i + 1] : t[i];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = odd ? __funnelshift_r(u[i], u[i + 1], 16) : u[i];
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -274,7 +311,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
-        if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C) prefetch_tensormap(&tmD);
+        if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) prefetch_tensormap(&tmD);
         if constexpr (EPI == EPI_TMA_C) prefetch_tensormap(&tmC);
     }
     if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -446,6 +483,26 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if constexpr (EPI == EPI_TMA_C) {
                 if (!partial) issue_first_c();
             }
+            // Misaligned C: the words covering this thread's row of 64-column chunk c,
+            // requested one chunk ahead (the first before the accumulator is ready) and
+            // shifted into place when the chunk is written.
+            uint32_t ccover[36];
+            uint32_t c_sh = 0;
+            auto prefetch_cg = [&](int c) {
+                const int64_t row = arow0 + lane;
+                const int64_t col0 = acol0 + c * 64;
+                const __half* src = static_cast<const __half*>(p.C);
+                int valid = 0;
+                if (row < p.M && col0 < p.N) {
+                    valid = static_cast<int>(p.N - col0 < 64 ? p.N - col0 : 64);
+                    src += static_cast<int64_t>(w.b) * p.strideC + row * p.ldc + col0;
+                }
+                c_sh = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u) >> 1;
+                load_cover64(src, valid, ccover);
+            };
+            if constexpr (EPI == EPI_TMA_CG) {
+                if (!partial) prefetch_cg(0);
+            }
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, p.err, p.timeout_ns, abort_flag, 5) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -503,7 +560,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // (stream-K fixup, PARTS) from the sum of the contributors' partials.
             auto emit_tile = [&](auto parts_tag) {
                 constexpr bool PARTS = decltype(parts_tag)::value;
-                if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C) {
+                if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) {
                     auto fetch64 = [&](int c, uint32_t (&v0)[32], uint32_t (&v1)[32]) {
                         if constexpr (!PARTS && ACC16) {
                             acc_ld32(c * 64, v0);
@@ -527,7 +584,45 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         }
                         ++chunk_count;
                     };
-                    if constexpr (!tma_c) {
+                    if constexpr (EPI == EPI_TMA_CG) {
+                        // D = alpha * acc + beta * C, C read from global memory at its own alignment
+                        if constexpr (PARTS) prefetch_cg(0);
+#pragma unroll 1
+                        for (int c = 0; c < BN / 64; ++c) {
+                            uint32_t cw[32];
+                            align_cover64(ccover, c_sh, cw);
+                            if (c + 1 < BN / 64) prefetch_cg(c + 1);
+                            uint32_t v0[32], v1[32];
+                            fetch64(c, v0, v1);
+                            const uint32_t buf = chunk_count & 1u;
+                            if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+                            __syncwarp();
+                            const uint32_t sb = smem_u32(ebuf) + buf * 4096u;
+                            const uint32_t row_addr = sb + lane * 128u;
+                            const float al = p.alpha, be = p.beta;
+                            // alpha * acc + beta * C for two columns, rounded once to fp16
+                            auto o2 = [&](uint32_t xa, uint32_t xb, uint32_t cword) {
+                                const float2 cf = __half22float2(*reinterpret_cast<const __half2*>(&cword));
+                                return pack_half2(fmaf(be, cf.x, al * __uint_as_float(xa)),
+                                                  fmaf(be, cf.y, al * __uint_as_float(xb)));
+                            };
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4),
+                                             o2(v0[8 * j + 0], v0[8 * j + 1], cw[4 * j + 0]),
+                                             o2(v0[8 * j + 2], v0[8 * j + 3], cw[4 * j + 1]),
+                                             o2(v0[8 * j + 4], v0[8 * j + 5], cw[4 * j + 2]),
+                                             o2(v0[8 * j + 6], v0[8 * j + 7], cw[4 * j + 3]));
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                st_shared_v4(row_addr + ((static_cast<uint32_t>(j + 4) ^ (lane & 7u)) << 4),
+                                             o2(v1[8 * j + 0], v1[8 * j + 1], cw[16 + 4 * j + 0]),
+                                             o2(v1[8 * j + 2], v1[8 * j + 3], cw[16 + 4 * j + 1]),
+                                             o2(v1[8 * j + 4], v1[8 * j + 5], cw[16 + 4 * j + 2]),
+                                             o2(v1[8 * j + 6], v1[8 * j + 7], cw[16 + 4 * j + 3]));
+                            store_chunk(c, sb);
+                        }
+                    } else if constexpr (!tma_c) {
                         // D = alpha * acc
 #pragma unroll 1
                         for (int c = 0; c < BN / 64; ++c) {
@@ -756,7 +851,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             }
         }
-        if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C) {
+        if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) {
             if (lane == 0) bulk_wait_group<0>();
             __syncwarp();
         }

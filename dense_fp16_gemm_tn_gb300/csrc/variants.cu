@@ -17,23 +17,31 @@ bool capacity_family_swap(const TcVariant&, int, int64_t*);
 static const TcVariant kVariants[] = {
     {256, 1, 4, EPI_TMA, 0, 0},
     {256, 1, 4, EPI_TMA_C, 0, 0},
+    {256, 1, 4, EPI_TMA_CG, 0, 0},
     {256, 1, 4, EPI_TMA, 1, 0},
     {256, 1, 4, EPI_TMA_A16, 0, 0},
     {256, 1, 4, EPI_TMA_C, 1, 0},
+    {256, 1, 4, EPI_TMA_CG, 1, 0},
     {256, 2, 6, EPI_TMA, 0, 0},
     {256, 2, 6, EPI_TMA_C, 0, 0},
+    {256, 2, 6, EPI_TMA_CG, 0, 0},
     {256, 2, 6, EPI_TMA, 1, 0},
     {256, 2, 6, EPI_TMA_A16, 0, 0},
     {256, 2, 6, EPI_TMA_C, 1, 0},
+    {256, 2, 6, EPI_TMA_CG, 1, 0},
     {128, 1, 6, EPI_TMA, 0, 0},
     {128, 1, 6, EPI_TMA_C, 0, 0},
+    {128, 1, 6, EPI_TMA_CG, 0, 0},
     {128, 1, 6, EPI_TMA, 1, 0},
     {128, 1, 6, EPI_TMA_A16, 0, 0},
     {128, 1, 6, EPI_TMA_C, 1, 0},
+    {128, 1, 6, EPI_TMA_CG, 1, 0},
     {128, 2, 8, EPI_TMA, 0, 0},
     {128, 2, 8, EPI_TMA_C, 0, 0},
+    {128, 2, 8, EPI_TMA_CG, 0, 0},
     {128, 2, 8, EPI_TMA, 1, 0},
     {128, 2, 8, EPI_TMA_C, 1, 0},
+    {128, 2, 8, EPI_TMA_CG, 1, 0},
     {256, 1, 4, EPI_GENERIC, 0, 0},
     {256, 1, 4, EPI_GENERIC, 1, 0},
     {256, 1, 4, EPI_GENERIC_A16, 0, 0},

@@ -252,7 +252,9 @@ typedef struct {
     int32_t swap_ab;         /* 1: computes D^T = B . A^T (small M) */
     int32_t splits;          /* K slices (1 = no split) */
     int32_t stages;          /* shared-memory pipeline depth */
-    int32_t epi_tma;         /* 1: D written (and C read, if beta != 0) by tensor copies; 0: plain predicated accesses */
+    int32_t epi_tma;         /* 1: D written by tensor copies (C, if beta != 0, read by tensor copies when
+                                its rows are 16-byte aligned, else by the epilogue's own aligned
+                                loads); 0: plain predicated accesses */
     int32_t pack_a;          /* 1: A is first repacked to an aligned scratch copy */
     int32_t pack_b;          /* 1: B is first repacked */
     int64_t units;           /* work units (tiles x splits x batch) */
@@ -262,9 +264,10 @@ typedef struct {
     int32_t sk_maxc;         /* stream-K: largest number of CTA groups contributing to one tile */
     int64_t dp_tiles;        /* tiles computed whole (data-parallel), before the stream-K tiles */
     int64_t sk_tiles;        /* tiles shared out by k-block */
-    int32_t stage_cd;        /* bit 0: C copied to an aligned scratch copy first; bit 1: D written
-                                to an aligned scratch copy by tensor copies, then moved into place
-                                (large problems whose C or D rows are not 16-byte aligned) */
+    int32_t stage_cd;        /* bit 1: D written to an aligned scratch copy by tensor copies, then
+                                moved into place (large problems whose D rows are not 16-byte
+                                aligned); bit 0 is always 0 (C of any alignment is read by the
+                                epilogue directly) */
     int32_t reserved;
 } gemm_tn_plan_t;
 

@@ -1,7 +1,8 @@
-"""Large problems whose C or D rows TMA cannot address: C is repacked and D written
-to an aligned scratch copy, then moved into place (plan field stage_cd).  Against the
-oracle element by element, with guard bands around D, and against the predicated
-epilogue the same problems took before."""
+"""Problems whose C or D rows TMA cannot address.  D: written by TMA to an aligned
+scratch copy, then moved into place (large problems; plan field stage_cd).  C: read
+where it is by the TMA epilogue's own aligned loads, at any 2-byte alignment, shifted
+into place per row.  Against the oracle element by element, with guard bands around D,
+and against the predicated epilogue bit for bit."""
 import numpy as np
 import pytest
 
@@ -30,7 +31,57 @@ def test_staged_c_d(name, M, N, K, batch, ldc, ldd, beta):
 
 def test_staged_plan_is_taken():
     p = G.gemm_tn_f16_plan(1100, 1000, 320, 1, 320, 320, 1001, 1003, 0, 0, 0, 0, 1.5, 15, 152)
-    assert p["stage_cd"] == 3 and p["epi_tma"] == 1
+    assert p["stage_cd"] == 2 and p["epi_tma"] == 1
+
+
+C_CASES = [
+    # name, M, N, K, batch, ldc, beta, stream-K expected
+    ("small_odd_ldc", 256, 256, 192, 1, 257, 1.0, None),
+    ("ragged_n_odd_ldc", 300, 1000, 256, 1, 1001, -0.5, None),
+    ("single_stream_k", 1280, 1280, 1024, 1, 1283, 0.75, 1),
+    ("pair_stream_k", 2560, 2560, 1024, 1, 2563, -1.5, 1),
+    ("batched_odd_stride", 200, 392, 128, 3, 395, 1.25, None),
+    ("narrow_n", 520, 72, 96, 1, 75, 2.0, None),
+]
+
+
+@pytest.mark.parametrize("name,M,N,K,batch,ldc,beta,sk", C_CASES, ids=[c[0] for c in C_CASES])
+def test_c_read_in_place(name, M, N, K, batch, ldc, beta, sk):
+    """Misaligned C with an aligned D: the TMA epilogue reads C itself, nothing is staged."""
+    p = G.gemm_tn_f16_plan(M, N, K, batch, K, K, ldc, N, M * K, N * K, M * ldc, M * N, beta, 15, 152)
+    assert p["epi_tma"] == 1 and p["stage_cd"] == 0
+    if sk is not None:
+        assert p["stream_k"] == sk
+    run_problem(M, N, K, batch=batch, ldc=ldc, ldd=N, alpha=0.5, beta=beta, seed=len(name) + 40, d_pad_rows=2)
+
+
+def test_c_read_in_place_misaligned_base_every_row_shift():
+    """C starts 2 bytes past a 16-byte boundary and its leading dimension is odd, so the
+    eight possible shifts occur row after row; the last row ends at the end of C's buffer."""
+    t = torch()
+    M, N, K, ldc = 1031, 520, 200, 523
+    A = inputs.uniform_half(21, M, K)
+    B = inputs.uniform_half(22, N, K)
+    C = inputs.with_ld(inputs.uniform_half(23, M, N), ldc).reshape(-1)[: (M - 1) * ldc + N]
+    ref = oracle.gemm_tn(A, B, C, M, N, K, -0.75, 1.5, ldc=ldc, ldd=N)
+    cbuf = t.zeros((C.size + 1,), dtype=t.int16, device="cuda")
+    cbuf[1:] = t.from_numpy(C.view(np.int16)).cuda()
+    dC = cbuf.view(t.float16)[1:]
+    dD = t.full((M * N + 2 * N,), 0, dtype=t.int16, device="cuda")
+    dD.fill_(np.int16(np.uint16(SENTINEL).view(np.int16)))
+    dD = dD.view(t.float16)
+    G.gemm_tn_f16(to_dev(A), K, to_dev(B), K, dC, ldc, dD, N, M, N, K, -0.75, 1.5)
+    t.cuda.synchronize()
+    assert_device_ok()
+    got = to_host(dD)
+    assert (got[M * N:] == SENTINEL).all(), "store past the end of D"
+    assert_close(got[: M * N], ref, K, what="misaligned C base")
+
+
+def test_c_read_in_place_small_integers_bit_exact():
+    run_problem(1100, 1000, 256, ldc=1001, ldd=1000, beta=-1.0, dist="int", compare="exact", seed=6, d_pad_rows=2)
+    run_problem(600, 640, 512, ldc=645, ldd=640, beta=1.0, dist="int", compare="exact", seed=7, d_pad_rows=2,
+                opts=dict(stream_k=1))
 
 
 def test_staged_small_integers_bit_exact():
