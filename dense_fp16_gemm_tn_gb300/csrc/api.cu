@@ -260,15 +260,15 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
     pub.sk_tiles = 0;
     pl.sk_iters = 0;
     pl.sk_w_bytes = pl.sk_ctr_bytes = 0;
-    const bool sk_epi = pl.epi == EPI_TMA || pl.epi == EPI_TMA_C || pl.epi == EPI_TMA_CG || pl.epi == EPI_GENERIC ||
-                        pl.epi == EPI_SWAP;
+    const bool sk_epi = pl.epi == EPI_TMA || pl.epi == EPI_TMA_C || pl.epi == EPI_TMA_CG || pl.epi == EPI_VEC ||
+                        pl.epi == EPI_GENERIC || pl.epi == EPI_SWAP;
     // Automatic stream-K when whole tiles would leave much of the machine idle.  At
     // full occupancy the GEMM runs at the power limit, so a partly empty last wave
     // costs less than its share; with the TMA epilogue the fixup is cheap enough
     // to pay from 10% idle, with the predicated one only from 40%.  Forced on, it
     // applies whenever the tiles do not divide evenly.
     const int64_t mode = g_opt_stream_k.load();
-    const double threshold = mode > 0 ? 1.0 : ((pl.epi == EPI_TMA || pl.epi == EPI_TMA_C || pl.epi == EPI_TMA_CG) ? 0.9 : 0.6);
+    const double threshold = mode > 0 ? 1.0 : ((pl.epi == EPI_TMA || pl.epi == EPI_TMA_C || pl.epi == EPI_TMA_CG || pl.epi == EPI_VEC) ? 0.9 : 0.6);
     if (mode >= 0 && sk_epi && pub.splits == 1 && kb >= 8 && tiles % G != 0) {
         const double dp_eff = static_cast<double>(tiles) / static_cast<double>(ceil_div(tiles, G) * G);
         // Every group must get at least one iteration (contributors to a tile are
@@ -365,16 +365,21 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     }
 
     // A large problem whose D rows TMA cannot address writes D by TMA to an aligned
-    // scratch copy that is moved into place after (two streaming passes cost less than
-    // the predicated epilogue's element accesses).  C at any alignment is read by the
-    // epilogue itself (EPI_TMA_CG) whenever D can take the TMA path, staged or not.
+    // scratch copy that is moved into place after: two streaming passes cost less than
+    // the predicated epilogue's element accesses, and on 4095 x 3073 x 2047 with an odd
+    // ldd less than the row-word epilogue's scattered stores (65.2 against 69.6 us).  C at
+    // any alignment is read by the epilogue itself (EPI_TMA_CG, EPI_VEC).
     const bool force_generic = g_opt_force_generic.load() != 0;
-    const bool stage = !pr.acc16 && splits == 1 && !swap && !force_generic && (!d_ok || !c_ok) &&
+    const bool stage = !pr.acc16 && splits == 1 && !swap && !force_generic && !d_ok &&
                        pr.M * pr.N * pr.batch >= kStageMinElems;
+    // A smaller problem with such a D writes it from the epilogue, row by row, through the
+    // aligned words that cover each row segment (EPI_VEC).
+    const bool vec = !pr.acc16 && splits == 1 && !swap && !force_generic && !d_ok && !stage;
     int epi;
     if (pr.acc16) epi = (pr.beta == 0.0f && d_ok && !force_generic) ? EPI_TMA_A16 : EPI_GENERIC_A16;
     else if (splits > 1) epi = swap ? EPI_PARTIAL_SWAP : EPI_PARTIAL;
     else if (swap) epi = EPI_SWAP;
+    else if (vec) epi = EPI_VEC;
     else if ((d_ok && !force_generic) || stage) epi = pr.beta == 0.0f ? EPI_TMA : (c_ok ? EPI_TMA_C : EPI_TMA_CG);
     else epi = EPI_GENERIC;
     if (stage) {

@@ -1,4 +1,5 @@
-// Variants with predicated epilogues (alpha/beta, any alignment) and split-K partial sums.
+// Variants with predicated epilogues (alpha/beta, any alignment), split-K partial sums, and the
+// row-word epilogue for C and D at any alignment.
 #include "tc_launch.cuh"
 
 namespace gtn {
@@ -21,6 +22,14 @@ bool launch_family_generic(const TcVariant& v, const CUtensorMap& tmA, const CUt
     GTN_CASE(128, 1, 6, EPI_GENERIC, 1)
     GTN_CASE(128, 1, 6, EPI_GENERIC_A16, 0)
     GTN_CASE(128, 1, 6, EPI_PARTIAL, 0)
+    GTN_CASE(256, 1, 4, EPI_VEC, 0)
+    GTN_CASE(256, 1, 4, EPI_VEC, 1)
+    GTN_CASE(256, 2, 6, EPI_VEC, 0)
+    GTN_CASE(256, 2, 6, EPI_VEC, 1)
+    GTN_CASE(128, 1, 6, EPI_VEC, 0)
+    GTN_CASE(128, 1, 6, EPI_VEC, 1)
+    GTN_CASE(128, 2, 8, EPI_VEC, 0)
+    GTN_CASE(128, 2, 8, EPI_VEC, 1)
 #undef GTN_CASE
     return false;
 }
@@ -41,6 +50,14 @@ bool capacity_family_generic(const TcVariant& v, int sms, int64_t* cap) {
     GTN_CASE(128, 1, 6, EPI_GENERIC, 1)
     GTN_CASE(128, 1, 6, EPI_GENERIC_A16, 0)
     GTN_CASE(128, 1, 6, EPI_PARTIAL, 0)
+    GTN_CASE(256, 1, 4, EPI_VEC, 0)
+    GTN_CASE(256, 1, 4, EPI_VEC, 1)
+    GTN_CASE(256, 2, 6, EPI_VEC, 0)
+    GTN_CASE(256, 2, 6, EPI_VEC, 1)
+    GTN_CASE(128, 1, 6, EPI_VEC, 0)
+    GTN_CASE(128, 1, 6, EPI_VEC, 1)
+    GTN_CASE(128, 2, 8, EPI_VEC, 0)
+    GTN_CASE(128, 2, 8, EPI_VEC, 1)
 #undef GTN_CASE
     return false;
 }

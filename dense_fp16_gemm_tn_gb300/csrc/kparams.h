@@ -15,6 +15,7 @@ enum EpiMode : int {
     EPI_TMA_A16 = 6,       // EPI_TMA with an fp16 accumulator
     EPI_GENERIC_A16 = 7,   // EPI_GENERIC with an fp16 accumulator
     EPI_TMA_CG = 8,        // EPI_TMA_C with C read straight from global memory at any 2-byte alignment
+    EPI_VEC = 9,           // D (and C) at any 2-byte alignment through aligned 16-byte words, per row
 };
 
 #ifdef __CUDACC__

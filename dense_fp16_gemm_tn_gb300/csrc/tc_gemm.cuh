@@ -52,6 +52,7 @@
 
 #include "kparams.h"
 #include "ptx.cuh"
+#include "rowio.h"
 
 namespace gtn {
 
@@ -82,8 +83,9 @@ struct TileCfg {
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N in [16,256], N%16==0");
     static_assert(BN_LOCAL % 8 == 0, "B tile must hold whole 8-row swizzle atoms");
     static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "tiles must stay 1024-byte aligned");
-    static_assert((epi_base(EPI) != EPI_TMA && EPI != EPI_TMA_C && EPI != EPI_TMA_CG) || BN % 64 == 0,
-                  "TMA epilogue stores 64-column chunks");
+    static_assert((epi_base(EPI) != EPI_TMA && EPI != EPI_TMA_C && EPI != EPI_TMA_CG && EPI != EPI_VEC) ||
+                      BN % 64 == 0,
+                  "the TMA and row-word epilogues work in 64-column chunks");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory per CTA");
     static_assert(PAIR == 1 || PAIR == 2, "CTA pair or single CTA");
 };
@@ -221,42 +223,6 @@ __device__ __forceinline__ void spin_ns(uint64_t ns) {
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
     const __half2 h = __floats2half2_rn(a, b);
     return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// Misaligned C: the 16-byte-aligned words that cover halves src[0..63] of one row
-// (src only 2-byte aligned).  Only words that hold at least one of the first `valid`
-// halves are read, so no read leaves the pages the real elements live on; the rest
-// stay zero.
-__device__ __forceinline__ void load_cover64(const __half* src, int valid, uint32_t (&v)[36]) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(src);
-    const uintptr_t base = a & ~uintptr_t(15);
-    const bool any = valid > 0;
-    const uintptr_t end = a + 2u * static_cast<uint32_t>(any ? valid : 0);
-#pragma unroll
-    for (int q = 0; q < 9; ++q) {
-        const uintptr_t wa = base + 16u * q;
-        uint4 x = make_uint4(0u, 0u, 0u, 0u);
-        if (any && wa < end) x = __ldg(reinterpret_cast<const uint4*>(wa));
-        v[4 * q] = x.x;
-        v[4 * q + 1] = x.y;
-        v[4 * q + 2] = x.z;
-        v[4 * q + 3] = x.w;
-    }
-}
-
-// The 64 halves starting `sh` halves (0..7, per lane) into the covering words, as 32
-// words of two halves (low half first): word-granular selects by 2 and by 1 words,
-// then a 16-bit funnel shift for an odd `sh` — no divergence, no indexed registers.
-__device__ __forceinline__ void align_cover64(const uint32_t (&v)[36], uint32_t sh, uint32_t (&w)[32]) {
-    const bool by2 = (sh & 4u) != 0, by1 = (sh & 2u) != 0, odd = (sh & 1u) != 0;
-    uint32_t t[34];
-#pragma unroll
-    for (int i = 0; i < 34; ++i) t[i] = by2 ? v[i + 2] : v[i];
-    uint32_t u[33];
-#pragma unroll
-    for (int i = 0; i < 33; ++i) u[i] = by1 ? t[i + 1] : t[i];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = odd ? __funnelshift_r(u[i], u[i + 1], 16) : u[i];
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -497,11 +463,10 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     valid = static_cast<int>(p.N - col0 < 64 ? p.N - col0 : 64);
                     src += static_cast<int64_t>(w.b) * p.strideC + row * p.ldc + col0;
                 }
-                c_sh = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(src) & 15u) >> 1;
-                load_cover64(src, valid, ccover);
+                c_sh = load_cover64(reinterpret_cast<const uint16_t*>(src), valid, ccover);
             };
-            if constexpr (EPI == EPI_TMA_CG) {
-                if (!partial) prefetch_cg(0);
+            if constexpr (EPI == EPI_TMA_CG || EPI == EPI_VEC) {
+                if (!partial && p.beta != 0.0f) prefetch_cg(0);
             }
             int ok = 1;
             if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, p.err, p.timeout_ns, abort_flag, 5) ? 1 : 0;
@@ -560,7 +525,56 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // (stream-K fixup, PARTS) from the sum of the contributors' partials.
             auto emit_tile = [&](auto parts_tag) {
                 constexpr bool PARTS = decltype(parts_tag)::value;
-                if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) {
+                if constexpr (EB == EPI_VEC) {
+                    // D (and C) at any 2-byte alignment: this thread's row, 64 columns at a
+                    // time, through the aligned 16-byte words that cover it; only the real
+                    // elements are written.  Same arithmetic and rounding as the TMA epilogue.
+                    const bool with_c = p.beta != 0.0f;
+                    if constexpr (PARTS) {
+                        if (with_c) prefetch_cg(0);
+                    }
+                    const int64_t row = arow0 + lane;
+                    __half* const drow =
+                        static_cast<__half*>(p.D) + static_cast<int64_t>(w.b) * p.strideD + row * p.ldd;
+#pragma unroll 1
+                    for (int c = 0; c < BN / 64; ++c) {
+                        uint32_t cw[32];
+                        if (with_c) {
+                            align_cover64(ccover, c_sh, cw);
+                            if (c + 1 < BN / 64) prefetch_cg(c + 1);
+                        }
+                        uint32_t v0[32], v1[32];
+                        if constexpr (!PARTS) {
+                            tmem_ld_32x32b_x32(t_row + c * 64, v0);
+                            tmem_ld_32x32b_x32(t_row + c * 64 + 32, v1);
+                            tmem_ld_wait();
+                        } else {
+                            sum_parts(c * 64, v0);
+                            sum_parts(c * 64 + 32, v1);
+                        }
+                        const float al = p.alpha, be = p.beta;
+                        uint32_t o[32];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float x0 = al * __uint_as_float(v0[2 * i]), x1 = al * __uint_as_float(v0[2 * i + 1]);
+                            float y0 = al * __uint_as_float(v1[2 * i]), y1 = al * __uint_as_float(v1[2 * i + 1]);
+                            if (with_c) {
+                                const float2 c0 = __half22float2(*reinterpret_cast<const __half2*>(&cw[i]));
+                                const float2 c1 = __half22float2(*reinterpret_cast<const __half2*>(&cw[16 + i]));
+                                x0 = fmaf(be, c0.x, x0);
+                                x1 = fmaf(be, c0.y, x1);
+                                y0 = fmaf(be, c1.x, y0);
+                                y1 = fmaf(be, c1.y, y1);
+                            }
+                            o[i] = pack_half2(x0, x1);
+                            o[16 + i] = pack_half2(y0, y1);
+                        }
+                        const int64_t col0 = acol0 + c * 64;
+                        const int valid =
+                            (row < p.M && col0 < p.N) ? static_cast<int>(p.N - col0 < 64 ? p.N - col0 : 64) : 0;
+                        store_row64(reinterpret_cast<uint16_t*>(drow + col0), valid, o);
+                    }
+                } else if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) {
                     auto fetch64 = [&](int c, uint32_t (&v0)[32], uint32_t (&v1)[32]) {
                         if constexpr (!PARTS && ACC16) {
                             acc_ld32(c * 64, v0);

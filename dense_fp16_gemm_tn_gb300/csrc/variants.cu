@@ -52,6 +52,14 @@ static const TcVariant kVariants[] = {
     {128, 1, 6, EPI_GENERIC, 1, 0},
     {128, 1, 6, EPI_GENERIC_A16, 0, 0},
     {128, 1, 6, EPI_PARTIAL, 0, 0},
+    {256, 1, 4, EPI_VEC, 0, 0},
+    {256, 1, 4, EPI_VEC, 1, 0},
+    {256, 2, 6, EPI_VEC, 0, 0},
+    {256, 2, 6, EPI_VEC, 1, 0},
+    {128, 1, 6, EPI_VEC, 0, 0},
+    {128, 1, 6, EPI_VEC, 1, 0},
+    {128, 2, 8, EPI_VEC, 0, 0},
+    {128, 2, 8, EPI_VEC, 1, 0},
     {16, 1, 12, EPI_SWAP, 0, 0},
     {16, 1, 12, EPI_SWAP, 1, 0},
     {32, 1, 11, EPI_SWAP, 0, 0},
