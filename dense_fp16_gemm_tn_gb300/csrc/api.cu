@@ -262,15 +262,29 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
     pl.sk_w_bytes = pl.sk_ctr_bytes = 0;
     const bool sk_epi = pl.epi == EPI_TMA || pl.epi == EPI_TMA_C || pl.epi == EPI_TMA_CG || pl.epi == EPI_VEC ||
                         pl.epi == EPI_GENERIC || pl.epi == EPI_SWAP;
-    // Automatic stream-K when whole tiles would leave much of the machine idle.  At
-    // full occupancy the GEMM runs at the power limit, so a partly empty last wave
-    // costs less than its share; with the TMA epilogue the fixup is cheap enough
-    // to pay from 10% idle, with the predicated one only from 40%.  Forced on, it
-    // applies whenever the tiles do not divide evenly.
+    // Stream-K trades the idle part of the last wave for fix-up work: every contributor
+    // to a split tile parks its fp32 partial (128 x tile_n per CTA) and the last one sums
+    // them and runs the epilogue, holding up its own later tiles meanwhile.  Measured on
+    // GB300 (data-parallel against stream-K), it pays only when the saved share of a wave
+    // is long or the partials are small:
+    //   - narrow swapped tiles (tile_n <= 32): 16x8192x8192 33.9 against 43.2 us;
+    //   - 128 or more k-blocks per tile: 2560^2x8192 67.9 against 82.2 us, 4096^2x8192
+    //     155 against 166 us (one loss, 256x8192x8192, where both sides are bound by
+    //     reading B: 65.7 against 59.6 us);
+    //   - 64 k-blocks per tile behind at least three whole waves, which hide the fix-ups:
+    //     4096^3 85.1 against 86.3 us, 5120^2x4096 124.8 against 128.0 us;
+    // and in each case the idle part of the last wave is worth at least 36 k-blocks
+    // (8192^3, last wave 47 % full: 586.9 against 597.0 us; 4096x8192x4096, 17 k-blocks:
+    // 154.8 against 150.1 us).  Shorter K, fewer waves, a small saving or many
+    // contributors per split tile lose, often badly: 2048^2x1024 32.9 against 14.3 us,
+    // 1280x4096x4096 (19 contributors per split tile) 99.9 against 47.1 us,
+    // 384x4096x4096 38.5 against 32.8 us.  Forced on, stream-K applies whenever the
+    // tiles do not divide evenly.
     const int64_t mode = g_opt_stream_k.load();
-    const double threshold = mode > 0 ? 1.0 : ((pl.epi == EPI_TMA || pl.epi == EPI_TMA_C || pl.epi == EPI_TMA_CG || pl.epi == EPI_VEC) ? 0.9 : 0.6);
     if (mode >= 0 && sk_epi && pub.splits == 1 && kb >= 8 && tiles % G != 0) {
-        const double dp_eff = static_cast<double>(tiles) / static_cast<double>(ceil_div(tiles, G) * G);
+        // k-blocks a group would idle through in the last data-parallel wave
+        const double saved_kb = static_cast<double>(ceil_div(tiles, G) * G - tiles) / static_cast<double>(G) *
+                                static_cast<double>(kb);
         // Every group must get at least one iteration (contributors to a tile are
         // then consecutive groups); with no whole wave, launch fewer groups instead.
         int64_t Gs = G;
@@ -279,17 +293,21 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
         const int64_t sk = tiles - dp;
         const int64_t I = sk * kb;
         TcVariant skv;
-        if (dp_eff < threshold && I >= Gs && find_tc_variant(pl.var.bn, pl.var.pair, pl.epi, 1, &skv)) {
+        if (I >= Gs && find_tc_variant(pl.var.bn, pl.var.pair, pl.epi, 1, &skv)) {
             auto owner = [&](int64_t i) { return ((i + 1) * Gs - 1) / I; };
             int64_t maxc = 1;
             for (int64_t t = 0; t < sk; ++t) maxc = std::max(maxc, owner((t + 1) * kb - 1) - owner(t * kb) + 1);
-            pub.stream_k = 1;
-            pub.sk_maxc = static_cast<int32_t>(maxc);
-            pub.dp_tiles = dp;
-            pub.sk_tiles = sk;
-            pl.sk_iters = I;
-            pl.sk_w_bytes = round_up(sk * maxc * pair * 128 * static_cast<int64_t>(pub.tile_n) * 4, 256);
-            pl.sk_ctr_bytes = round_up(sk * pair * 4 * 8, 256);
+            const bool narrow = pub.tile_n <= 32;
+            const bool pays = narrow || (maxc <= 8 && saved_kb >= 36.0 && (kb >= 128 || (kb >= 64 && tiles >= 3 * G)));
+            if (mode > 0 || pays) {
+                pub.stream_k = 1;
+                pub.sk_maxc = static_cast<int32_t>(maxc);
+                pub.dp_tiles = dp;
+                pub.sk_tiles = sk;
+                pl.sk_iters = I;
+                pl.sk_w_bytes = round_up(sk * maxc * pair * 128 * static_cast<int64_t>(pub.tile_n) * 4, 256);
+                pl.sk_ctr_bytes = round_up(sk * pair * 4 * 8, 256);
+            }
         }
     }
     find_tc_variant(pl.var.bn, pl.var.pair, pl.epi, pub.stream_k, &pl.var);

@@ -107,8 +107,9 @@ def test_plan_large_square_uses_cta_pairs_and_tma_store():
     p = plan(8192, 8192, 8192, sms=152)
     assert p["kernel"] == 2 and p["cta_pair"] == 2 and p["tile_m"] == 256 and p["tile_n"] == 256
     assert p["epi_tma"] == 1 and p["splits"] == 1 and p["pack_a"] == 0 and p["pack_b"] == 0
-    # 1024 tiles over 76 pairs = 13.5 waves: well filled, so data-parallel only by default
-    assert p["stream_k"] == 0 and p["units"] == 1024 and p["grid"] == 152 and p["workspace_bytes"] == 0
+    # 1024 tiles over 76 pairs = 13.5 waves; the half-empty last wave (68 k-blocks of 128 per
+    # group) is shared out by k-block
+    assert p["stream_k"] == 1 and p["dp_tiles"] == 13 * 76 and p["grid"] == 152
 
 
 def test_plan_forced_stream_k_splits_the_partial_wave():
@@ -138,10 +139,25 @@ def test_plan_skinny_m_swaps_and_streams_k():
 
 
 def test_plan_stream_k_needs_one_iteration_per_group():
-    p = plan(128, 128, 512)  # one tile, 8 k-blocks: only 8 groups take part
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 1)
+    try:
+        p = plan(128, 128, 512)  # one tile, 8 k-blocks: only 8 groups take part
+        q = plan(128, 128, 448)  # 7 k-blocks: too few to share out
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 0)
     assert p["stream_k"] == 1 and p["grid"] == 8 and p["sk_maxc"] == 8
-    p = plan(128, 128, 448)  # 7 k-blocks: too few to share out
-    assert p["stream_k"] == 0 and p["grid"] == 1
+    assert q["stream_k"] == 0 and q["grid"] == 1
+
+
+def test_plan_automatic_stream_k_only_where_it_was_measured_to_pay():
+    # long K or narrow swapped tiles: split the partial wave
+    for M, N, K in ((4096, 4096, 4096), (4096, 4096, 8192), (2560, 2560, 8192), (128, 8192, 8192), (16, 8192, 8192),
+                    (8192, 8192, 8192), (5120, 5120, 4096)):
+        assert plan(M, N, K, sms=152)["stream_k"] == 1, (M, N, K)
+    # short K, too few whole waves, or many contributors per split tile: data-parallel
+    for M, N, K in ((1024, 1024, 1024), (2048, 2048, 1024), (4096, 4096, 2048), (1280, 4096, 4096),
+                    (384, 4096, 4096), (2560, 2560, 1024), (4096, 8192, 4096)):
+        assert plan(M, N, K, sms=152)["stream_k"] == 0, (M, N, K)
 
 
 def test_plan_forced_splits_use_the_reduction_kernel():

@@ -63,7 +63,7 @@ CASES = [
     ("tma_c_beta", dict(M=300, N=520, K=200, alpha=0.5, beta=1.5)),
     ("generic_packed", dict(M=257, N=263, K=129, alpha=0.5, beta=1.5)),
     ("padded_ld", dict(M=200, N=136, K=100, lda=None, ldb=None, ldc=140, ldd=144, beta=-1.0)),
-    ("streamk", dict(M=1280, N=1280, K=1024)),
+    ("streamk", dict(M=1280, N=1280, K=1024, opts=dict(stream_k=1))),
     ("batched", dict(M=200, N=136, K=72, batch=3, alpha=0.125, beta=1.0)),
     ("k65", dict(M=130, N=136, K=65)),
     ("k7", dict(M=130, N=136, K=7)),

@@ -32,7 +32,7 @@ CASES = [
     ("tma_beta_bn128", dict(M=300, N=264, K=130, alpha=-1.0, beta=0.25, opts=dict(force_bn=128, force_pair=1))),
     ("tma_beta_pair", dict(M=600, N=776, K=520, alpha=0.5, beta=1.5, opts=dict(force_bn=256, force_pair=2))),
     ("tma_beta_ldc_padded", dict(M=257, N=264, K=96, alpha=0.5, beta=1.5, ldc=272, ldd=280)),
-    ("tma_beta_streamk", dict(M=1280, N=1280, K=1024, alpha=0.5, beta=1.5)),
+    ("tma_beta_streamk", dict(M=1280, N=1280, K=1024, alpha=0.5, beta=1.5, opts=dict(stream_k=1))),
     ("tma_beta_batched", dict(M=200, N=136, K=72, batch=3, alpha=0.125, beta=1.0)),
     ("tma_beta_batched_bcast_c_free", dict(M=256, N=256, K=128, batch=2, beta=-0.5)),
     ("packed_ragged", dict(M=257, N=263, K=129, alpha=0.5, beta=1.5)),
@@ -61,16 +61,16 @@ CASES = [
     ("batched_swap", dict(M=16, N=300, K=128, batch=3)),
     ("batched_short_k_normal", dict(M=512, N=512, K=64, batch=4, alpha=0.125, dist="normal")),
     # stream-K: the k-blocks of the tiles that do not fill a whole wave are spread over all CTA groups
-    ("streamk_pair_no_dp_wave", dict(M=1280, N=1280, K=1024)),
+    ("streamk_pair_no_dp_wave", dict(M=1280, N=1280, K=1024, opts=dict(stream_k=1))),
     ("streamk_pair_dp_plus_sk", dict(M=2560, N=2560, K=512, opts=dict(stream_k=1))),
     ("streamk_pair_generic_forced", dict(M=2000, N=1800, K=900, alpha=0.5, beta=1.5,
                                          opts=dict(stream_k=1, force_pair=2, force_bn=256))),
     ("streamk_single_tma_forced", dict(M=1100, N=1032, K=1000, opts=dict(stream_k=1, force_pair=1))),
-    ("streamk_pair_generic_beta", dict(M=1290, N=1288, K=1000, alpha=0.5, beta=1.5)),
-    ("streamk_single_packed_beta", dict(M=1500, N=1100, K=700, alpha=0.5, beta=1.5)),
+    ("streamk_pair_generic_beta", dict(M=1290, N=1288, K=1000, alpha=0.5, beta=1.5, opts=dict(stream_k=1))),
+    ("streamk_single_packed_beta", dict(M=1500, N=1100, K=700, alpha=0.5, beta=1.5, opts=dict(stream_k=1))),
     ("streamk_swap_skinny", dict(M=16, N=1024, K=4096)),
-    ("streamk_swap_beta", dict(M=40, N=2000, K=1000, alpha=0.5, beta=1.5)),
-    ("streamk_batched", dict(M=600, N=600, K=640, batch=3)),
+    ("streamk_swap_beta", dict(M=40, N=2000, K=1000, alpha=0.5, beta=1.5, opts=dict(stream_k=1))),
+    ("streamk_batched", dict(M=600, N=600, K=640, batch=3, opts=dict(stream_k=1))),
 ]
 
 

@@ -47,12 +47,16 @@ C_CASES = [
 
 @pytest.mark.parametrize("name,M,N,K,batch,ldc,beta,sk", C_CASES, ids=[c[0] for c in C_CASES])
 def test_c_read_in_place(name, M, N, K, batch, ldc, beta, sk):
-    """Misaligned C with an aligned D: the TMA epilogue reads C itself, nothing is staged."""
-    p = G.gemm_tn_f16_plan(M, N, K, batch, K, K, ldc, N, M * K, N * K, M * ldc, M * N, beta, 15, 152)
+    """Misaligned C with an aligned D: the TMA epilogue reads C itself, nothing is staged
+    (the stream-K cases force the split, so that the fix-up path reads C too)."""
+    opts = dict(stream_k=1) if sk else {}
+    with options(**opts):
+        p = G.gemm_tn_f16_plan(M, N, K, batch, K, K, ldc, N, M * K, N * K, M * ldc, M * N, beta, 15, 152)
     assert p["epi_tma"] == 1 and p["stage_cd"] == 0
     if sk is not None:
         assert p["stream_k"] == sk
-    run_problem(M, N, K, batch=batch, ldc=ldc, ldd=N, alpha=0.5, beta=beta, seed=len(name) + 40, d_pad_rows=2)
+    run_problem(M, N, K, batch=batch, ldc=ldc, ldd=N, alpha=0.5, beta=beta, seed=len(name) + 40, d_pad_rows=2,
+                opts=opts)
 
 
 def test_c_read_in_place_misaligned_base_every_row_shift():
