@@ -37,7 +37,10 @@
  * Alignment: every pointer must be 2-byte aligned.  Any leading dimension
  * and any 2-byte-aligned address is accepted; 16-byte aligned pointers with
  * leading dimensions (and batch strides) that are multiples of 8 take the
- * direct tensor-memory-accelerator path, other operands are first repacked.
+ * direct tensor-memory-accelerator path.  Otherwise: A and B are first repacked
+ * to aligned scratch copies; C is read by the epilogue from its own rows; D is
+ * written by the epilogue to its own rows (problems under 2^20 outputs) or through
+ * an aligned scratch copy moved into place afterwards (larger ones).
  *
  * Special cases: M == 0, N == 0 or batch == 0 does nothing and returns
  * GEMM_OK.  K == 0 gives D = beta*C (D = 0 when beta == 0).  When beta == 0,
@@ -291,10 +294,12 @@ GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int6
  *   GEMM_TN_OPT_FORCE_GENERIC_EPI 1: never use the TMA-store epilogue.
  *   GEMM_TN_OPT_FORCE_PACK        1: repack A and B through scratch even when aligned.
  *   GEMM_TN_OPT_STREAM_K          0 (default): spread the k-blocks of the tiles of a partial
- *                                 last wave over all CTA groups when whole tiles would use
- *                                 under 90% (TMA-store epilogue) or 60% (predicated
- *                                 epilogue) of the machine; 1: whenever the tiles do not
- *                                 divide evenly; -1: never.
+ *                                 last wave over all CTA groups where that was measured to
+ *                                 pay (narrow swapped tiles; or 128+ k-blocks per tile, or
+ *                                 64 behind three whole waves, with at least 36 k-blocks of
+ *                                 the last wave idle and at most 8 contributors per split
+ *                                 tile); 1: whenever the tiles do not divide evenly;
+ *                                 -1: never.
  * A forced setting that no compiled kernel supports for a problem is ignored.
  * Returns GEMM_ERR_INVALID_VALUE for an unknown option or an out-of-range value.
  */
