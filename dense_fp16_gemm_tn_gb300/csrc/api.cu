@@ -56,9 +56,6 @@ gemm_status_t cuda_fail(cudaError_t e) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-// Elements of D from which misaligned C / D are staged through aligned copies.
-constexpr int64_t kStageMinElems = int64_t(1) << 20;
-
 // A fresh 56-bit tag for each stream-K launch: splitmix64 of a process-wide
 // sequence number (a bijection, so no two launches share a tag), never zero.
 unsigned long long next_sk_epoch() {
@@ -220,8 +217,6 @@ struct Plan {
     int64_t ldo_a, ldo_b;        // leading dims of the packed copies
     int64_t pack_a_bytes, pack_b_bytes, partial_bytes;
     int64_t sk_w_bytes, sk_ctr_bytes;  // stream-K partial slots and arrival counters
-    int64_t ldo_cd;                    // leading dimension of the staged D copy
-    int64_t stage_d_bytes;
     int64_t sk_iters;
     int group_m;
 };
@@ -313,8 +308,7 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
     find_tc_variant(pl.var.bn, pl.var.pair, pl.epi, pub.stream_k, &pl.var);
     pub.units = pub.stream_k ? pub.dp_tiles : tiles * pub.splits;
     pub.grid = pub.stream_k ? std::min<int64_t>(G, tiles * kb) * pair : std::min<int64_t>(pub.units, G) * pair;
-    pub.workspace_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes +
-                          pl.stage_d_bytes;
+    pub.workspace_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes;
 }
 
 // Tensor-core tile plan; pure host arithmetic, no CUDA calls.
@@ -382,31 +376,22 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
         if (!swap) bn = 128;  // the partial-sum variant exists at 128 columns
     }
 
-    // A large problem whose D rows TMA cannot address writes D by TMA to an aligned
-    // scratch copy that is moved into place after: two streaming passes cost less than
-    // the predicated epilogue's element accesses, and on 4095 x 3073 x 2047 with an odd
-    // ldd less than the row-word epilogue's scattered stores (65.2 against 69.6 us).  C at
-    // any alignment is read by the epilogue itself (EPI_TMA_CG, EPI_VEC).
+    // D rows TMA cannot address are written by the epilogue itself, each thread its row,
+    // through the aligned 16-byte words that cover each row segment (EPI_VEC); C of any
+    // alignment is read the same way (EPI_TMA_CG, EPI_VEC).  Against the predicated
+    // epilogue, and against writing D by TMA to an aligned scratch copy moved into place
+    // afterwards, this measured faster at every size: 4095 x 3073 x 2047 with ldd 3073
+    // 59.5-60.4 against 64.4-64.9 us staged; 2048^2 x 1024 20.5 against 26.2; 512^3 12.3
+    // against 16.4 predicated.
     const bool force_generic = g_opt_force_generic.load() != 0;
-    const bool stage = !pr.acc16 && splits == 1 && !swap && !force_generic && !d_ok &&
-                       pr.M * pr.N * pr.batch >= kStageMinElems;
-    // A smaller problem with such a D writes it from the epilogue, row by row, through the
-    // aligned words that cover each row segment (EPI_VEC).
-    const bool vec = !pr.acc16 && splits == 1 && !swap && !force_generic && !d_ok && !stage;
+    const bool vec = !pr.acc16 && splits == 1 && !swap && !force_generic && !d_ok;
     int epi;
     if (pr.acc16) epi = (pr.beta == 0.0f && d_ok && !force_generic) ? EPI_TMA_A16 : EPI_GENERIC_A16;
     else if (splits > 1) epi = swap ? EPI_PARTIAL_SWAP : EPI_PARTIAL;
     else if (swap) epi = EPI_SWAP;
     else if (vec) epi = EPI_VEC;
-    else if ((d_ok && !force_generic) || stage) epi = pr.beta == 0.0f ? EPI_TMA : (c_ok ? EPI_TMA_C : EPI_TMA_CG);
+    else if (d_ok && !force_generic) epi = pr.beta == 0.0f ? EPI_TMA : (c_ok ? EPI_TMA_C : EPI_TMA_CG);
     else epi = EPI_GENERIC;
-    if (stage) {
-        pl.ldo_cd = round_up(pr.N, 8);
-        if (!d_ok) {
-            pub.stage_cd |= 2;
-            pl.stage_d_bytes = round_up(pr.batch * pr.M * pl.ldo_cd * 2, 256);
-        }
-    }
 
     TcVariant v;
     if (!find_tc_variant(bn, pair, epi, 0, &v)) {
@@ -516,10 +501,8 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
                                       64, boxB))
         pl.pub.pack_b = 1,
         pl.pack_b_bytes = round_up(((p.batch > 1 && p.sB != 0) ? p.batch : 1) * b_rows(p) * pl.ldo_b * 2, 256);
-    // staged C / D get their maps once the scratch copies exist
-    const bool stage_d = (pl.pub.stage_cd & 2) != 0;
     if ((epi_base(pl.epi) == EPI_TMA || pl.epi == EPI_TMA_C || pl.epi == EPI_TMA_CG) &&
-        ((!stage_d && !encode_map(&mapD, D, p.N, p.M, p.batch, p.ldd, p.sD, p.batch > 1, 64, 32)) ||
+        (!encode_map(&mapD, D, p.N, p.M, p.batch, p.ldd, p.sD, p.batch > 1, 64, 32) ||
          (pl.epi == EPI_TMA_C &&
           !encode_map(&mapC, C, p.N, p.M, p.batch, p.ldc, p.sC, p.batch > 1 && p.sC != 0, 64, 32)))) {
         TcVariant v;
@@ -528,8 +511,6 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
             pl.var = v;
             pl.epi = generic;
             pl.pub.epi_tma = 0;
-            pl.pub.stage_cd = 0;
-            pl.stage_d_bytes = 0;
         } else {
             return GEMM_ERR_UNSUPPORTED;
         }
@@ -543,8 +524,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     }
     plan_stream_k(p, pl, cap / pl.var.pair);
 
-    const int64_t ws_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes +
-                             pl.stage_d_bytes;
+    const int64_t ws_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes;
     uint8_t* ws = nullptr;
     if (ws_bytes > 0) {
         e = cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), static_cast<size_t>(ws_bytes), dev->pool, stream);
@@ -559,7 +539,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
 
     const bool a_batched = p.batch > 1 && p.sA != 0;
     const bool b_batched = p.batch > 1 && p.sB != 0;
-    RepackArgs jobs[3];
+    RepackArgs jobs[2];
     int njobs = 0;
     if (pl.pub.pack_a) {
         void* dst = ws;
@@ -578,13 +558,6 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
             release();
             return GEMM_ERR_UNSUPPORTED;
         }
-    }
-    uint8_t* const stage_base = ws + pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes +
-                                pl.sk_ctr_bytes;
-    void* const Ds = stage_d ? static_cast<void*>(stage_base) : nullptr;
-    if (stage_d && !encode_map(&mapD, Ds, p.N, p.M, p.batch, pl.ldo_cd, p.M * pl.ldo_cd, p.batch > 1, 64, 32)) {
-        release();
-        return GEMM_ERR_UNSUPPORTED;
     }
     if (njobs > 0) {
         e = launch_repack(jobs, njobs, dev->sms, stream);
@@ -642,10 +615,6 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     if (pl.pub.splits > 1) {
         e = launch_splitk_reduce(kp.W, pl.pub.splits, p.M, p.N, p.batch, alpha, p.beta, C, p.ldc, p.sC, D, p.ldd,
                                  p.sD, dev->sms, stream);
-        if (e != cudaSuccess) { release(); return cuda_fail(e); }
-    }
-    if (stage_d) {
-        e = launch_unpack(Ds, pl.ldo_cd, D, p.ldd, p.sD, p.M, p.N, p.batch, dev->sms, stream);
         if (e != cudaSuccess) { release(); return cuda_fail(e); }
     }
     release();

@@ -49,7 +49,7 @@ __device__ __forceinline__ uint4 window16(const uint32_t (&w)[8], uint32_t shift
 // in flight.
 constexpr int kRepackGroups = 4;
 
-constexpr int kMaxRepackJobs = 3;
+constexpr int kMaxRepackJobs = 2;
 struct RepackJobs {
     RepackJob j[kMaxRepackJobs];
     int64_t first_item[kMaxRepackJobs + 1];  // job i owns items [first_item[i], first_item[i + 1])
@@ -189,98 +189,6 @@ cudaError_t launch_repack(const RepackArgs* ops, int count, int sms, cudaStream_
     const int64_t want = (items + 7) / 8;
     int64_t blocks = want < static_cast<int64_t>(sms) * 4 ? want : static_cast<int64_t>(sms) * 4;
     repack_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(jobs);
-    return cudaGetLastError();
-}
-
-// dst[b][r][0..N) = src[b * M + r][0..N) for a source with a leading dimension lds that
-// is a multiple of 8 and a 16-byte aligned base (a staging copy the GEMM wrote with TMA)
-// and a destination rows of which start at any 2-byte boundary: the inverse of the
-// repack.  Destination blocks are the aligned 16-byte blocks that hold row elements; a
-// full block is one 16-byte store of halves shifted out of two source groups, the
-// partial first and last blocks of a row are written half by half.  Source groups past
-// the row's last element are not read.  A warp takes a span of 128 blocks of one row.
-struct UnpackJob {
-    const __half* src;
-    int64_t lds;
-    __half* dst;
-    int64_t ldd, stride_dst, rows, N, batch;
-};
-
-__global__ void __launch_bounds__(256, 4) unpack_rows_kernel(const UnpackJob j) {
-    constexpr int32_t kSpan = 32 * kRepackGroups;
-    const int32_t N = static_cast<int32_t>(j.N);
-    const int64_t bpr_max = (j.N + 7) / 8 + 1;           // blocks a row can touch
-    const int64_t cpr = (bpr_max + kSpan - 1) / kSpan;
-    const int64_t items_total = j.batch * j.rows * cpr;
-    const int lane = threadIdx.x & 31;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; item < items_total;
-         item += nwarps) {
-        const int64_t rb = item / cpr;  // b * rows + r
-        const int32_t span0 = static_cast<int32_t>(item - rb * cpr) * kSpan;
-        const int64_t bi = j.batch > 1 ? rb / j.rows : 0;
-        const int64_t r = rb - bi * j.rows;
-        const uint4* src_row = reinterpret_cast<const uint4*>(j.src + rb * j.lds);
-        __half* dst_row = j.dst + bi * j.stride_dst + r * j.ldd;
-        const int32_t o = static_cast<int32_t>((reinterpret_cast<uintptr_t>(dst_row) & 15u) / 2u);  // halves
-        __half* dst_blk0 = dst_row - o;  // 16-byte aligned
-        const int32_t nblk = (N + o + 7) / 8;
-        // destination block q holds elements 8q - o .. 8q - o + 7: the last o halves of
-        // source group q - 1 and the first 8 - o of group q
-        const uint32_t shift = static_cast<uint32_t>(16 - 2 * o) & 15u;  // bytes into the window
-        uint32_t w[kRepackGroups][8];
-#pragma unroll
-        for (int u = 0; u < kRepackGroups; ++u) {
-            const int32_t q = span0 + u * 32 + lane;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) w[u][t] = 0;
-            if (q < nblk) {
-                if (o == 0) {
-                    const uint4 v = src_row[q];
-                    w[u][0] = v.x; w[u][1] = v.y; w[u][2] = v.z; w[u][3] = v.w;
-                } else {
-                    if (q >= 1) {
-                        const uint4 v = src_row[q - 1];
-                        w[u][0] = v.x; w[u][1] = v.y; w[u][2] = v.z; w[u][3] = v.w;
-                    }
-                    if (8 * q < N) {
-                        const uint4 v = src_row[q];
-                        w[u][4] = v.x; w[u][5] = v.y; w[u][6] = v.z; w[u][7] = v.w;
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kRepackGroups; ++u) {
-            const int32_t q = span0 + u * 32 + lane;
-            if (q >= nblk) break;
-            const uint4 out = window16(w[u], shift);
-            const int32_t e0 = 8 * q - o;  // first element of this block
-            if (e0 >= 0 && e0 + 8 <= N) {
-                *reinterpret_cast<uint4*>(dst_blk0 + 8 * q) = out;
-            } else {
-                const uint32_t ow[4] = {out.x, out.y, out.z, out.w};
-#pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    const int32_t e = e0 + t;
-                    if (e >= 0 && e < N)
-                        dst_blk0[8 * q + t] = __ushort_as_half(static_cast<unsigned short>(ow[t >> 1] >> (16 * (t & 1))));
-                }
-            }
-        }
-    }
-}
-
-cudaError_t launch_unpack(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t stride_dst, int64_t rows,
-                          int64_t N, int64_t batch, int sms, cudaStream_t stream) {
-    if (rows == 0 || N == 0 || batch == 0) return cudaSuccess;
-    const UnpackJob j = {static_cast<const __half*>(src), lds, static_cast<__half*>(dst), ldd, stride_dst, rows, N,
-                         batch};
-    constexpr int64_t kSpan = 32 * kRepackGroups;
-    const int64_t items = batch * rows * (((N + 7) / 8 + 1 + kSpan - 1) / kSpan);
-    const int64_t want = (items + 7) / 8;
-    int64_t blocks = want < static_cast<int64_t>(sms) * 4 ? want : static_cast<int64_t>(sms) * 4;
-    unpack_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(j);
     return cudaGetLastError();
 }
 

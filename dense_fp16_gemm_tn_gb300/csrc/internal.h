@@ -44,12 +44,8 @@ struct RepackArgs {
     void* dst;
     int64_t ldo, rows, K, batch;
 };
-// Repacks up to three operands in one launch.
+// Repacks up to two operands in one launch.
 cudaError_t launch_repack(const RepackArgs* ops, int count, int sms, cudaStream_t stream);
-// Copies a staging matrix (leading dimension a multiple of 8, 16-byte aligned base,
-// batch entries rows x lds apart) into rows x N of a matrix with any 2-byte alignment.
-cudaError_t launch_unpack(const void* src, int64_t lds, void* dst, int64_t ldd, int64_t stride_dst, int64_t rows,
-                          int64_t N, int64_t batch, int sms, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const float* W, int32_t splits, int64_t M, int64_t N, int64_t batch, float alpha,
                                  float beta, const void* C, int64_t ldc, int64_t strideC, void* D, int64_t ldd,
                                  int64_t strideD, int sms, cudaStream_t stream);

@@ -2,8 +2,8 @@
 // 16-byte-aligned words that cover them.  The epilogue uses these for C and D rows
 // whose start or leading dimension rules out TMA (tensor copies need 16-byte-aligned
 // rows): every access is a whole aligned word, except the stores to the two edge words
-// of a segment, which go out element by element so that no byte outside the segment
-// is written.  Plain C++ off the device, so that the index arithmetic is tested on the
+// of a segment, which go out in smaller aligned pieces so that no byte outside the
+// segment is written.  Plain C++ off the device, so that the index arithmetic is tested on the
 // host.
 #pragma once
 
@@ -44,6 +44,46 @@ GTN_ROWIO void store_word16(uintptr_t addr, const uint32_t* w) {
 #endif
 }
 
+// Bytes [lo, hi) (even offsets, lo < hi <= 16) of the aligned 16-byte word at `wa`,
+// whose content is w0..w3, in at most three naturally aligned 2-, 4- or 8-byte stores
+// (a 2-byte piece up to 4-byte alignment, a 4-byte piece up to 8, an 8-byte piece, then
+// 4- and 2-byte pieces down to hi).
+GTN_ROWIO void store_part16(uintptr_t wa, uint32_t lo, uint32_t hi, uint32_t w0, uint32_t w1, uint32_t w2,
+                            uint32_t w3) {
+    auto word = [&](uint32_t o) { return (o & 8u) ? ((o & 4u) ? w3 : w2) : ((o & 4u) ? w1 : w0); };
+    auto put16 = [&](uint32_t o) {
+        const uint16_t v = static_cast<uint16_t>(word(o) >> (8u * (o & 2u)));
+#ifdef __CUDA_ARCH__
+        *reinterpret_cast<uint16_t*>(wa + o) = v;
+#else
+        std::memcpy(reinterpret_cast<void*>(wa + o), &v, 2);
+#endif
+    };
+    auto put32 = [&](uint32_t o) {
+        const uint32_t v = word(o);
+#ifdef __CUDA_ARCH__
+        *reinterpret_cast<uint32_t*>(wa + o) = v;
+#else
+        std::memcpy(reinterpret_cast<void*>(wa + o), &v, 4);
+#endif
+    };
+    auto put64 = [&](uint32_t o) {
+        const uint32_t a = (o & 8u) ? w2 : w0, b = (o & 8u) ? w3 : w1;
+#ifdef __CUDA_ARCH__
+        *reinterpret_cast<uint2*>(wa + o) = make_uint2(a, b);
+#else
+        const uint32_t v[2] = {a, b};
+        std::memcpy(reinterpret_cast<void*>(wa + o), v, 8);
+#endif
+    };
+    uint32_t o = lo;
+    if ((o & 2u) && o + 2u <= hi) { put16(o); o += 2u; }
+    if ((o & 4u) && o + 4u <= hi) { put32(o); o += 4u; }
+    if (!(o & 7u) && o + 8u <= hi) { put64(o); o += 8u; }
+    if (o + 4u <= hi) { put32(o); o += 4u; }
+    if (o + 2u <= hi) { put16(o); o += 2u; }
+}
+
 // The nine aligned words that cover halves src[0..63].  Only words holding at least one
 // of the first `valid` halves are read (so no read leaves the pages those elements live
 // on); the others are zero.  Returns the offset of src in its first word, in halves.
@@ -82,7 +122,7 @@ GTN_ROWIO void align_cover64(const uint32_t (&v)[36], uint32_t sh, uint32_t (&w)
 
 // Writes the first `valid` (0..64) of the 64 halves in o (32 words, low half first) to
 // dst: the mirror of align_cover64 places them in the covering words; whole words go out
-// as 16-byte stores, the edge words half by half.
+// as 16-byte stores, the two edge words in aligned pieces (store_part16).
 GTN_ROWIO void store_row64(uint16_t* dst, int valid, const uint32_t (&o)[32]) {
     if (valid <= 0) return;
     const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
@@ -109,12 +149,9 @@ GTN_ROWIO void store_row64(uint16_t* dst, int valid, const uint32_t (&o)[32]) {
         if (wa >= a && wa + 16u <= end) {
             store_word16(wa, z + 4 * q);
         } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const uintptr_t ha = wa + 2u * e;
-                if (ha >= a && ha < end)
-                    *reinterpret_cast<uint16_t*>(ha) = static_cast<uint16_t>(z[4 * q + (e >> 1)] >> (16 * (e & 1)));
-            }
+            const uint32_t lo = a > wa ? static_cast<uint32_t>(a - wa) : 0u;
+            const uint32_t hi = end < wa + 16u ? static_cast<uint32_t>(end - wa) : 16u;
+            store_part16(wa, lo, hi, z[4 * q], z[4 * q + 1], z[4 * q + 2], z[4 * q + 3]);
         }
     }
 }

@@ -37,10 +37,10 @@
  * Alignment: every pointer must be 2-byte aligned.  Any leading dimension
  * and any 2-byte-aligned address is accepted; 16-byte aligned pointers with
  * leading dimensions (and batch strides) that are multiples of 8 take the
- * direct tensor-memory-accelerator path.  Otherwise: A and B are first repacked
- * to aligned scratch copies; C is read by the epilogue from its own rows; D is
- * written by the epilogue to its own rows (problems under 2^20 outputs) or through
- * an aligned scratch copy moved into place afterwards (larger ones).
+ * direct tensor-memory-accelerator path.  Otherwise A and B are first repacked to
+ * aligned scratch copies, while C is read and D written by the epilogue in their
+ * own rows, through the aligned 16-byte words that cover each row segment (only
+ * D's own elements are ever written).
  *
  * Special cases: M == 0, N == 0 or batch == 0 does nothing and returns
  * GEMM_OK.  K == 0 gives D = beta*C (D = 0 when beta == 0).  When beta == 0,
@@ -257,7 +257,9 @@ typedef struct {
     int32_t stages;          /* shared-memory pipeline depth */
     int32_t epi_tma;         /* 1: D written by tensor copies (C, if beta != 0, read by tensor copies when
                                 its rows are 16-byte aligned, else by the epilogue's own aligned
-                                loads); 0: plain predicated accesses */
+                                loads); 0: D (and C) accessed by the epilogue's own loads and
+                                stores, through aligned 16-byte words (D rows not 16-byte
+                                aligned) or element by element (a forced predicated epilogue) */
     int32_t pack_a;          /* 1: A is first repacked to an aligned scratch copy */
     int32_t pack_b;          /* 1: B is first repacked */
     int64_t units;           /* work units (tiles x splits x batch) */
@@ -267,10 +269,8 @@ typedef struct {
     int32_t sk_maxc;         /* stream-K: largest number of CTA groups contributing to one tile */
     int64_t dp_tiles;        /* tiles computed whole (data-parallel), before the stream-K tiles */
     int64_t sk_tiles;        /* tiles shared out by k-block */
-    int32_t stage_cd;        /* bit 1: D written to an aligned scratch copy by tensor copies, then
-                                moved into place (large problems whose D rows are not 16-byte
-                                aligned); bit 0 is always 0 (C of any alignment is read by the
-                                epilogue directly) */
+    int32_t stage_cd;        /* always 0: no scratch copies of C or D are made (the epilogue reads
+                                C and writes D in place at any alignment) */
     int32_t reserved;
 } gemm_tn_plan_t;
 

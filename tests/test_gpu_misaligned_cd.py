@@ -1,8 +1,9 @@
-"""Problems whose C or D rows TMA cannot address.  D: written by TMA to an aligned
-scratch copy, then moved into place (large problems; plan field stage_cd).  C: read
-where it is by the TMA epilogue's own aligned loads, at any 2-byte alignment, shifted
-into place per row.  Against the oracle element by element, with guard bands around D,
-and against the predicated epilogue bit for bit."""
+"""Problems whose C or D rows TMA cannot address, at sizes past 2^20 outputs and with
+misaligned C beside an aligned D.  C is read where it is by the epilogue's own aligned
+loads, shifted into place per row (TMA epilogue, plan epi_tma 1, when D is aligned); a
+misaligned D is written in place by the row-word epilogue (epi_tma 0); nothing is staged
+(stage_cd 0).  Against the oracle element by element, with guard bands around D, and
+against the predicated epilogue bit for bit."""
 import numpy as np
 import pytest
 
@@ -25,13 +26,13 @@ CASES = [
 
 
 @pytest.mark.parametrize("name,M,N,K,batch,ldc,ldd,beta", CASES, ids=[c[0] for c in CASES])
-def test_staged_c_d(name, M, N, K, batch, ldc, ldd, beta):
+def test_large_misaligned_c_d(name, M, N, K, batch, ldc, ldd, beta):
     run_problem(M, N, K, batch=batch, ldc=ldc, ldd=ldd, alpha=0.5, beta=beta, seed=len(name), d_pad_rows=2)
 
 
-def test_staged_plan_is_taken():
+def test_large_misaligned_plan():
     p = G.gemm_tn_f16_plan(1100, 1000, 320, 1, 320, 320, 1001, 1003, 0, 0, 0, 0, 1.5, 15, 152)
-    assert p["stage_cd"] == 2 and p["epi_tma"] == 1
+    assert p["stage_cd"] == 0 and p["epi_tma"] == 0 and p["workspace_bytes"] == 0
 
 
 C_CASES = [
@@ -88,11 +89,11 @@ def test_c_read_in_place_small_integers_bit_exact():
                 opts=dict(stream_k=1))
 
 
-def test_staged_small_integers_bit_exact():
+def test_large_misaligned_small_integers_bit_exact():
     run_problem(1100, 1000, 256, ldc=1001, ldd=1003, beta=1.0, dist="int", compare="exact", seed=5, d_pad_rows=2)
 
 
-def test_staged_matches_predicated_epilogue_bitwise():
+def test_large_misaligned_matches_predicated_epilogue_bitwise():
     """Both epilogues compute alpha*acc + beta*c in fp32 and round once: same bits."""
     t = torch()
     M, N, K, ldc, ldd = 1100, 1000, 384, 1001, 1003
@@ -109,7 +110,7 @@ def test_staged_matches_predicated_epilogue_bitwise():
     assert t.equal(D1, D2)
 
 
-def test_staged_in_place_and_misaligned_base():
+def test_large_misaligned_in_place_and_misaligned_base():
     """D == C (same odd leading dimension), and a D whose base is 2 bytes off 16."""
     t = torch()
     M, N, K, ld = 1024, 1027, 256, 1027
@@ -131,7 +132,7 @@ def test_staged_in_place_and_misaligned_base():
     A2 = inputs.uniform_half(14, M2, K)
     B2 = inputs.uniform_half(15, N2, K)
     plan = G.gemm_tn_f16_plan(M2, N2, K, 1, K, K, N2, ld2, 0, 0, 0, 0, 0.0, 0b0111, 152)
-    assert plan["stage_cd"] == 2
+    assert plan["stage_cd"] == 0 and plan["epi_tma"] == 0
     G.gemm_tn_f16(to_dev(A2), K, to_dev(B2), K, None, N2, bufh[1:], ld2, M2, N2, K, 1.0, 0.0)
     t.cuda.synchronize()
     assert_device_ok()

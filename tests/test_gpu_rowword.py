@@ -1,5 +1,5 @@
-"""The row-word epilogue (plan: epi_tma 0, stage_cd 0 for problems under 2^20 outputs whose
-D rows TMA cannot address): each thread writes its row of D, and reads its row of C, through
+"""The row-word epilogue (plan: epi_tma 0, stage_cd 0 for problems whose D rows TMA cannot
+address, at any size): each thread writes its row of D, and reads its row of C, through
 the 16-byte-aligned words that cover the row segment, with element stores at the two edges.
 Against the oracle element by element with sentinels in D's padding columns and after its
 last row, and against the predicated epilogue bit for bit."""
