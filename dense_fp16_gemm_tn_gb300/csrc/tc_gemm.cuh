@@ -20,8 +20,11 @@
 //               There is no shared->register step: the tensor core reads its
 //               operands from shared memory itself.
 //   warps 2-5   epilogue: tcgen05.ld tensor memory -> registers, alpha/beta in
-//               fp32, one round-to-nearest-even to fp16, then TMA stores (or
-//               predicated stores for ragged / misaligned outputs).
+//               fp32, one round-to-nearest-even to fp16, then TMA stores; for a
+//               D whose rows TMA cannot address, each thread writes its row
+//               through the aligned 16-byte words that cover it (rowio.h); a
+//               predicated element-wise epilogue remains for forced use and
+//               fp16 accumulators.
 //
 // Two accumulators in tensor memory let the epilogue of one tile overlap the
 // main loop of the next.  The grid is persistent: CTA (or CTA pair) i takes
@@ -31,7 +34,8 @@
 //
 // Tails: TMA loads zero-fill rows/columns past M, N and K, and TMA stores
 // clip at the tensor bounds, so ragged shapes need no masks on the fast path;
-// the predicated epilogues mask element by element.
+// the row-word epilogue writes only a row's real elements, the predicated ones
+// mask element by element.
 //
 // Stream-K: when the tiles do not divide evenly over the CTA groups, the last
 // partial wave is not run tile by tile; its k-block iterations are spread
