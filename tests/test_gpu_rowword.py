@@ -90,3 +90,37 @@ def test_row_word_in_place_and_misaligned_base():
     assert got[0] == SENTINEL and (got[1 + M2 * ld2:] == SENTINEL).all()
     ref2 = oracle.gemm_tn(A2, B2, None, M2, N2, K, 1.0, 0.0, ldd=ld2)
     assert_close(got[1:1 + M2 * ld2], ref2, K, what="misaligned base")
+
+
+OFFSETS = [0, 1, 3, 7]
+
+
+@pytest.mark.parametrize("oc", OFFSETS)
+@pytest.mark.parametrize("od", OFFSETS)
+def test_row_word_base_offsets(oc, od):
+    """C and D starting 0, 2, 6 or 14 bytes past a 16-byte boundary, with odd leading
+    dimensions, one problem with a stream-K split and one without; sentinels before D,
+    in its padding columns and after it."""
+    t = torch()
+    for M, N, K, ldc, ldd, sk in ((200, 330, 96, 333, 335, 0), (300, 520, 1024, 521, 527, 1)):
+        A = inputs.uniform_half(40 + oc, M, K)
+        B = inputs.uniform_half(50 + od, N, K)
+        C = inputs.with_ld(inputs.uniform_half(60 + oc + od, M, N), ldc).reshape(-1)
+        ref = oracle.gemm_tn(A, B, C, M, N, K, 0.75, -1.25, ldc=ldc, ldd=ldd).reshape(M, ldd)
+        cbuf = t.zeros((C.size + 8,), dtype=t.int16, device="cuda")
+        cbuf[oc:oc + C.size] = t.from_numpy(C.view(np.int16)).cuda()
+        dbuf = t.full((M * ldd + 16,), 0, dtype=t.int16, device="cuda")
+        dbuf.fill_(np.int16(np.uint16(SENTINEL).view(np.int16)))
+        dC = cbuf.view(t.float16)[oc:]
+        dD = dbuf.view(t.float16)[od:]
+        with options(stream_k=1 if sk else -1):
+            p = G.gemm_tn_f16_plan(M, N, K, 1, K, K, ldc, ldd, 0, 0, 0, 0, -1.25, 0b0011, 152)
+            G.gemm_tn_f16(to_dev(A), K, to_dev(B), K, dC, ldc, dD, ldd, M, N, K, 0.75, -1.25)
+            t.cuda.synchronize()
+        assert_device_ok()
+        assert p["epi_tma"] == 0 and p["stream_k"] == sk
+        got = to_host(dbuf.view(t.float16))
+        assert (got[:od] == SENTINEL).all() and (got[od + M * ldd:] == SENTINEL).all(), "store outside D"
+        body = got[od:od + M * ldd].reshape(M, ldd)
+        assert (body[:, N:] == SENTINEL).all(), "store into D's padding columns"
+        assert_close(body[:, :N], ref[:, :N], K, what=f"C offset {oc}, D offset {od}, stream-K {sk}")
