@@ -403,6 +403,9 @@ def time_score_softmax(G, device, flush_buf, read_buf, peaks, sms, steps=10, hea
             "l2": "flushed before every step"}
 
 
+NOMINAL_PEAKS = {"bf16_tflops": 2250.0, "hbm_gbs": 7900.0}  # dense fp16/bf16 tensor rate; HBM3e
+
+
 def roofline_tflops(w, peaks):
     tensor = peaks["bf16_tflops"]
     hbm = peaks["hbm_gbs"] * 1e9
@@ -550,12 +553,18 @@ def run_ours(args, rank, world, dist):
             tk, _ = time_steps(pk, G, steps_k, 3, flush, dist, read_buf)
             mk = statistics.median(tk)
             rk, bk = roofline_tflops(wk, peaks)
+            rn, _ = roofline_tflops(wk, NOMINAL_PEAKS)
             tfl = wk.flops / (mk * 1e-3) / 1e12
             per_config[key] = {"workload": wk.name, "tflops": tfl, "ms": mk, "bound": bk,
                                "l2": "flushed before every step" if needs_flush(wk) else "operands exceed twice the L2; not flushed",
                                "roofline_tflops": rk, "frac_of_roofline": tfl / rk,
+                               "roofline_tflops_nominal": rn, "frac_of_nominal_roofline": tfl / rn,
                                "frac_of_measured_peak": tfl / peaks["bf16_tflops"],
                                "hbm_gbs": wk.algorithmic_bytes / (mk * 1e-3) / 1e9}
+            if wk.flops < 1e9:
+                # latency-bound: also the time with operands left in L2 by the previous call
+                th, _ = time_steps(pk, G, steps_k, 3, flush, dist, None)
+                per_config[key]["ms_l2_hot"] = statistics.median(th)
             del pk
         st = G.gemm_tn_f16_last_device_error()
         if st != G.GEMM_OK:
@@ -566,6 +575,11 @@ def run_ours(args, rank, world, dist):
     if rank != 0:
         return
     cpu = None if args.skip_cpu_baseline else cpu_baseline(w)
+    clocks = clk.summary()
+    if clocks.get("sm_mhz"):
+        # 8192 dense fp16 FLOP per clock per SM at the SM clock sampled under load
+        clocks["peak_tflops_at_sm_mhz"] = sms * 8192 * clocks["sm_mhz"] * 1e6 / 1e12
+        clocks["frac_of_peak_at_sm_mhz"] = value / world / clocks["peak_tflops_at_sm_mhz"]
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -575,7 +589,7 @@ def run_ours(args, rank, world, dist):
         "frac_of_nominal_peak": value / world / 2250.0,
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": nl * args.steps,
         "plan": plan,
