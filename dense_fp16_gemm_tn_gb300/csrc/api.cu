@@ -293,7 +293,8 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
             int64_t maxc = 1;
             for (int64_t t = 0; t < sk; ++t) maxc = std::max(maxc, owner((t + 1) * kb - 1) - owner(t * kb) + 1);
             const bool narrow = pub.tile_n <= 32;
-            const bool pays = narrow || (maxc <= 8 && saved_kb >= 36.0 && (kb >= 128 || (kb >= 64 && tiles >= 3 * G)));
+            const bool pays = narrow || (pub.tile_n <= 256 && maxc <= 8 && saved_kb >= 36.0 &&
+                                         (kb >= 128 || (kb >= 64 && tiles >= 3 * G)));
             if (mode > 0 || pays) {
                 pub.stream_k = 1;
                 pub.sk_maxc = static_cast<int32_t>(maxc);
@@ -348,7 +349,17 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
         // when short K or few tiles make the pair's fixed costs dominate.
         const int64_t t_pair = ceil_div(pr.M, 256) * ceil_div(pr.N, 256) * pr.batch;
         const int64_t t_256 = ceil_div(pr.M, 128) * ceil_div(pr.N, 256) * pr.batch;
-        if (pr.K >= 512 && 2 * t_pair >= slots) {
+        // 256x512 pair tiles halve the B rows loaded per MMA and measured faster only with
+        // many full waves of long tiles (8192^3: 586-588 against 595-597 us); with fewer
+        // waves the coarser quantisation loses (4096^3: 87.5 against 83-87 us, and their
+        // 256 KB-per-CTA stream-K partials make the fix-up dearer than the idle wave: 98 us).
+        const int64_t t_wide = ceil_div(pr.M, 256) * ceil_div(pr.N, 512) * pr.batch;
+        const int64_t pairs = slots / 2;
+        const int64_t wide_tail = t_wide % pairs;
+        if (pr.K >= 8192 && t_wide >= 6 * pairs && (wide_tail == 0 || 10 * wide_tail >= 7 * pairs)) {
+            pair = 2;
+            bn = 512;
+        } else if (pr.K >= 512 && 2 * t_pair >= slots) {
             pair = 2;
             bn = 256;
         } else if (t_256 >= slots || pr.N > 128 * 8) {
@@ -359,7 +370,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
             bn = 128;
         }
         const int64_t fbn = g_opt_force_bn.load(), fpair = g_opt_force_pair.load();
-        if (fbn == 128 || fbn == 256) bn = static_cast<int>(fbn);
+        if (fbn == 128 || fbn == 256 || fbn == 512) bn = static_cast<int>(fbn);
         if (fpair == 1 || fpair == 2) pair = static_cast<int>(fpair);
     }
     const int64_t rows_a = swap ? pr.N : pr.M;
@@ -394,6 +405,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     else epi = EPI_GENERIC;
 
     TcVariant v;
+    if (bn == 512 && !find_tc_variant(bn, pair, epi, 0, nullptr)) bn = 256;  // 512 columns: CTA pairs, TMA epilogues
     if (!find_tc_variant(bn, pair, epi, 0, &v)) {
         // Fall back to the single-CTA variant of the same epilogue.
         pair = 1;
@@ -483,7 +495,8 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
 
     // Tensor maps first: an operand whose map the driver rejects is repacked instead.
     const bool swap = pl.pub.swap_ab != 0;
-    const uint32_t box_rows_b = static_cast<uint32_t>(pl.var.bn / pl.var.pair);
+    // B rows per box: one box per MMA of N <= 256 columns, split between a CTA pair
+    const uint32_t box_rows_b = static_cast<uint32_t>(std::min(pl.var.bn, 256) / pl.var.pair);
     CUtensorMap mapA_op, mapB_op, mapC, mapD;
     std::memset(&mapC, 0, sizeof(mapC));
     std::memset(&mapD, 0, sizeof(mapD));
@@ -507,10 +520,15 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
           !encode_map(&mapC, C, p.N, p.M, p.batch, p.ldc, p.sC, p.batch > 1 && p.sC != 0, 64, 32)))) {
         TcVariant v;
         const int generic = epi_acc16(pl.epi) ? EPI_GENERIC_A16 : EPI_GENERIC;
-        if (find_tc_variant(pl.var.bn, pl.var.pair, generic, 0, &v)) {
+        // (512-column tiles exist with TMA epilogues only: 256 columns, same B boxes)
+        if (find_tc_variant(pl.var.bn, pl.var.pair, generic, 0, &v) ||
+            find_tc_variant(std::min(pl.var.bn, 256), pl.var.pair, generic, 0, &v)) {
             pl.var = v;
             pl.epi = generic;
             pl.pub.epi_tma = 0;
+            pl.pub.stages = v.stages;
+            pl.pub.tile_n = v.bn;
+            pl.tiles_n = ceil_div(pl.rows_b, v.bn);
         } else {
             return GEMM_ERR_UNSUPPORTED;
         }
@@ -979,7 +997,7 @@ gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value) {
             return GEMM_OK;
         case GEMM_TN_OPT_SKIP_FIRST_LOAD: g_opt_skip_first_load = value ? 1 : 0; return GEMM_OK;
         case GEMM_TN_OPT_FORCE_BN:
-            if (value != 0 && value != 128 && value != 256) return GEMM_ERR_INVALID_VALUE;
+            if (value != 0 && value != 128 && value != 256 && value != 512) return GEMM_ERR_INVALID_VALUE;
             g_opt_force_bn = value;
             return GEMM_OK;
         case GEMM_TN_OPT_FORCE_PAIR:

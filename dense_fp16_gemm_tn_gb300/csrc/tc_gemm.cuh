@@ -15,7 +15,8 @@
 //               STAGES-deep shared-memory ring; `full`/`empty` mbarriers gate
 //               each slot (the multi-stage ring the smem_gemm page calls "09").
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128 or 256 for a
-//               CTA pair, N=BN, K=16, fp16 x fp16 -> fp32) straight from the
+//               CTA pair, N=BN, or two N=256 MMAs side by side for 512-column
+//               pair tiles, K=16, fp16 x fp16 -> fp32) straight from the
 //               shared-memory descriptors into a tensor-memory accumulator.
 //               There is no shared->register step: the tensor core reads its
 //               operands from shared memory itself.
@@ -27,7 +28,10 @@
 //               fp16 accumulators.
 //
 // Two accumulators in tensor memory let the epilogue of one tile overlap the
-// main loop of the next.  The grid is persistent: CTA (or CTA pair) i takes
+// main loop of the next.  A 512-column tile fills tensor memory with one
+// accumulator: the epilogue hands its first half back as soon as it has read
+// it, and the MMA starts the next tile's first k-block on that half while the
+// second half is still being read.  The grid is persistent: CTA (or CTA pair) i takes
 // work units i, i+G, i+2G, ... in an order grouped along M so that tiles
 // running at the same time share A and B rows in L2.  A work unit is one
 // output tile of one batch entry and, for split-K, one slice of K.
@@ -65,6 +69,16 @@ struct TileCfg {
     static constexpr int BM = 128;               // accumulator rows per CTA (tensor-memory lanes)
     static constexpr int BK = 64;                // halves per 128-byte swizzled row
     static constexpr int BN_LOCAL = BN / PAIR;   // B rows each CTA of a pair loads
+    // A 512-column pair tile is two N=256 MMAs per 16-wide K step, one per half of the
+    // tile's columns; each CTA loads one 128-row B box per MMA.
+    static constexpr int MMA_N = BN > 256 ? 256 : BN;
+    static constexpr int N_MMAS = BN / MMA_N;
+    static constexpr int B_BOX_ROWS = MMA_N / PAIR;
+    static constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;
+    // Accumulators in tensor memory (512 columns): two of BN <= 256 columns, so that the
+    // epilogue of one tile overlaps the main loop of the next; one of 512 columns, whose
+    // halves are released separately.
+    static constexpr int ACC_BUFS = (2 * BN <= 512) ? 2 : 1;
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN_LOCAL * BK * 2;
     static constexpr uint32_t STAGE_TX = uint32_t(A_BYTES + B_BYTES) * PAIR;
@@ -84,9 +98,13 @@ struct TileCfg {
     static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
     static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;  // + slack to align the base to 1024
 
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "tcgen05 M=128 needs N in [16,256], N%16==0");
+    static_assert(BN % 16 == 0 && BN >= 16 && (BN <= 256 || (BN == 512 && PAIR == 2)),
+                  "tcgen05 needs N in [16,256], N%16==0; 512 columns are two MMAs of a CTA pair");
+    static_assert(BN <= 256 || EPI == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG,
+                  "512-column tiles have the TMA epilogues only");
     static_assert(BN_LOCAL % 8 == 0, "B tile must hold whole 8-row swizzle atoms");
-    static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "tiles must stay 1024-byte aligned");
+    static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && B_BOX_BYTES % 1024 == 0,
+                  "tiles must stay 1024-byte aligned");
     static_assert((epi_base(EPI) != EPI_TMA && EPI != EPI_TMA_C && EPI != EPI_TMA_CG && EPI != EPI_VEC) ||
                       BN % 64 == 0,
                   "the TMA and row-word epilogues work in 64-column chunks");
@@ -301,7 +319,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             Seg w;
             while (ok && seg_next<SK>(p, it, w)) {
                 const int32_t rowA = w.tm * (Cfg::BM * PAIR) + Cfg::BM * static_cast<int32_t>(rank);
-                const int32_t rowB = w.tn * BN + Cfg::BN_LOCAL * static_cast<int32_t>(rank);
+                // B box nb holds tile columns nb*MMA_N + [0, MMA_N), split between the pair
+                const int32_t rowB = w.tn * BN + Cfg::B_BOX_ROWS * static_cast<int32_t>(rank);
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     if (!wait_bounded(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 1)) {
                         ok = false;
@@ -328,13 +347,18 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             for (int i = 0; i < Cfg::BM / 64; ++i)
                                 load(dA + 8192u * i, &tmA, rowA + 64 * i, kb * Cfg::BK, w.b * p.zA);
                         }
-                        if (!p.b_mn) {
-                            load(dB, &tmB, kb * Cfg::BK, rowB, w.b * p.zB);
-                        } else {
-                            if constexpr (Cfg::BN_LOCAL % 64 == 0) {
 #pragma unroll
-                                for (int i = 0; i < Cfg::BN_LOCAL / 64; ++i)
-                                    load(dB + 8192u * i, &tmB, rowB + 64 * i, kb * Cfg::BK, w.b * p.zB);
+                        for (int nb = 0; nb < Cfg::N_MMAS; ++nb) {
+                            const uint32_t dBn = dB + static_cast<uint32_t>(nb * Cfg::B_BOX_BYTES);
+                            const int32_t rowBn = rowB + nb * Cfg::MMA_N;
+                            if (!p.b_mn) {
+                                load(dBn, &tmB, kb * Cfg::BK, rowBn, w.b * p.zB);
+                            } else {
+                                if constexpr (Cfg::B_BOX_ROWS % 64 == 0) {
+#pragma unroll
+                                    for (int i = 0; i < Cfg::B_BOX_ROWS / 64; ++i)
+                                        load(dBn + 8192u * i, &tmB, rowBn + 64 * i, kb * Cfg::BK, w.b * p.zB);
+                                }
                             }
                         }
                     }
@@ -351,7 +375,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (leader CTA only)
         if (rank == 0 && lane == 0) {
-            const uint32_t IDESC = idesc_f16_f32(Cfg::BM * PAIR, BN, p.a_mn ? 1u : 0u, p.b_mn ? 1u : 0u, ACC16 ? 0u : 1u);
+            const uint32_t IDESC =
+                idesc_f16_f32(Cfg::BM * PAIR, Cfg::MMA_N, p.a_mn ? 1u : 0u, p.b_mn ? 1u : 0u, ACC16 ? 0u : 1u);
             // Per 16-wide K step: +32 bytes inside a K-major 128-byte row, +2048 bytes
             // (16 rows of 128 bytes) in an MN-major box.
             const uint32_t a_step = p.a_mn ? 128u : 2u, b_step = p.b_mn ? 128u : 2u;
@@ -367,9 +392,15 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             SegIter it = seg_begin<SK>(p, group, ngroups);
             Seg w;
             while (ok && seg_next<SK>(p, it, w)) {
-                if (!wait_bounded(tempty_bar(acc), acc_phase ^ 1u, p.err, p.timeout_ns, abort_flag, 3)) break;
+                // One accumulator of 512 columns: wait here for its first half only; the
+                // second half is waited for just before its first MMA, so that the tile's
+                // first k-block of MMAs runs while the epilogue still drains that half.
+                if (!wait_bounded(tempty_bar(Cfg::ACC_BUFS == 1 ? 0 : acc), acc_phase ^ 1u, p.err, p.timeout_ns,
+                                  abort_flag, 3))
+                    break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                bool hi_ready = Cfg::ACC_BUFS != 1;  // second half of the accumulator free
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     // The stage was written by TMA (async proxy) and completed through the
                     // mbarrier's transaction count: the wait alone orders the MMA's reads.
@@ -380,18 +411,33 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint64_t adesc = adesc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
                     const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
 #pragma unroll
-                    for (int k = 0; k < Cfg::BK / 16; ++k) {
-                        mma_f16<PAIR>(d_tmem, adesc + a_step * k, bdesc + b_step * k, IDESC,
-                                      (kb > w.kb0 || k > 0) ? 1u : 0u);
+                    for (int nb = 0; nb < Cfg::N_MMAS; ++nb) {
+                        if (nb == 1 && !hi_ready) {
+                            if (!wait_bounded(tempty_bar(1), acc_phase ^ 1u, p.err, p.timeout_ns, abort_flag, 3)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            hi_ready = true;
+                        }
+                        const uint64_t bdesc_n = bdesc + static_cast<uint64_t>(nb * (Cfg::B_BOX_BYTES >> 4));
+#pragma unroll
+                        for (int k = 0; k < Cfg::BK / 16; ++k) {
+                            mma_f16<PAIR>(d_tmem + static_cast<uint32_t>(nb * Cfg::MMA_N), adesc + a_step * k,
+                                          bdesc_n + b_step * k, IDESC, (kb > w.kb0 || k > 0) ? 1u : 0u);
+                        }
                     }
+                    if (!ok) break;
                     if constexpr (PAIR == 1) mma_commit(empty_bar(stage));
                     else mma_commit_pair(empty_bar(stage), 0x3);
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
+                if (ok && !hi_ready)  // (a segment always has k-blocks; keeps the phases in step regardless)
+                    ok = wait_bounded(tempty_bar(1), acc_phase ^ 1u, p.err, p.timeout_ns, abort_flag, 3);
                 if (!ok) break;
                 if constexpr (PAIR == 1) mma_commit(tfull_bar(acc));
                 else mma_commit_pair(tfull_bar(acc), 0x3);
-                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+                if (++acc == Cfg::ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
             }
         }
     } else {
@@ -478,6 +524,17 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             if (!ok) break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+            // This warp is done reading accumulator part `idx` (a whole accumulator, or a
+            // half of the single 512-column one).
+            auto arrive_tempty = [&](int idx) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (PAIR == 1) mbar_arrive(tempty_bar(idx));
+                    else mbar_arrive_cluster(map_to_cta(tempty_bar(idx), 0));
+                }
+            };
+            bool lo_released = false;
             // 32 accumulator columns of this thread's row as fp32 bits (fp16 accumulators widened).
             auto acc_ld32 = [&](int col, uint32_t (&v)[32]) {
                 if constexpr (!ACC16) {
@@ -529,6 +586,16 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // (stream-K fixup, PARTS) from the sum of the contributors' partials.
             auto emit_tile = [&](auto parts_tag) {
                 constexpr bool PARTS = decltype(parts_tag)::value;
+                // Called once chunk c (64 columns) has been read out of tensor memory: the
+                // first half of a 512-column accumulator goes back to the MMA early.
+                auto fetched = [&](int c) {
+                    if constexpr (!PARTS && Cfg::ACC_BUFS == 1) {
+                        if (c == BN / 128 - 1) {
+                            arrive_tempty(0);
+                            lo_released = true;
+                        }
+                    }
+                };
                 if constexpr (EB == EPI_VEC) {
                     // D (and C) at any 2-byte alignment: this thread's row, 64 columns at a
                     // time, through the aligned 16-byte words that cover it; only the real
@@ -612,6 +679,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             if (c + 1 < BN / 64) prefetch_cg(c + 1);
                             uint32_t v0[32], v1[32];
                             fetch64(c, v0, v1);
+                            fetched(c);
                             const uint32_t buf = chunk_count & 1u;
                             if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
                             __syncwarp();
@@ -646,6 +714,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         for (int c = 0; c < BN / 64; ++c) {
                             uint32_t v0[32], v1[32];
                             fetch64(c, v0, v1);
+                            fetched(c);
                             const uint32_t buf = chunk_count & 1u;
                             if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
                             __syncwarp();
@@ -677,6 +746,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         for (int c = 0; c < BN / 64; ++c) {
                             uint32_t v0[32], v1[32];
                             fetch64(c, v0, v1);
+                            fetched(c);
                             const uint32_t buf = chunk_count & 1u;
                             if (lane == 0) {
                                 // the other buffer's store (last chunk) must have read its data
@@ -816,13 +886,14 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             };
 
             auto release_accumulator = [&]() {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) {
-                    if constexpr (PAIR == 1) mbar_arrive(tempty_bar(acc));
-                    else mbar_arrive_cluster(map_to_cta(tempty_bar(acc), 0));
+                if constexpr (Cfg::ACC_BUFS == 1) {
+                    if (!lo_released) arrive_tempty(0);
+                    arrive_tempty(1);
+                    acc_phase ^= 1u;
+                } else {
+                    arrive_tempty(acc);
+                    if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
                 }
-                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             };
 
             if (!partial) {

@@ -10,7 +10,10 @@ bool launch_family_generic(const TcVariant&, const CUtensorMap&, const CUtensorM
                            const KParams&, int64_t, cudaStream_t, int64_t*, cudaError_t*);
 bool launch_family_swap(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const KParams&,
                         int64_t, cudaStream_t, int64_t*, cudaError_t*);
+bool launch_family_wide(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                        const KParams&, int64_t, cudaStream_t, int64_t*, cudaError_t*);
 bool capacity_family_tma(const TcVariant&, int, int64_t*);
+bool capacity_family_wide(const TcVariant&, int, int64_t*);
 bool capacity_family_generic(const TcVariant&, int, int64_t*);
 bool capacity_family_swap(const TcVariant&, int, int64_t*);
 
@@ -66,6 +69,12 @@ static const TcVariant kVariants[] = {
     {32, 1, 11, EPI_SWAP, 1, 0},
     {64, 1, 9, EPI_SWAP, 0, 0},
     {64, 1, 9, EPI_SWAP, 1, 0},
+    {512, 2, 4, EPI_TMA, 0, 0},
+    {512, 2, 4, EPI_TMA, 1, 0},
+    {512, 2, 4, EPI_TMA_C, 0, 0},
+    {512, 2, 4, EPI_TMA_C, 1, 0},
+    {512, 2, 4, EPI_TMA_CG, 0, 0},
+    {512, 2, 4, EPI_TMA_CG, 1, 0},
     {16, 1, 12, EPI_PARTIAL_SWAP, 0, 0},
     {32, 1, 11, EPI_PARTIAL_SWAP, 0, 0},
     {64, 1, 9, EPI_PARTIAL_SWAP, 0, 0},
@@ -93,6 +102,7 @@ cudaError_t launch_tc_variant(const TcVariant& v, const CUtensorMap& tmA, const 
                               cudaStream_t stream, int64_t* grid_out) {
     cudaError_t e = cudaErrorInvalidValue;
     if (launch_family_tma(v, tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out, &e)) return e;
+    if (launch_family_wide(v, tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out, &e)) return e;
     if (launch_family_generic(v, tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out, &e)) return e;
     if (launch_family_swap(v, tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out, &e)) return e;
     return cudaErrorInvalidValue;
@@ -100,7 +110,7 @@ cudaError_t launch_tc_variant(const TcVariant& v, const CUtensorMap& tmA, const 
 
 int64_t tc_variant_capacity(const TcVariant& v, int sms) {
     int64_t cap = 0;
-    if (capacity_family_tma(v, sms, &cap) || capacity_family_generic(v, sms, &cap) ||
+    if (capacity_family_tma(v, sms, &cap) || capacity_family_wide(v, sms, &cap) || capacity_family_generic(v, sms, &cap) ||
         capacity_family_swap(v, sms, &cap))
         return cap;
     return 0;

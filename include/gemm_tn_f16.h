@@ -287,7 +287,8 @@ GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int6
  *                                 load, so its MMA wait runs out and the kernel reports
  *                                 GEMM_ERR_TIMEOUT -- exercises the stall path without any
  *                                 fault.  Testing only; 0 restores normal operation.
- *   GEMM_TN_OPT_FORCE_BN          force the accumulator tile width (16..256), 0 = automatic.
+ *   GEMM_TN_OPT_FORCE_BN          force the tile width: 128, 256 or 512 (CTA pairs with a TMA
+ *                                 epilogue only; else 256), 0 = automatic.
  *   GEMM_TN_OPT_FORCE_PAIR        force 1 (single CTA) or 2 (CTA pair), 0 = automatic.
  *   GEMM_TN_OPT_FORCE_SPLITS      force the number of K slices, 0 = automatic.
  *   GEMM_TN_OPT_FORCE_SWAP        force operand swapping off (-1) or on (1), 0 = automatic.

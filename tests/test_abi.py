@@ -104,21 +104,49 @@ def plan(M, N, K, batch=1, lda=None, ldb=None, ldc=None, ldd=None, sA=0, sB=0, s
 
 
 def test_plan_large_square_uses_cta_pairs_and_tma_store():
-    p = plan(8192, 8192, 8192, sms=152)
+    p = plan(5120, 5120, 4096, sms=152)
     assert p["kernel"] == 2 and p["cta_pair"] == 2 and p["tile_m"] == 256 and p["tile_n"] == 256
     assert p["epi_tma"] == 1 and p["splits"] == 1 and p["pack_a"] == 0 and p["pack_b"] == 0
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 256)
+    try:
+        p = plan(8192, 8192, 8192, sms=152)
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 0)
     # 1024 tiles over 76 pairs = 13.5 waves; the half-empty last wave (68 k-blocks of 128 per
     # group) is shared out by k-block
-    assert p["stream_k"] == 1 and p["dp_tiles"] == 13 * 76 and p["grid"] == 152
+    assert p["tile_n"] == 256 and p["stream_k"] == 1 and p["dp_tiles"] == 13 * 76 and p["grid"] == 152
+
+
+def test_plan_wide_pair_tiles_only_for_many_full_waves_of_long_tiles():
+    # 8192^3: 512 tiles of 256 x 512 over 76 pairs, 6.7 waves, data-parallel
+    p = plan(8192, 8192, 8192, sms=152)
+    assert p["cta_pair"] == 2 and p["tile_m"] == 256 and p["tile_n"] == 512 and p["epi_tma"] == 1
+    assert p["stream_k"] == 0 and p["units"] == 512 and p["grid"] == 152 and p["stages"] == 4
+    assert plan(16384, 16384, 8192, sms=152)["tile_n"] == 512
+    # too few waves, short K, a mostly empty last wave, or an epilogue without TMA stores
+    for M, N, K, kw in ((4096, 4096, 4096, {}), (4096, 4096, 8192, {}), (8192, 8192, 4096, {}),
+                        (8192, 6144, 8192, {}), (8192, 8192, 8192, dict(ldd=8193)),
+                        (8192, 8192, 8192, dict(align=0b0111))):
+        assert plan(M, N, K, sms=152, **kw)["tile_n"] == 256, (M, N, K, kw)
+    # forced: 512 columns with CTA pairs and a TMA epilogue, else 256
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 512)
+    try:
+        assert plan(4096, 4096, 4096, sms=152)["tile_n"] == 512
+        assert plan(4096, 4096, 4096, sms=152, beta=1.0, ldc=4097)["tile_n"] == 512
+        assert plan(4096, 4096, 4096, sms=152, ldd=4097)["tile_n"] == 256
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 0)
 
 
 def test_plan_forced_stream_k_splits_the_partial_wave():
     G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 1)
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 256)
     try:
         p = plan(8192, 8192, 8192, sms=152)
         q = plan(8192, 8192, 8192, sms=128)  # 16 whole waves over 64 pairs: nothing to split
     finally:
         G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 0)
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 0)
     # 13 whole waves run data-parallel, the remaining tiles are shared by k-block
     assert p["stream_k"] == 1 and p["dp_tiles"] == 13 * 76 and p["sk_tiles"] == 1024 - 13 * 76
     assert p["grid"] == 152 and p["units"] == 13 * 76
@@ -152,8 +180,11 @@ def test_plan_stream_k_needs_one_iteration_per_group():
 def test_plan_automatic_stream_k_only_where_it_was_measured_to_pay():
     # long K or narrow swapped tiles: split the partial wave
     for M, N, K in ((4096, 4096, 4096), (4096, 4096, 8192), (2560, 2560, 8192), (128, 8192, 8192), (16, 8192, 8192),
-                    (8192, 8192, 8192), (5120, 5120, 4096)):
+                    (5120, 5120, 4096)):
         assert plan(M, N, K, sms=152)["stream_k"] == 1, (M, N, K)
+    # 256 x 512 tiles: their 256 KB-per-CTA partials did not pay back (8192^3 603-612 against
+    # 586-588 us data-parallel)
+    assert plan(8192, 8192, 8192, sms=152)["stream_k"] == 0
     # short K, too few whole waves, or many contributors per split tile: data-parallel
     for M, N, K in ((1024, 1024, 1024), (2048, 2048, 1024), (4096, 4096, 2048), (1280, 4096, 4096),
                     (384, 4096, 4096), (2560, 2560, 1024), (4096, 8192, 4096)):
@@ -222,7 +253,10 @@ def test_options_roundtrip_and_validation():
     p = plan(8192, 8192, 8192)
     assert p["tile_n"] == 128
     G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 0)
-    assert plan(8192, 8192, 8192)["tile_n"] == 256
+    assert plan(5120, 5120, 4096)["tile_n"] == 256
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 512)
+    assert G.gemm_tn_f16_get_option(G.GEMM_TN_OPT_FORCE_BN) == 512
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 0)
     with pytest.raises(G.GemmError):
         G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 100)
     with pytest.raises(G.GemmError):
