@@ -618,6 +618,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     kp.err = dev->err;
     kp.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
     kp.debug_skip_first_load = g_opt_skip_first_load.load() != 0 ? 1 : 0;
+    kp.pdl = njobs > 0 ? 1 : 0;  // directly behind the repack launch
 
     if (pl.sk_iters > 0) {
         uint8_t* sk_base = ws + pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes;

@@ -14,6 +14,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace gtn {
 
@@ -57,6 +58,9 @@ struct RepackJobs {
 
 __global__ void __launch_bounds__(256, 4) repack_rows_kernel(const RepackJobs jobs) {
     constexpr int32_t kSpan = 32 * kRepackGroups;  // groups of one work item
+    // The GEMM that reads these copies may start its set-up now; it waits for this
+    // grid's completion before its first load.
+    griddep_launch_dependents();
     const int64_t items_total = jobs.first_item[kMaxRepackJobs];
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;

@@ -64,6 +64,10 @@ struct KParams {
     uint32_t* err;
     uint64_t timeout_ns;
     int32_t debug_skip_first_load;  // test hook: CTA 0 never issues its first load
+    // 1: launched as a programmatic dependent of the kernel before it (the operand
+    // repack), whose output the producer waits for before its first load; everything
+    // up to that point (barriers, tensor memory, tensor maps) overlaps that kernel.
+    int32_t pdl;
 };
 
 }  // namespace gtn

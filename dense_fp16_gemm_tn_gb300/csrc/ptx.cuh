@@ -158,6 +158,12 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed and their memory is visible (returns at once without such a grid) ...
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// ... and, in the earlier grid, allow the dependent grid to be scheduled.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
 // ------------------------------------------------------------------ tcgen05
 
 template <int CG>

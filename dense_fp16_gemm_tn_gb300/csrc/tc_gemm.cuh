@@ -311,6 +311,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            if (p.pdl) griddep_wait();  // the repacked operands are complete and visible
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;

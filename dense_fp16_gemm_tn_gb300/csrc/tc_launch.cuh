@@ -69,18 +69,27 @@ struct TcLauncher {
         grid = (grid / PAIR) * PAIR;
         if (grid < PAIR) grid = PAIR;
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
+        unsigned na = 0;
         cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
         cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
         cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
         cfg.stream = stream;
         if constexpr (PAIR == 2) {
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = 2;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
+            attr[na].id = cudaLaunchAttributeClusterDimension;
+            attr[na].val.clusterDim.x = 2;
+            attr[na].val.clusterDim.y = 1;
+            attr[na].val.clusterDim.z = 1;
+            ++na;
+        }
+        if (p.pdl) {
+            attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[na].val.programmaticStreamSerializationAllowed = 1;
+            ++na;
+        }
+        if (na > 0) {
             cfg.attrs = attr;
-            cfg.numAttrs = 1;
+            cfg.numAttrs = na;
         }
         if (grid_out) *grid_out = grid;
         return cudaLaunchKernelEx(&cfg, gemm_tn_tc_kernel<BN, PAIR, STAGES, EPI, SK>, tmA, tmB, tmC, tmD, p);
