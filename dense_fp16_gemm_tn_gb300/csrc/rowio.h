@@ -120,15 +120,9 @@ GTN_ROWIO void align_cover64(const uint32_t (&v)[36], uint32_t sh, uint32_t (&w)
     for (int i = 0; i < 32; ++i) w[i] = odd ? join_halves(u[i], u[i + 1]) : u[i];
 }
 
-// Writes the first `valid` (0..64) of the 64 halves in o (32 words, low half first) to
-// dst: the mirror of align_cover64 places them in the covering words; whole words go out
-// as 16-byte stores, the two edge words in aligned pieces (store_part16).
-GTN_ROWIO void store_row64(uint16_t* dst, int valid, const uint32_t (&o)[32]) {
-    if (valid <= 0) return;
-    const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
-    const uintptr_t base = a & ~uintptr_t(15);
-    const uint32_t sh = static_cast<uint32_t>(a - base) >> 1;
-    const uintptr_t end = a + 2u * static_cast<uint32_t>(valid);
+// The mirror of align_cover64: the 64 halves in o (32 words, low half first) placed at
+// an offset of `sh` (0..7) halves into nine 16-byte words z (zero elsewhere).
+GTN_ROWIO void place_row64(uint32_t sh, const uint32_t (&o)[32], uint32_t (&z)[36]) {
     const bool by2 = (sh & 4u) != 0, by1 = (sh & 2u) != 0, odd = (sh & 1u) != 0;
     uint32_t op[33];  // one half to the right when sh is odd
 #pragma unroll
@@ -139,9 +133,20 @@ GTN_ROWIO void store_row64(uint16_t* dst, int valid, const uint32_t (&o)[32]) {
     uint32_t t[34];
 #pragma unroll
     for (int i = 0; i < 34; ++i) t[i] = by1 ? (i >= 1 ? op[i - 1] : 0u) : (i < 33 ? op[i] : 0u);
-    uint32_t z[36];
 #pragma unroll
     for (int i = 0; i < 36; ++i) z[i] = by2 ? (i >= 2 ? t[i - 2] : 0u) : (i < 34 ? t[i] : 0u);
+}
+
+// Writes the first `valid` (0..64) of the 64 halves in o (32 words, low half first) to
+// dst: place_row64 puts them in the covering words; whole words go out as 16-byte
+// stores, the two edge words in aligned pieces (store_part16).
+GTN_ROWIO void store_row64(uint16_t* dst, int valid, const uint32_t (&o)[32]) {
+    if (valid <= 0) return;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
+    const uintptr_t base = a & ~uintptr_t(15);
+    const uintptr_t end = a + 2u * static_cast<uint32_t>(valid);
+    uint32_t z[36];
+    place_row64(static_cast<uint32_t>(a - base) >> 1, o, z);
 #pragma unroll
     for (int q = 0; q < 9; ++q) {
         const uintptr_t wa = base + 16u * q;

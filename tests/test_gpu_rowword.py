@@ -21,6 +21,8 @@ CASES = [
     ("ragged_n", 200, 1000, 96, 1, 1001, 1003, 0.5, {}),
     ("narrow_n", 640, 40, 64, 1, 41, 45, 2.0, {}),
     ("batched", 130, 300, 128, 3, 303, 305, 0.75, {}),
+    ("batched_stride8", 128, 600, 136, 3, 601, 605, -0.5, {}),
+    ("many_tiles_odd_ld", 1100, 1800, 320, 1, 1801, 1803, 1.5, {}),
     ("stream_k", 700, 700, 1024, 1, 701, 703, 1.0, {"stream_k": 1}),
     ("pair", 768, 768, 1024, 1, 769, 771, -0.5, {"force_pair": 2, "force_bn": 256}),
     ("pair_stream_k", 520, 776, 2048, 1, 777, 779, 1.25, {"force_pair": 2, "force_bn": 256, "stream_k": 1}),
