@@ -557,26 +557,29 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             };
 
             // Sum of all contributors' partials for this thread's row, columns
-            // [col, col + NC), added in contributor order (deterministic).  Two
-            // contributors' loads are in flight at a time.
+            // [col, col + NC), added in contributor order (deterministic).  The loads of
+            // IN contributors are in flight at a time: four for narrow tiles (all of a
+            // skinny GEMM's contributors in one round trip), else two.
             auto sum_parts = [&](int col, auto& v) {
                 constexpr int NC = sizeof(v) / sizeof(v[0]);
+                constexpr int IN = NC <= 16 ? 4 : 2;
                 float acc_f[NC];
 #pragma unroll
                 for (int q = 0; q < NC; ++q) acc_f[q] = 0.0f;
-                for (int j = 0; j < w.sk_n; j += 2) {
-                    const float* s0 = slot_block(j) + col * 32;
-                    const float* s1 = slot_block(j + 1 < w.sk_n ? j + 1 : j) + col * 32;
-                    float a[NC], b[NC];
+                for (int j = 0; j < w.sk_n; j += IN) {
+                    float a[IN][NC];
 #pragma unroll
-                    for (int q = 0; q < NC; ++q) a[q] = __ldcg(s0 + q * 32);
+                    for (int u = 0; u < IN; ++u) {
+                        const float* s = slot_block(j + u < w.sk_n ? j + u : j) + col * 32;
 #pragma unroll
-                    for (int q = 0; q < NC; ++q) b[q] = __ldcg(s1 + q * 32);
+                        for (int q = 0; q < NC; ++q) a[u][q] = __ldcg(s + q * 32);
+                    }
 #pragma unroll
-                    for (int q = 0; q < NC; ++q) acc_f[q] += a[q];
-                    if (j + 1 < w.sk_n) {
+                    for (int u = 0; u < IN; ++u) {
+                        if (j + u < w.sk_n) {
 #pragma unroll
-                        for (int q = 0; q < NC; ++q) acc_f[q] += b[q];
+                            for (int q = 0; q < NC; ++q) acc_f[q] += a[u][q];
+                        }
                     }
                 }
 #pragma unroll
