@@ -250,7 +250,8 @@ typedef struct {
     int32_t kernel;          /* 0 none (empty problem), 1 scale-only (K == 0),
                                 2 tensor-core tile kernel, 3 split-K (+ reduction) */
     int32_t tile_m;          /* output rows per tile as seen by the tensor core (128 or 256) */
-    int32_t tile_n;          /* output columns per tile as seen by the tensor core */
+    int32_t tile_n;          /* output columns per tile as seen by the tensor core (16..256, or 512:
+                                two N=256 MMAs side by side on a CTA pair) */
     int32_t cta_pair;        /* 1: one CTA per tile; 2: CTA pair sharing one 256-row tile */
     int32_t swap_ab;         /* 1: computes D^T = B . A^T (small M) */
     int32_t splits;          /* K slices (1 = no split) */
