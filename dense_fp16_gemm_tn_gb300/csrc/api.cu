@@ -12,6 +12,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -276,6 +277,7 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
     // 384x4096x4096 38.5 against 32.8 us.  Forced on, stream-K applies whenever the
     // tiles do not divide evenly.
     const int64_t mode = g_opt_stream_k.load();
+    int64_t sk_groups = 0;  // CTA groups of a stream-K launch
     if (mode >= 0 && sk_epi && pub.splits == 1 && kb >= 8 && tiles % G != 0) {
         // k-blocks a group would idle through in the last data-parallel wave
         const double saved_kb = static_cast<double>(ceil_div(tiles, G) * G - tiles) / static_cast<double>(G) *
@@ -284,6 +286,12 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
         // then consecutive groups); with no whole wave, launch fewer groups instead.
         int64_t Gs = G;
         if (tiles < G) Gs = std::min(G, tiles * kb);
+        // Long K on a few tiles (operand layouts without a split-K variant): data-parallel
+        // would leave most of the GPU idle for a long time, so split anyway, over at most
+        // 16 groups per tile (the fix-up reads every contributor's partial in turn; 26
+        // per tile measured slower, 256 x 384 x 131072: 100 against 65 us).
+        const bool long_k = mode == 0 && kb >= 128 && tiles * 4 <= G;
+        if (long_k) Gs = std::min<int64_t>(Gs, tiles * 16);
         const int64_t dp = (tiles / Gs) * Gs;
         const int64_t sk = tiles - dp;
         const int64_t I = sk * kb;
@@ -293,8 +301,9 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
             int64_t maxc = 1;
             for (int64_t t = 0; t < sk; ++t) maxc = std::max(maxc, owner((t + 1) * kb - 1) - owner(t * kb) + 1);
             const bool narrow = pub.tile_n <= 32;
-            const bool pays = narrow || (pub.tile_n <= 256 && maxc <= 8 && saved_kb >= 36.0 &&
-                                         (kb >= 128 || (kb >= 64 && tiles >= 3 * G)));
+            const bool pays = narrow || long_k ||
+                              (pub.tile_n <= 256 && maxc <= 8 && saved_kb >= 36.0 &&
+                               (kb >= 128 || (kb >= 64 && tiles >= 3 * G)));
             if (mode > 0 || pays) {
                 pub.stream_k = 1;
                 pub.sk_maxc = static_cast<int32_t>(maxc);
@@ -303,12 +312,13 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
                 pl.sk_iters = I;
                 pl.sk_w_bytes = round_up(sk * maxc * pair * 128 * static_cast<int64_t>(pub.tile_n) * 4, 256);
                 pl.sk_ctr_bytes = round_up(sk * pair * 4 * 8, 256);
+                sk_groups = Gs;
             }
         }
     }
     find_tc_variant(pl.var.bn, pl.var.pair, pl.epi, pub.stream_k, &pl.var);
     pub.units = pub.stream_k ? pub.dp_tiles : tiles * pub.splits;
-    pub.grid = pub.stream_k ? std::min<int64_t>(G, tiles * kb) * pair : std::min<int64_t>(pub.units, G) * pair;
+    pub.grid = pub.stream_k ? sk_groups * pair : std::min<int64_t>(pub.units, G) * pair;
     pub.workspace_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes;
 }
 
@@ -377,14 +387,26 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     const int64_t rows_b = swap ? pr.M : pr.N;
     const int64_t kb = ceil_div(pr.K, 64);
 
-    // Split-K with a separate reduction only when forced (the default for too
-    // few tiles is the stream-K split decided in plan_stream_k).
+    // Split-K with a separate reduction: when forced, and for long K on tiles that would
+    // leave at least three quarters of the SMs idle.  There the K slices fill the GPU and
+    // the reduction kernel reads the fp32 partials with every SM; the stream-K fix-up,
+    // one CTA per tile reading its contributors one after another, measured slower
+    // (256 x 384 x 131072: 65 us stream-K, 75 with 8 slices, 472 data-parallel).  Other
+    // shapes with too few tiles take the stream-K split decided in plan_stream_k.
     int splits = 1;
     const int64_t fsplit = g_opt_force_splits.load();
-    if (fsplit >= 1 && !pr.a_mn && !pr.b_mn && !pr.acc16) {
+    const bool split_ok = !pr.a_mn && !pr.b_mn && !pr.acc16;
+    if (fsplit >= 1 && split_ok) {
         pair = 1;
         splits = static_cast<int>(std::min<int64_t>(fsplit, kb));
         if (!swap) bn = 128;  // the partial-sum variant exists at 128 columns
+    } else if (fsplit == 0 && split_ok && !swap && g_opt_stream_k.load() == 0) {
+        const int64_t t128 = ceil_div(pr.M, 128) * ceil_div(pr.N, 128) * pr.batch;
+        if (kb >= 128 && t128 * 4 <= slots) {
+            pair = 1;
+            bn = 128;
+            splits = static_cast<int>(std::min<int64_t>({32, kb / 8, std::max<int64_t>(2, slots / t128)}));
+        }
     }
 
     // D rows TMA cannot address are written by the epilogue itself, each thread its row,

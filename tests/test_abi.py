@@ -191,6 +191,25 @@ def test_plan_automatic_stream_k_only_where_it_was_measured_to_pay():
         assert plan(M, N, K, sms=152)["stream_k"] == 0, (M, N, K)
 
 
+def test_plan_long_k_on_few_tiles_splits_k_to_fill_the_gpu():
+    # K slices so that tiles x slices ~ the SM count (2..32, >= 8 k-blocks each), reduced
+    # by the separate kernel
+    for M, N, K, splits in ((256, 384, 131072, 25), (128, 128, 262144, 32), (512, 512, 65536, 9),
+                            (256, 256, 8192, 16)):
+        p = plan(M, N, K, sms=152)
+        assert p["kernel"] == 3 and p["splits"] == splits and p["tile_n"] == 128 and p["cta_pair"] == 1, (M, N, K)
+        assert p["workspace_bytes"] >= splits * M * N * 4
+    # not for short K, many tiles, swapped skinny problems, or a forced stream-K choice
+    for M, N, K in ((256, 256, 4096), (1024, 1024, 32768), (16, 8192, 8192), (4096, 4096, 4096)):
+        assert plan(M, N, K, sms=152)["splits"] == 1, (M, N, K)
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 1)
+    try:
+        p = plan(256, 384, 131072, sms=152)
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 0)
+    assert p["splits"] == 1 and p["stream_k"] == 1
+
+
 def test_plan_forced_splits_use_the_reduction_kernel():
     G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_SPLITS, 4)
     try:
