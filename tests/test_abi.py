@@ -199,6 +199,10 @@ def test_plan_long_k_on_few_tiles_splits_k_to_fill_the_gpu():
         p = plan(M, N, K, sms=152)
         assert p["kernel"] == 3 and p["splits"] == splits and p["tile_n"] == 128 and p["cta_pair"] == 1, (M, N, K)
         assert p["workspace_bytes"] >= splits * M * N * 4
+    # swapped small-M problems with room for 3+ slices per tile: slices too
+    for M, N, K, splits in ((48, 1024, 32768, 19), (64, 512, 131072, 32), (16, 1024, 65536, 19)):
+        p = plan(M, N, K, sms=152)
+        assert p["kernel"] == 3 and p["swap_ab"] == 1 and p["splits"] == splits, (M, N, K)
     # not for short K, many tiles, swapped skinny problems, or a forced stream-K choice
     for M, N, K in ((256, 256, 4096), (1024, 1024, 32768), (16, 8192, 8192), (4096, 4096, 4096)):
         assert plan(M, N, K, sms=152)["splits"] == 1, (M, N, K)

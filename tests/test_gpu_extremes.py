@@ -1,7 +1,8 @@
 """Shapes at the edges of the tile scheduler, against the oracle: a very long K (2048
 k-blocks per tile; small-integer inputs keep every fp32 sum exact, so the result must
-match bit for bit), many batch entries of tiny matrices, tall matrices with a handful of
-columns, and K shorter than one k-block on many tiles."""
+match bit for bit) on the automatic K-slice plan, stream-K and fixed slices, swapped
+small-M problems with long K, many batch entries of tiny matrices, tall matrices with a
+handful of columns, and K shorter than one k-block on many tiles."""
 import numpy as np
 import pytest
 
@@ -46,3 +47,24 @@ def test_tall_matrix_with_few_columns():
 def test_k_shorter_than_one_block_on_many_tiles():
     run_problem(1500, 1800, 8, alpha=2.0, beta=0.5, seed=24)
     run_problem(1024, 1032, 24, seed=25, dist="int", compare="exact")
+
+
+def test_swapped_long_k_slices():
+    """Small M with long K: swapped operands, K slices (the plan's automatic choice)."""
+    t = torch()
+    M, N, K = 48, 1024, 32768
+    plan = G.gemm_tn_f16_plan(M, N, K, 1, K, K, N, N, 0, 0, 0, 0, 0.0, 15, 152)
+    assert plan["swap_ab"] == 1 and plan["splits"] > 1
+    A = inputs.small_int_half(6, M, K)
+    B = inputs.small_int_half(7, N, K)
+    D = t.empty(M * N, dtype=t.float16, device="cuda")
+    G.gemm_tn_f16(to_dev(A), K, to_dev(B), K, None, N, D, N, M, N, K, 1.0, 0.0)
+    t.cuda.synchronize()
+    assert_device_ok()
+    got = to_host(D).reshape(M, N)
+    rng = np.random.default_rng(8)
+    m = rng.integers(0, M, 2000)
+    n = rng.integers(0, N, 2000)
+    ref = oracle.gemm_tn_entries(A, B, None, K, 1.0, 0.0, np.zeros_like(m), m, n, lda=K, ldb=K)
+    assert np.array_equal(got[m, n], ref)
+    run_problem(24, 1500, 16384, alpha=0.5, beta=1.5, seed=26)
