@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(256, 4) repack_rows_kernel(const RepackJobs jo
 __global__ void splitk_reduce_kernel(const float* __restrict__ W, int32_t splits, int64_t M, int64_t N,
                                      int64_t batch, float alpha, float beta, const __half* C, int64_t ldc,
                                      int64_t strideC, __half* D, int64_t ldd, int64_t strideD) {
+    griddep_wait();  // launched as a dependent of the GEMM that writes W: its partials are visible
     const int64_t mn = M * N;
     const int64_t total = batch * mn;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -199,10 +200,19 @@ cudaError_t launch_repack(const RepackArgs* ops, int count, int sms, cudaStream_
 cudaError_t launch_splitk_reduce(const float* W, int32_t splits, int64_t M, int64_t N, int64_t batch, float alpha,
                                  float beta, const void* C, int64_t ldc, int64_t strideC, void* D, int64_t ldd,
                                  int64_t strideD, int sms, cudaStream_t stream) {
-    splitk_reduce_kernel<<<grid_for(batch * M * N, 256, sms), 256, 0, stream>>>(
-        W, splits, M, N, batch, alpha, beta, static_cast<const __half*>(C), ldc, strideC, static_cast<__half*>(D),
-        ldd, strideD);
-    return cudaGetLastError();
+    // A programmatic dependent of the GEMM before it on the stream: scheduled while that
+    // GEMM runs, it waits for the GEMM's completion before reading the partials.
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_for(batch * M * N, 256, sms)), 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, W, splits, M, N, batch, alpha, beta,
+                              static_cast<const __half*>(C), ldc, strideC, static_cast<__half*>(D), ldd, strideD);
 }
 
 cudaError_t launch_scale(int64_t M, int64_t N, int64_t batch, float beta, const void* C, int64_t ldc,

@@ -279,6 +279,9 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = (PAIR == 2) ? cluster_cta_rank() : 0u;
+    // A kernel launched as this one's programmatic dependent (the split-K reduction) may
+    // be scheduled now; it waits for this grid's completion before it reads anything.
+    griddep_launch_dependents();
     const int64_t group = blockIdx.x / PAIR;
     const int64_t ngroups = gridDim.x / PAIR;
 
