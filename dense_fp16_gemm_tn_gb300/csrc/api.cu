@@ -191,6 +191,21 @@ bool encode_map_uncached(CUtensorMap* map, const void* base, int64_t inner, int6
     return r == CUDA_SUCCESS;
 }
 
+// fp32 split-K partials W[slice][M][N] (slices = batch x splits) for TMA stores: boxes of
+// 32 rows x 32 columns (128 bytes) with 128-byte swizzle.  Needs N % 4 == 0.
+bool encode_partials_map(CUtensorMap* map, const float* W, int64_t M, int64_t N, int64_t slices) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn || N % 4 != 0) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(slices)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(N) * 4u, static_cast<cuuint64_t>(M * N) * 4u};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(W), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------------ problem + plan
 
 struct Problem {
@@ -387,11 +402,13 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     const int64_t rows_b = swap ? pr.M : pr.N;
     const int64_t kb = ceil_div(pr.K, 64);
 
-    // Split-K with a separate reduction: when forced, and for long K on tiles that would
-    // leave at least three quarters of the SMs idle.  There the K slices fill the GPU and
-    // the reduction kernel reads the fp32 partials with every SM; the stream-K fix-up,
-    // one CTA per tile reading its contributors one after another, measured slower
-    // (256 x 384 x 131072: 65 us stream-K, 75 with 8 slices, 472 data-parallel).  Other
+    // Split-K with a separate reduction: when forced, and for K of 32 or more k-blocks on
+    // tiles that would leave at least three quarters of the SMs idle.  There the K slices
+    // fill the GPU (their fp32 partials leave by TMA) and the reduction kernel reads them
+    // with every SM; the stream-K fix-up, one CTA per tile reading its contributors one
+    // after another, measured slower (256 x 384 x 131072: 65 us stream-K, 75 with 8
+    // slices, 472 data-parallel), and so did data-parallel tiles from 32 k-blocks on
+    // (256 x 256 x 4096 22.1 against 14.0 us, 512 x 512 x 2048 15.9 against 14.5).  Other
     // shapes with too few tiles take the stream-K split decided in plan_stream_k.
     int splits = 1;
     const int64_t fsplit = g_opt_force_splits.load();
@@ -400,7 +417,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
         pair = 1;
         splits = static_cast<int>(std::min<int64_t>(fsplit, kb));
         if (!swap) bn = 128;  // the partial-sum variant exists at 128 columns
-    } else if (fsplit == 0 && split_ok && g_opt_stream_k.load() == 0 && kb >= 128) {
+    } else if (fsplit == 0 && split_ok && g_opt_stream_k.load() == 0 && kb >= 32) {
         if (!swap) {
             const int64_t t128 = ceil_div(pr.M, 128) * ceil_div(pr.N, 128) * pr.batch;
             if (t128 * 4 <= slots) {
@@ -414,7 +431,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
             // 27.9 against 40.8 us; 64 x 512 x 131072 39.4 against 59.3; 32 x 2048 x 32768
             // 36.6 against 40.3); with two (16 x 8192 x 8192) the two tie, and stream-K stays.
             const int64_t tsw = ceil_div(pr.N, 128) * pr.batch;
-            if (tsw * 3 <= slots)
+            if (kb >= 128 && tsw * 3 <= slots)
                 splits = static_cast<int>(std::min<int64_t>({32, kb / 8, slots / tsw}));
         }
     }
@@ -651,6 +668,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     kp.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
     kp.debug_skip_first_load = g_opt_skip_first_load.load() != 0 ? 1 : 0;
     kp.pdl = njobs > 0 ? 1 : 0;  // directly behind the repack launch
+    if (pl.epi == EPI_PARTIAL && encode_partials_map(&mapD, kp.W, p.M, p.N, p.batch * pl.pub.splits)) kp.w_tma = 1;
 
     if (pl.sk_iters > 0) {
         uint8_t* sk_base = ws + pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes;

@@ -127,6 +127,49 @@ __global__ void __launch_bounds__(256, 4) repack_rows_kernel(const RepackJobs jo
     }
 }
 
+// D[b][m][n] = alpha * sum_{s<S} W[b][s][m][n] + beta * C[b][m][n], four consecutive n per
+// thread (N % 4 == 0): 16-byte loads of the partials, up to eight slices' loads in flight,
+// added in slice order.
+__global__ void splitk_reduce4_kernel(const float* __restrict__ W, int32_t splits, int64_t M, int64_t N,
+                                      int64_t batch, float alpha, float beta, const __half* C, int64_t ldc,
+                                      int64_t strideC, __half* D, int64_t ldd, int64_t strideD) {
+    griddep_wait();  // launched as a dependent of the GEMM that writes W: its partials are visible
+    const int64_t mn = M * N;
+    const int64_t total = batch * mn / 4;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t e4 = i * 4;
+        const int64_t b = e4 / mn;
+        const int64_t e = e4 - b * mn;
+        const int64_t m = e / N;
+        const int64_t n = e - m * N;
+        const float4* w = reinterpret_cast<const float4*>(W + b * splits * mn + e);
+        const int64_t step = mn / 4;
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int32_t s0 = 0; s0 < splits; s0 += 8) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (s0 + u < splits) v[u] = __ldcs(w + (s0 + u) * step);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                if (s0 + u < splits) {
+                    acc[0] += v[u].x;
+                    acc[1] += v[u].y;
+                    acc[2] += v[u].z;
+                    acc[3] += v[u].w;
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float x = alpha * acc[q];
+            if (beta != 0.0f) x = fmaf(beta, __half2float(C[b * strideC + m * ldc + n + q]), x);
+            D[b * strideD + m * ldd + n + q] = __float2half_rn(x);
+        }
+    }
+}
+
 // D[b][m][n] = alpha * sum_{s<S} W[b][s][m][n] + beta * C[b][m][n]
 __global__ void splitk_reduce_kernel(const float* __restrict__ W, int32_t splits, int64_t M, int64_t N,
                                      int64_t batch, float alpha, float beta, const __half* C, int64_t ldc,
@@ -206,11 +249,16 @@ cudaError_t launch_splitk_reduce(const float* W, int32_t splits, int64_t M, int6
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(grid_for(batch * M * N, 256, sms)), 1, 1);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (N % 4 == 0) {
+        cfg.gridDim = dim3(static_cast<unsigned>(grid_for(batch * M * N / 4, 256, sms)), 1, 1);
+        return cudaLaunchKernelEx(&cfg, splitk_reduce4_kernel, W, splits, M, N, batch, alpha, beta,
+                                  static_cast<const __half*>(C), ldc, strideC, static_cast<__half*>(D), ldd, strideD);
+    }
+    cfg.gridDim = dim3(static_cast<unsigned>(grid_for(batch * M * N, 256, sms)), 1, 1);
     return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, W, splits, M, N, batch, alpha, beta,
                               static_cast<const __half*>(C), ldc, strideC, static_cast<__half*>(D), ldd, strideD);
 }

@@ -68,6 +68,9 @@ struct KParams {
     // repack), whose output the producer waits for before its first load; everything
     // up to that point (barriers, tensor memory, tensor maps) overlaps that kernel.
     int32_t pdl;
+    // EPI_PARTIAL: 1 when the tmD slot holds a tensor map of W (fp32, [batch * splits][M][N],
+    // boxes of 32 rows x 32 columns, 128-byte swizzle), so partials are stored by TMA.
+    int32_t w_tma;
 };
 
 }  // namespace gtn

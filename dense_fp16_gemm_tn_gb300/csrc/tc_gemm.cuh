@@ -88,7 +88,8 @@ struct TileCfg {
                                    : (2 * BN <= 256) ? 256 : 512;
     static constexpr int EPI_WARP_BYTES =
         (epi_base(EPI) == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) ? 2 * 32 * 128
-        : (epi_base(EPI) == EPI_GENERIC || EPI == EPI_PARTIAL) ? 32 * 33 * 4 : 0;
+        : (EPI == EPI_PARTIAL) ? 2 * 32 * 128  // TMA staging (or the padded transpose, 32 x 33 x 4)
+        : (epi_base(EPI) == EPI_GENERIC) ? 32 * 33 * 4 : 0;
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
@@ -302,7 +303,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
-        if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) prefetch_tensormap(&tmD);
+        if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG || EPI == EPI_PARTIAL)
+            prefetch_tensormap(&tmD);
         if constexpr (EPI == EPI_TMA_C) prefetch_tensormap(&tmC);
     }
     if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
@@ -792,6 +794,41 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         }
                     }
                 } else if constexpr (EB == EPI_GENERIC || EB == EPI_PARTIAL) {
+                    bool stored = false;
+                    if constexpr (EB == EPI_PARTIAL) {
+                        if (p.w_tma) {
+                            // fp32 partials by TMA: 32 columns (128 bytes) of this thread's row
+                            // into the swizzled staging buffer, one 32 x 32 box per chunk.
+#pragma unroll 1
+                            for (int c = 0; c < BN / 32; ++c) {
+                                uint32_t v[32];
+                                if constexpr (!PARTS) {
+                                    acc_ld32(c * 32, v);
+                                } else {
+                                    sum_parts(c * 32, v);
+                                }
+                                const uint32_t buf = chunk_count & 1u;
+                                if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+                                __syncwarp();
+                                const uint32_t sb = smem_u32(ebuf) + buf * 4096u;
+                                const uint32_t row_addr = sb + lane * 128u;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), v[4 * j],
+                                                 v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                                fence_proxy_async_smem();
+                                __syncwarp();
+                                if (lane == 0) {
+                                    tma_store_3d(&tmD, sb, static_cast<int32_t>(acol0 + c * 32),
+                                                 static_cast<int32_t>(arow0), w.b * p.splits + w.split);
+                                    bulk_commit_group();
+                                }
+                                ++chunk_count;
+                            }
+                            stored = true;
+                        }
+                    }
+                    if (stored) return;
                     // Transpose each 32x32 block through padded shared memory so that a warp
                     // reads C and writes D along rows (coalesced), whatever the alignment.
                     float* T = reinterpret_cast<float*>(ebuf);
@@ -947,7 +984,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             }
         }
-        if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) {
+        if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG || EPI == EPI_PARTIAL) {
             if (lane == 0) bulk_wait_group<0>();
             __syncwarp();
         }
