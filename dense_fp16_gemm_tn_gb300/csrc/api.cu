@@ -388,7 +388,12 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
             pair = 2;
             bn = 256;
         } else if (t_256 >= slots || pr.N > 128 * 8) {
-            pair = 1;
+            // Under a wave of pair tiles, pairs and single CTAs with 128 x 256 tiles keep the
+            // same SMs busy, and a pair loads 32 KB per SM and k-block where a single CTA
+            // loads 48 KB for the same output: from 64 k-blocks on the pairs measured faster
+            // (2048^2 x 8192 46.6 against 57.9 us, 1536^2 x 4096 28.8 against 33.0,
+            // 1024 x 4096 x 4096 28.9 against 32.9), at 32 k-blocks even, at 16 slower.
+            pair = pr.K >= 64 * 64 ? 2 : 1;
             bn = 256;
         } else {
             pair = 1;
