@@ -431,12 +431,13 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
                 splits = static_cast<int>(std::min<int64_t>({32, kb / 8, std::max<int64_t>(2, slots / t128)}));
             }
         } else {
-            // swapped (small M): 128-row tiles along N.  With room for three or more slices
-            // per tile in one wave, slices measured faster than stream-K (48 x 1024 x 32768
-            // 27.9 against 40.8 us; 64 x 512 x 131072 39.4 against 59.3; 32 x 2048 x 32768
-            // 36.6 against 40.3); with two (16 x 8192 x 8192) the two tie, and stream-K stays.
+            // swapped (small M): 128-row tiles along N.  With room for two or more slices per
+            // tile in one wave and 64+ k-blocks, slices measured faster than stream-K or whole
+            // tiles (48 x 1024 x 32768 27.9 against 40.8 us; 64 x 512 x 131072 39.4 against
+            // 59.3; 64 x 8192 x 8192 33.7 against 40.3; 64 x 4096 x 4096 18.5 against 26.6;
+            // 32 x 8192 x 4096 24.3 against 26.8), or tied (16 x 8192 x 8192 34.6 against 34.7).
             const int64_t tsw = ceil_div(pr.N, 128) * pr.batch;
-            if (kb >= 128 && tsw * 3 <= slots)
+            if (kb >= 64 && tsw * 2 <= slots)
                 splits = static_cast<int>(std::min<int64_t>({32, kb / 8, slots / tsw}));
         }
     }

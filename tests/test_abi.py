@@ -158,12 +158,22 @@ def test_plan_forced_stream_k_splits_the_partial_wave():
         G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 0)
 
 
-def test_plan_skinny_m_swaps_and_streams_k():
+def test_plan_skinny_m_swaps_and_splits_k():
+    # 64 swapped tiles of 128 rows: two K slices fill the SMs
     p = plan(16, 8192, 8192)
-    assert p["kernel"] == 2 and p["swap_ab"] == 1 and p["tile_n"] == 16 and p["splits"] == 1
-    assert p["stream_k"] == 1 and p["dp_tiles"] == 0 and p["sk_tiles"] == 64 and p["grid"] == 148
-    assert 2 <= p["sk_maxc"] <= 4
-    assert p["workspace_bytes"] >= 64 * p["sk_maxc"] * 128 * 16 * 4
+    assert p["kernel"] == 3 and p["swap_ab"] == 1 and p["tile_n"] == 16 and p["splits"] == 2
+    assert p["workspace_bytes"] >= 2 * 16 * 8192 * 4
+    # stream-K when no whole slices fit (128 tiles), and when asked for
+    q = plan(16, 16384, 8192, sms=152)
+    assert q["kernel"] == 2 and q["swap_ab"] == 1 and q["splits"] == 1 and q["stream_k"] == 1
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 1)
+    try:
+        r = plan(16, 8192, 8192)
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 0)
+    assert r["kernel"] == 2 and r["splits"] == 1 and r["stream_k"] == 1 and r["dp_tiles"] == 0
+    assert r["sk_tiles"] == 64 and r["grid"] == 148 and 2 <= r["sk_maxc"] <= 4
+    assert r["workspace_bytes"] >= 64 * r["sk_maxc"] * 128 * 16 * 4
 
 
 def test_plan_stream_k_needs_one_iteration_per_group():
@@ -179,7 +189,7 @@ def test_plan_stream_k_needs_one_iteration_per_group():
 
 def test_plan_automatic_stream_k_only_where_it_was_measured_to_pay():
     # long K or narrow swapped tiles: split the partial wave
-    for M, N, K in ((4096, 4096, 4096), (4096, 4096, 8192), (2560, 2560, 8192), (128, 8192, 8192), (16, 8192, 8192),
+    for M, N, K in ((4096, 4096, 4096), (4096, 4096, 8192), (2560, 2560, 8192), (128, 8192, 8192), (16, 16384, 8192),
                     (5120, 5120, 4096)):
         assert plan(M, N, K, sms=152)["stream_k"] == 1, (M, N, K)
     # 256 x 512 tiles: their 256 KB-per-CTA partials did not pay back (8192^3 603-612 against
@@ -204,7 +214,7 @@ def test_plan_long_k_on_few_tiles_splits_k_to_fill_the_gpu():
         p = plan(M, N, K, sms=152)
         assert p["kernel"] == 3 and p["swap_ab"] == 1 and p["splits"] == splits, (M, N, K)
     # not for short K, many tiles, swapped skinny problems, or a forced stream-K choice
-    for M, N, K in ((256, 256, 1024), (1024, 1024, 4096), (1024, 1024, 32768), (16, 8192, 8192), (4096, 4096, 4096)):
+    for M, N, K in ((256, 256, 1024), (1024, 1024, 4096), (1024, 1024, 32768), (16, 16384, 8192), (4096, 4096, 4096)):
         assert plan(M, N, K, sms=152)["splits"] == 1, (M, N, K)
     G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 1)
     try:
