@@ -425,7 +425,12 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     } else if (fsplit == 0 && split_ok && g_opt_stream_k.load() == 0 && kb >= 32) {
         if (!swap) {
             const int64_t t128 = ceil_div(pr.M, 128) * ceil_div(pr.N, 128) * pr.batch;
-            if (t128 * 4 <= slots) {
+            // Up to half the SMs busy and 128-255 k-blocks: two slices measured faster too
+            // (768 x 1280 x 8192 30.2 against 44.5 us, 1024^2 x 8192 30.7 against 33.9,
+            // 640 x 1024 x 8192 28.7 against 30.2); from 256 k-blocks on it was mixed
+            // (896 x 1024 x 16384 44.7 against 42.6, 1024^2 x 16384 45.1 against 46.6).
+            const bool half = t128 * 2 <= slots && kb >= 128 && kb < 256;
+            if (t128 * 4 <= slots || half) {
                 pair = 1;
                 bn = 128;
                 splits = static_cast<int>(std::min<int64_t>({32, kb / 8, std::max<int64_t>(2, slots / t128)}));

@@ -189,7 +189,7 @@ def test_plan_stream_k_needs_one_iteration_per_group():
 
 def test_plan_automatic_stream_k_only_where_it_was_measured_to_pay():
     # long K or narrow swapped tiles: split the partial wave
-    for M, N, K in ((4096, 4096, 4096), (4096, 4096, 8192), (2560, 2560, 8192), (128, 8192, 8192), (16, 16384, 8192),
+    for M, N, K in ((4096, 4096, 4096), (4096, 4096, 8192), (2560, 2560, 8192), (256, 8192, 8192), (16, 16384, 8192),
                     (5120, 5120, 4096)):
         assert plan(M, N, K, sms=152)["stream_k"] == 1, (M, N, K)
     # 256 x 512 tiles: their 256 KB-per-CTA partials did not pay back (8192^3 603-612 against
@@ -205,7 +205,9 @@ def test_plan_long_k_on_few_tiles_splits_k_to_fill_the_gpu():
     # K slices so that tiles x slices ~ the SM count (2..32, >= 8 k-blocks each), reduced
     # by the separate kernel
     for M, N, K, splits in ((256, 384, 131072, 25), (128, 128, 262144, 32), (512, 512, 65536, 9),
-                            (256, 256, 8192, 16), (256, 256, 4096, 8), (512, 512, 2048, 4), (768, 768, 4096, 4)):
+                            (256, 256, 8192, 16), (256, 256, 4096, 8), (512, 512, 2048, 4), (768, 768, 4096, 4),
+                            # up to half the SMs busy, 128-255 k-blocks
+                            (1024, 1024, 8192, 2), (128, 8192, 8192, 2), (640, 1024, 8192, 3)):
         p = plan(M, N, K, sms=152)
         assert p["kernel"] == 3 and p["splits"] == splits and p["tile_n"] == 128 and p["cta_pair"] == 1, (M, N, K)
         assert p["workspace_bytes"] >= splits * M * N * 4
@@ -214,7 +216,8 @@ def test_plan_long_k_on_few_tiles_splits_k_to_fill_the_gpu():
         p = plan(M, N, K, sms=152)
         assert p["kernel"] == 3 and p["swap_ab"] == 1 and p["splits"] == splits, (M, N, K)
     # not for short K, many tiles, swapped skinny problems, or a forced stream-K choice
-    for M, N, K in ((256, 256, 1024), (1024, 1024, 4096), (1024, 1024, 32768), (16, 16384, 8192), (4096, 4096, 4096)):
+    for M, N, K in ((256, 256, 1024), (1024, 1024, 4096), (1024, 1024, 32768), (896, 1024, 16384), (16, 16384, 8192),
+                    (4096, 4096, 4096)):
         assert plan(M, N, K, sms=152)["splits"] == 1, (M, N, K)
     G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 1)
     try:
