@@ -291,11 +291,13 @@ GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int6
  *   GEMM_TN_OPT_FORCE_BN          force the tile width: 128, 256 or 512 (CTA pairs with a TMA
  *                                 epilogue only; else 256), 0 = automatic.
  *   GEMM_TN_OPT_FORCE_PAIR        force 1 (single CTA) or 2 (CTA pair), 0 = automatic.
- *   GEMM_TN_OPT_FORCE_SPLITS      force the number of K slices, 0 = automatic (K slices reduced
- *                                 by a second kernel when K has 128+ 64-wide blocks and
- *                                 128 x 128 tiles would occupy at most a quarter of the SMs,
- *                                 or, for swapped small-M problems, a third: about SMs /
- *                                 tiles slices, up to 32, at least 8 blocks each).
+ *   GEMM_TN_OPT_FORCE_SPLITS      force the number of K slices, 0 = automatic: K slices, summed
+ *                                 by a second kernel, when 128 x 128 tiles would occupy at
+ *                                 most a quarter of the SMs and K has 32+ 64-wide blocks,
+ *                                 or at most half with 128-255 blocks; for swapped small-M
+ *                                 problems when two or more slices per tile fit and K has
+ *                                 64+ blocks.  About SMs / tiles slices, up to 32, at least 8
+ *                                 blocks each.  Not with GEMM_TN_OPT_STREAM_K != 0.
  *   GEMM_TN_OPT_FORCE_SWAP        force operand swapping off (-1) or on (1), 0 = automatic.
  *   GEMM_TN_OPT_FORCE_GENERIC_EPI 1: never use the TMA-store epilogue.
  *   GEMM_TN_OPT_FORCE_PACK        1: repack A and B through scratch even when aligned.
