@@ -152,7 +152,10 @@ extern "C" GEMM_TN_API gemm_status_t gemm_tn_f16_splitk_static(const void* A, in
     const int64_t kb = cdiv(K, 64);
     int64_t s = splits;
     if (s == 0) {
-        // Same rule as the pooled path: fewest K slices that minimise waves x slice length.
+        // This path's own rule (the pooled entry points plan differently, with stream-K and
+        // data-parallel tiles as alternatives): the fewest K slices, up to 64 of at least four
+        // k-blocks, that minimise waves x (slice length + 2).  With a wave or more of tiles that
+        // is one slice, whose fp32 result still passes through the array and the sum kernel.
         int64_t best = INT64_MAX;
         s = 1;
         const int64_t max_s = kb / 4 < 64 ? (kb / 4 < 1 ? 1 : kb / 4) : 64;

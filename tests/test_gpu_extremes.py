@@ -68,3 +68,13 @@ def test_swapped_long_k_slices():
     ref = oracle.gemm_tn_entries(A, B, None, K, 1.0, 0.0, np.zeros_like(m), m, n, lda=K, ldb=K)
     assert np.array_equal(got[m, n], ref)
     run_problem(24, 1500, 16384, alpha=0.5, beta=1.5, seed=26)
+
+
+@pytest.mark.parametrize("M,N,K,beta", [(640, 1024, 8192, 0.75), (128, 8192, 8192, -1.25)])
+def test_automatic_two_or_three_k_slices_unswapped(M, N, K, beta):
+    """Tiles that fill at most half the SMs with 128-255 k-blocks take a few K slices on
+    the automatic plan (no forced option); the slices and their sum kernel, with C read
+    by the sum, must agree with the oracle element by element."""
+    plan = G.gemm_tn_f16_plan(M, N, K, 1, K, K, N, N, 0, 0, 0, 0, beta, 15, 152)
+    assert plan["swap_ab"] == 0 and plan["splits"] > 1 and plan["stream_k"] == 0
+    run_problem(M, N, K, alpha=0.5, beta=beta, seed=27)

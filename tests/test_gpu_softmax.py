@@ -208,10 +208,10 @@ def test_softmax_degenerate_sizes():
     assert_device_ok()
 
 
-def test_softmax_score_workload_sampled():
+def test_softmax_score_workload_every_row():
     """The batched score workload (8 x 16 heads, Q, K 4096 x 64, N(0,1), alpha 1/8) in one
-    call, 384 sampled rows against the oracle (first and last rows of the first and
-    last heads included)."""
+    call: 384 sampled rows against the oracle first (first and last rows of the first and
+    last heads included), then every one of the 524288 rows."""
     w = inputs.WORKLOADS["score_qk"]
     batch, M, N, d = w.batch, w.M, w.N, w.K
     Q, K, _ = w.make()
@@ -219,4 +219,5 @@ def test_softmax_score_workload_sampled():
     rng = np.random.default_rng(5)
     rows = np.unique(np.concatenate([rng.integers(0, batch * M, 376),
                                      [0, M - 1, M, (batch - 1) * M, batch * M - 128, batch * M - 1]]))
-    check_rows(Q, K, m, l, M, N, d, batch, w.alpha, d, d, M * d, N * d, rows=rows, what="score workload")
+    check_rows(Q, K, m, l, M, N, d, batch, w.alpha, d, d, M * d, N * d, rows=rows, what="score workload (sample)")
+    check_rows(Q, K, m, l, M, N, d, batch, w.alpha, d, d, M * d, N * d, what="score workload (every row)")

@@ -1,14 +1,16 @@
 """The six measured workloads at full size, in the launch configuration the
-bench times (the library's automatic plan), checked against the oracle on
-sampled outputs (computed one by one) plus edge rows/columns, and for
-properties that hold at any size (every output finite)."""
+bench times (the library's automatic plan): every output element against the
+oracle.  A sample of outputs (computed one by one) plus the edge rows and
+columns is checked first, as a quick pre-check, together with a property that
+holds at any size (every output finite); then the whole result is compared with
+the full oracle evaluation, a few batch entries at a time."""
 import numpy as np
 import pytest
 
 import oracle
 from dense_fp16_gemm_tn_gb300 import inputs
 import dense_fp16_gemm_tn_gb300 as G
-from gpu_util import assert_close, assert_device_ok, to_dev, to_host, torch
+from gpu_util import assert_close, assert_close_full, assert_device_ok, to_dev, to_host, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +33,7 @@ def _sample_positions(w, rng, n=3000):
 
 
 @pytest.mark.parametrize("key", list(inputs.WORKLOADS))
-def test_workload_sampled_parity(key):
+def test_workload_full_parity(key):
     t = torch()
     w = inputs.WORKLOADS[key]
     A, B, C = w.make()
@@ -56,3 +58,16 @@ def test_workload_sampled_parity(key):
     ref = oracle.gemm_tn_entries(A, B, C, w.K, w.alpha, w.beta, b, m, n, lda=w.lda_, ldb=w.ldb_, ldc=w.ldc_,
                                  strideA=sA, strideB=sB, strideC=sC)
     assert_close(got, ref, w.K, what=key)
+
+    # every element: the oracle over a few batch entries at a time (bounded host memory)
+    plan = G.gemm_tn_f16_plan(w.M, w.N, w.K, w.batch, w.lda_, w.ldb_, w.ldc_, w.ldd_, sA, sB, sC, sD, w.beta, 15,
+                              t.cuda.get_device_properties(0).multi_processor_count)
+    per = max(1, (1 << 26) // (w.M * w.ldd_))
+    for b0 in range(0, w.batch, per):
+        nb = min(per, w.batch - b0)
+        got_b = to_host(dD[b0 * sD:(b0 + nb) * sD]).reshape(nb, w.M, w.ldd_)[:, :, : w.N]
+        ref_b = oracle.gemm_tn(A[b0:b0 + nb], B[b0:b0 + nb], None if C is None else C[b0:b0 + nb],
+                               w.M, w.N, w.K, w.alpha, w.beta, lda=w.lda_, ldb=w.ldb_, ldc=w.ldc_, ldd=w.ldd_,
+                               batch=nb, strideA=sA, strideB=sB, strideC=sC, strideD=sD)
+        ref_b = ref_b[: nb * sD].reshape(nb, w.M, w.ldd_)[:, :, : w.N]
+        assert_close_full(got_b, ref_b, w.K, what=f"{key} batch entries {b0}..{b0 + nb - 1} (plan {plan})")
