@@ -23,6 +23,9 @@ from ._binding import (  # noqa: F401
     GEMM_TN_OPT_FORCE_PAIR,
     GEMM_TN_OPT_FORCE_SPLITS,
     GEMM_TN_OPT_FORCE_SWAP,
+    GEMM_TN_OPT_GROUP_M,
+    GEMM_TN_OPT_ROW_LOADER,
+    GEMM_TN_OPT_SERPENTINE,
     GEMM_TN_OPT_SKIP_FIRST_LOAD,
     GEMM_TN_OPT_STREAM_K,
     GEMM_TN_OPT_WAIT_TIMEOUT_NS,

@@ -33,6 +33,9 @@ GEMM_TN_OPT_FORCE_SWAP = 6
 GEMM_TN_OPT_FORCE_GENERIC_EPI = 7
 GEMM_TN_OPT_FORCE_PACK = 8
 GEMM_TN_OPT_STREAM_K = 9
+GEMM_TN_OPT_GROUP_M = 10
+GEMM_TN_OPT_SERPENTINE = 11
+GEMM_TN_OPT_ROW_LOADER = 12
 
 EXPORTED = ["gemm_tn_f16", "gemm_tn_f16_batched", "gemm_status_string", "gemm_tn_f16_last_device_error",
             "gemm_tn_f16_last_cuda_error", "gemm_tn_f16_shutdown", "gemm_tn_f16_version", "gemm_tn_f16_plan",
@@ -48,7 +51,10 @@ GEMM_TN_STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 class GemmError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {gemm_status_string(status)} (status {status})")
+        msg = f"{where}: {gemm_status_string(status)} (status {status})"
+        if status == GEMM_ERR_CUDA:
+            msg += f", cudaError_t {gemm_tn_f16_last_cuda_error()}"
+        super().__init__(msg)
 
 
 class gemm_tn_plan_t(ctypes.Structure):
@@ -58,7 +64,7 @@ class gemm_tn_plan_t(ctypes.Structure):
                 ("pack_b", ctypes.c_int32), ("units", ctypes.c_int64), ("grid", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("stream_k", ctypes.c_int32), ("sk_maxc", ctypes.c_int32),
                 ("dp_tiles", ctypes.c_int64), ("sk_tiles", ctypes.c_int64), ("stage_cd", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("row_load", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

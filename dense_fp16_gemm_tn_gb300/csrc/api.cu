@@ -49,6 +49,9 @@ std::atomic<int64_t> g_opt_force_swap{0};
 std::atomic<int64_t> g_opt_force_generic{0};
 std::atomic<int64_t> g_opt_force_pack{0};
 std::atomic<int64_t> g_opt_stream_k{0};
+std::atomic<int64_t> g_opt_group_m{0};
+std::atomic<int64_t> g_opt_serpentine{0};
+std::atomic<int64_t> g_opt_row_loader{0};
 
 gemm_status_t cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -235,6 +238,7 @@ struct Plan {
     int64_t sk_w_bytes, sk_ctr_bytes;  // stream-K partial slots and arrival counters
     int64_t sk_iters;
     int group_m;
+    int32_t rl, rl_a, rl_b;  // row-loader variant; A / B read by its loader warps (not repacked)
 };
 
 bool operand_tma_ok(bool aligned16, int64_t ld, int64_t stride, int64_t batch) {
@@ -311,7 +315,7 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
         const int64_t sk = tiles - dp;
         const int64_t I = sk * kb;
         TcVariant skv;
-        if (I >= Gs && find_tc_variant(pl.var.bn, pl.var.pair, pl.epi, 1, &skv)) {
+        if (I >= Gs && find_tc_variant(pl.var.bn, pl.var.pair, pl.epi | (pl.rl ? EPI_RL : 0), 1, &skv)) {
             auto owner = [&](int64_t i) { return ((i + 1) * Gs - 1) / I; };
             int64_t maxc = 1;
             for (int64_t t = 0; t < sk; ++t) maxc = std::max(maxc, owner((t + 1) * kb - 1) - owner(t * kb) + 1);
@@ -331,7 +335,7 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
             }
         }
     }
-    find_tc_variant(pl.var.bn, pl.var.pair, pl.epi, pub.stream_k, &pl.var);
+    find_tc_variant(pl.var.bn, pl.var.pair, pl.epi | (pl.rl ? EPI_RL : 0), pub.stream_k, &pl.var);
     pub.units = pub.stream_k ? pub.dp_tiles : tiles * pub.splits;
     pub.grid = pub.stream_k ? sk_groups * pair : std::min<int64_t>(pub.units, G) * pair;
     pub.workspace_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes;
@@ -474,13 +478,34 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
             find_tc_variant(bn, pair, epi, 0, &v);
         }
     }
+    // Operands whose rows TMA cannot address are repacked to an aligned scratch copy first,
+    // or, on request, read by the loader warps of a row-loader variant where one exists
+    // (K-major, unswapped, whole tiles): no scratch, but slower -- the loader warps' loads,
+    // one row per lane, cost about 2300 L1 wavefronts per k-block against the 512 cycles
+    // its MMAs take (GB300: 4095 x 3073 x 2047 packed, 190.9 against 56.5 us repacked;
+    // 4096^3 with lda = 4097, 591 against 81 us aligned).
+    if (g_opt_row_loader.load() > 0 && (pub.pack_a || pub.pack_b) && !force_pack && !swap && !pr.a_mn && !pr.b_mn &&
+        splits == 1) {
+        TcVariant rv;
+        if (find_tc_variant(v.bn, v.pair, epi | EPI_RL, 0, &rv)) {
+            v = rv;
+            pl.rl = 1;
+            pl.rl_a = pub.pack_a;
+            pl.rl_b = pub.pack_b;
+            pub.pack_a = pub.pack_b = 0;
+        }
+    }
+    pub.row_load = (pl.rl_a ? 1 : 0) | (pl.rl_b ? 2 : 0);
     pl.var = v;
     pl.epi = epi;
     pl.rows_a = rows_a;
     pl.rows_b = rows_b;
     pl.tiles_m = ceil_div(rows_a, 128 * pair);
     pl.tiles_n = ceil_div(rows_b, bn);
-    pl.group_m = pair == 2 ? 8 : 16;
+    // 16 tile rows per rasterisation group (ncu, GB300: 4096^3 DRAM traffic 125.7 MB against
+    // 151.9 MB with 8 rows, 85.4 against 86.1 us; 8192^3 with serpentine K order 831 MB
+    // against 1019 MB with 8 rows and forward K order).
+    pl.group_m = g_opt_group_m.load() > 0 ? static_cast<int>(g_opt_group_m.load()) : 16;
 
     pub.kernel = splits > 1 ? 3 : 2;
     pub.tile_m = 128 * pair;
@@ -566,11 +591,13 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     const uint32_t boxA = p.a_mn ? 64u : (swap ? box_rows_b : 128u);
     const uint32_t boxB = p.b_mn ? 64u : (swap ? 128u : box_rows_b);
     CUtensorMap mapPA, mapPB;
-    if (!pl.pub.pack_a && !encode_map(&mapPA, A, a_len(p), a_rows(p), p.batch, p.lda, p.sA, p.batch > 1 && p.sA != 0,
+    std::memset(&mapPA, 0, sizeof(mapPA));  // operands read by the row loader need no map
+    std::memset(&mapPB, 0, sizeof(mapPB));
+    if (!pl.pub.pack_a && !pl.rl_a && !encode_map(&mapPA, A, a_len(p), a_rows(p), p.batch, p.lda, p.sA, p.batch > 1 && p.sA != 0,
                                       64, boxA))
         pl.pub.pack_a = 1,
         pl.pack_a_bytes = round_up(((p.batch > 1 && p.sA != 0) ? p.batch : 1) * a_rows(p) * pl.ldo_a * 2, 256);
-    if (!pl.pub.pack_b && !encode_map(&mapPB, B, b_len(p), b_rows(p), p.batch, p.ldb, p.sB, p.batch > 1 && p.sB != 0,
+    if (!pl.pub.pack_b && !pl.rl_b && !encode_map(&mapPB, B, b_len(p), b_rows(p), p.batch, p.ldb, p.sB, p.batch > 1 && p.sB != 0,
                                       64, boxB))
         pl.pub.pack_b = 1,
         pl.pack_b_bytes = round_up(((p.batch > 1 && p.sB != 0) ? p.batch : 1) * b_rows(p) * pl.ldo_b * 2, 256);
@@ -583,6 +610,16 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
         // (512-column tiles exist with TMA epilogues only: 256 columns, same B boxes)
         if (find_tc_variant(pl.var.bn, pl.var.pair, generic, 0, &v) ||
             find_tc_variant(std::min(pl.var.bn, 256), pl.var.pair, generic, 0, &v)) {
+            if (pl.rl) {  // no row-loader variant with this epilogue: repack those operands
+                pl.pub.pack_a |= pl.rl_a;
+                pl.pub.pack_b |= pl.rl_b;
+                pl.pack_a_bytes = pl.pub.pack_a
+                    ? round_up(((p.batch > 1 && p.sA != 0) ? p.batch : 1) * a_rows(p) * pl.ldo_a * 2, 256) : 0;
+                pl.pack_b_bytes = pl.pub.pack_b
+                    ? round_up(((p.batch > 1 && p.sB != 0) ? p.batch : 1) * b_rows(p) * pl.ldo_b * 2, 256) : 0;
+                pl.rl = pl.rl_a = pl.rl_b = 0;
+                pl.pub.row_load = 0;
+            }
             pl.var = v;
             pl.epi = generic;
             pl.pub.epi_tma = 0;
@@ -657,6 +694,18 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     kp.splits = pl.pub.splits;
     kp.kb_total = static_cast<int32_t>(ceil_div(p.K, 64));
     kp.group_m = pl.group_m;
+    {
+        // Serpentine K order where the operands are too large to stay in L2 between two
+        // waves of data-parallel tiles.  An LRU model of the tile order reproduces the
+        // measured DRAM reads of 8192^3 (881 / 822 / 847 MB for groups of 8 / 12 / 16 tile
+        // rows) with about 50 MB of effective L2, and predicted 708 MB with serpentine order
+        // and 16-row groups; ncu measured 712 MB.
+        const int64_t mode = g_opt_serpentine.load();
+        const int64_t groups = std::max<int64_t>(pl.pub.grid / pl.var.pair, 1);
+        const int64_t op_bytes = 2 * (a_rows(p) * a_len(p) + b_rows(p) * b_len(p)) *
+                                 ((p.batch > 1 && (p.sA != 0 || p.sB != 0)) ? p.batch : 1);
+        kp.serp = (mode > 0 || (mode == 0 && pl.pub.dp_tiles >= 2 * groups && op_bytes >= (int64_t(128) << 20))) ? 1 : 0;
+    }
     kp.zA = swap ? (b_batched ? 1 : 0) : (a_batched ? 1 : 0);
     kp.zB = swap ? (a_batched ? 1 : 0) : (b_batched ? 1 : 0);
     kp.zC = (p.batch > 1 && p.sC != 0) ? 1 : 0;
@@ -679,6 +728,19 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     kp.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
     kp.debug_skip_first_load = g_opt_skip_first_load.load() != 0 ? 1 : 0;
     kp.pdl = njobs > 0 ? 1 : 0;  // directly behind the repack launch
+    if (pl.rl) {
+        // row loader: the MMA's operands are the problem's A and B (never swapped)
+        kp.rl_on[0] = pl.rl_a;
+        kp.rl_on[1] = pl.rl_b;
+        kp.rl_ptr[0] = A;
+        kp.rl_ptr[1] = B;
+        kp.rl_ld[0] = p.lda;
+        kp.rl_ld[1] = p.ldb;
+        kp.rl_stride[0] = p.batch > 1 ? p.sA : 0;
+        kp.rl_stride[1] = p.batch > 1 ? p.sB : 0;
+        const int64_t a_box = 128 * 64 * 2, b_box = static_cast<int64_t>(pl.var.bn / pl.var.pair) * 64 * 2;
+        kp.tma_tx = static_cast<uint32_t>(((pl.rl_a ? 0 : a_box) + (pl.rl_b ? 0 : b_box)) * pl.var.pair);
+    }
     if (pl.epi == EPI_PARTIAL && encode_partials_map(&mapD, kp.W, p.M, p.N, p.batch * pl.pub.splits)) kp.w_tma = 1;
 
     if (pl.sk_iters > 0) {
@@ -1080,6 +1142,15 @@ gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value) {
             if (value < -1 || value > 1) return GEMM_ERR_INVALID_VALUE;
             g_opt_stream_k = value;
             return GEMM_OK;
+        case GEMM_TN_OPT_GROUP_M:
+            if (value < 0 || value > 64) return GEMM_ERR_INVALID_VALUE;
+            g_opt_group_m = value;
+            return GEMM_OK;
+        case GEMM_TN_OPT_SERPENTINE:
+            if (value < -1 || value > 1) return GEMM_ERR_INVALID_VALUE;
+            g_opt_serpentine = value;
+            return GEMM_OK;
+        case GEMM_TN_OPT_ROW_LOADER: g_opt_row_loader = value ? 1 : 0; return GEMM_OK;
 
     }
     return GEMM_ERR_INVALID_VALUE;
@@ -1096,6 +1167,9 @@ int64_t gemm_tn_f16_get_option(int32_t option) {
         case GEMM_TN_OPT_FORCE_GENERIC_EPI: return g_opt_force_generic.load();
         case GEMM_TN_OPT_FORCE_PACK: return g_opt_force_pack.load();
         case GEMM_TN_OPT_STREAM_K: return g_opt_stream_k.load();
+        case GEMM_TN_OPT_GROUP_M: return g_opt_group_m.load();
+        case GEMM_TN_OPT_SERPENTINE: return g_opt_serpentine.load();
+        case GEMM_TN_OPT_ROW_LOADER: return g_opt_row_loader.load();
 
     }
     return -1;

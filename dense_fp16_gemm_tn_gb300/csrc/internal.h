@@ -20,7 +20,7 @@ struct TcVariant {
     int index;   // position in the variant table (for per-device caches)
 };
 
-constexpr int kMaxVariants = 64;
+constexpr int kMaxVariants = 96;
 
 // Looks up the compiled variant for (bn, pair, epi, sk); returns false if none exists.
 bool find_tc_variant(int bn, int pair, int epi, int sk, TcVariant* out);

@@ -18,17 +18,25 @@ enum EpiMode : int {
     EPI_VEC = 9,           // D (and C) at any 2-byte alignment through aligned 16-byte words, per row
 };
 
+// Variant flag (or-ed into the epilogue mode of a variant): eight more warps read the
+// rows of operands TMA cannot address (K-major, any 2-byte alignment) through the aligned
+// 16-byte words that cover them and write the swizzled shared-memory image themselves.
+constexpr int EPI_RL = 0x100;
+
 #ifdef __CUDACC__
 #define GTN_HD __host__ __device__
 #else
 #define GTN_HD
 #endif
 
+// Epilogue mode of a variant without its flags.
+GTN_HD constexpr int epi_mode(int epi) { return epi & 0xff; }
 // Epilogue mode without the accumulator precision; true when the accumulator is fp16.
 GTN_HD constexpr int epi_base(int epi) {
-    return epi == EPI_TMA_A16 ? EPI_TMA : epi == EPI_GENERIC_A16 ? EPI_GENERIC : epi;
+    return epi_mode(epi) == EPI_TMA_A16 ? EPI_TMA : epi_mode(epi) == EPI_GENERIC_A16 ? EPI_GENERIC : epi_mode(epi);
 }
-GTN_HD constexpr bool epi_acc16(int epi) { return epi == EPI_TMA_A16 || epi == EPI_GENERIC_A16; }
+GTN_HD constexpr bool epi_acc16(int epi) { return epi_mode(epi) == EPI_TMA_A16 || epi_mode(epi) == EPI_GENERIC_A16; }
+GTN_HD constexpr bool epi_rl(int epi) { return (epi & EPI_RL) != 0; }
 
 struct KParams {
     // Tensor-core view: the MMA's A operand has rows_a rows, its B operand rows_b rows.
@@ -37,6 +45,7 @@ struct KParams {
     int32_t splits;            // K slices per tile
     int32_t kb_total;          // number of 64-wide k-blocks, ceil(K/64)
     int32_t group_m;           // rasterisation group size along the tile rows
+    int32_t serp;              // 1: odd waves of data-parallel units walk K backwards (serpentine)
     int32_t zA, zB, zC, zD;    // batch coordinate multipliers (0 = operand not batched)
     int32_t a_mn, b_mn;        // 1: the MMA operand is stored MN-major (rows contiguous), 0: K-major
     int64_t num_units;         // data-parallel units: whole tiles, or (tile, K slice) pairs when splits > 1
@@ -68,6 +77,14 @@ struct KParams {
     // repack), whose output the producer waits for before its first load; everything
     // up to that point (barriers, tensor memory, tensor maps) overlaps that kernel.
     int32_t pdl;
+    // Row loader (EPI_RL variants): MMA operand X (0 = A, 1 = B) is read by the loader warps
+    // when rl_on[X] is 1 -- row-major, K contiguous, from rl_ptr[X] with leading dimension
+    // rl_ld[X] and batch stride rl_stride[X] (elements, 0 = broadcast) -- else by TMA.
+    const void* rl_ptr[2];
+    int64_t rl_ld[2];
+    int64_t rl_stride[2];
+    int32_t rl_on[2];
+    uint32_t tma_tx;  // bytes TMA brings per stage (both CTAs of a pair), for EPI_RL variants
     // EPI_PARTIAL: 1 when the tmD slot holds a tensor map of W (fp32, [batch * splits][M][N],
     // boxes of 32 rows x 32 columns, 128-byte swizzle), so partials are stored by TMA.
     int32_t w_tma;

@@ -64,8 +64,10 @@
 
 namespace gtn {
 
-template <int BN, int PAIR, int STAGES, int EPI>
+template <int BN, int PAIR, int STAGES, int EPIX>
 struct TileCfg {
+    static constexpr int EPI = epi_mode(EPIX);   // epilogue mode
+    static constexpr bool RL = epi_rl(EPIX);     // row-loader warps for operands TMA cannot address
     static constexpr int BM = 128;               // accumulator rows per CTA (tensor-memory lanes)
     static constexpr int BK = 64;                // halves per 128-byte swizzled row
     static constexpr int BN_LOCAL = BN / PAIR;   // B rows each CTA of a pair loads
@@ -83,7 +85,17 @@ struct TileCfg {
     static constexpr int B_BYTES = BN_LOCAL * BK * 2;
     static constexpr uint32_t STAGE_TX = uint32_t(A_BYTES + B_BYTES) * PAIR;
     static constexpr int EPI_WARPS = 4;
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int RL_WARPS = RL ? 8 : 0;  // one operand row per loader thread and k-block
+    // Warp roles: 0 TMA producer, 1 MMA issuer, then the epilogue warps, then the loader warps.
+    // With the row loader the block is four warpgroups whose register shares differ
+    // (setmaxnreg): warps 0-3 (producer, MMA, two idle) give registers up, the epilogue
+    // warpgroup (4-7) and the two loader warpgroups (8-15) take them.
+    static constexpr int EPI_W0 = RL ? 4 : 2;
+    static constexpr int RL_W0 = EPI_W0 + EPI_WARPS;
+    static constexpr int THREADS = 32 * RL_W0 + 32 * RL_WARPS;
+    static constexpr int REGS_CTRL = 48, REGS_EPI = 176, REGS_RL = 144;  // per thread, after setmaxnreg
+    // Registers per thread: all of the 64K register file over the block's warps, in steps of 8.
+    static constexpr int MAX_REGS = ((65536 / THREADS) / 8 * 8) > 255 ? 255 : ((65536 / THREADS) / 8 * 8);
     static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
     static constexpr int EPI_WARP_BYTES =
@@ -111,11 +123,19 @@ struct TileCfg {
                   "the TMA and row-word epilogues work in 64-column chunks");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory per CTA");
     static_assert(PAIR == 1 || PAIR == 2, "CTA pair or single CTA");
+    static_assert(!RL || (BM + BN_LOCAL <= 32 * RL_WARPS && BN_LOCAL % 32 == 0 && N_MMAS == 1),
+                  "row loader: one row of A or B per loader thread, whole warps per operand");
+    static_assert(!RL || EPI == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG || EPI == EPI_VEC,
+                  "row loader: unswapped whole-tile epilogues only");
+    static_assert(!RL || (THREADS == 512 && MAX_REGS == 128 &&
+                          REGS_CTRL + REGS_EPI + 2 * REGS_RL == 4 * MAX_REGS),
+                  "the warpgroups' register shares must add up to the block's launch allocation");
 };
 
 // One piece of work for a CTA (pair): k-blocks [kb0, kb1) of one output tile.
 struct Seg {
     int32_t b, tm, tn, kb0, kb1, split;
+    int32_t rev;      // 1: k-blocks are loaded from kb1 - 1 down to kb0
     int32_t sk_tile;  // index among the stream-K tiles, or -1 when this segment finishes its tile alone
     int32_t sk_j;     // this group's rank among the tile's contributors
     int32_t sk_n;     // number of contributors to the tile
@@ -127,6 +147,7 @@ struct Seg {
 struct SegIter {
     int64_t g, G;
     int64_t dp_next;
+    int32_t dp_wave;  // wave of the next data-parallel unit (dp_next / G)
     int64_t sk_i, sk_end;
 };
 
@@ -157,6 +178,7 @@ __device__ __forceinline__ SegIter seg_begin(const KParams& p, int64_t g, int64_
     it.g = g;
     it.G = G;
     it.dp_next = g;
+    it.dp_wave = 0;
     it.sk_i = (SK && p.sk_iters > 0) ? sk_start(p, g, G) : 0;
     it.sk_end = (SK && p.sk_iters > 0) ? sk_start(p, g + 1, G) : 0;
     return it;
@@ -173,6 +195,7 @@ __device__ __forceinline__ bool seg_next(const KParams& p, SegIter& it, Seg& s) 
         const int64_t k1 = min(kb, k0 + (it.sk_end - it.sk_i));
         tile_coords(p, p.num_units + tsk, s);
         s.split = 0;
+        s.rev = 0;
         s.kb0 = static_cast<int32_t>(k0);
         s.kb1 = static_cast<int32_t>(k1);
         if (k0 == 0 && k1 == kb) {
@@ -191,6 +214,11 @@ __device__ __forceinline__ bool seg_next(const KParams& p, SegIter& it, Seg& s) 
     if (it.dp_next < p.num_units) {
         const int64_t u = it.dp_next;
         it.dp_next += it.G;
+        // Serpentine K order: every other wave walks K backwards, so that it starts on the
+        // k-blocks the wave before it loaded last, which are still in L2 where the two
+        // waves share operand rows.
+        s.rev = p.serp & it.dp_wave;
+        it.dp_wave ^= 1;
         if (p.splits == 1) {  // whole tiles: no K-slice arithmetic
             s.split = 0;
             tile_coords(p, u, s);
@@ -231,10 +259,30 @@ static __device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, uin
     }
 }
 
+// The same slow path inlined: kernels that change register shares per warpgroup
+// (setmaxnreg) make no calls, since a callee is compiled for one register count.
+static __device__ __forceinline__ bool wait_slow_inl(uint32_t bar, uint32_t parity, uint32_t* err,
+                                                     uint64_t timeout_ns, volatile int* abort_flag, uint32_t who) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_ns(bar, parity, kWaitSuspendNs)) return true;
+        if ((i & 15u) == 0) {
+            if (*abort_flag) return false;
+            if (global_timer_ns() - t0 > timeout_ns) {
+                atomicCAS(err, 0u, 0x500u | who);
+                *abort_flag = 1;
+                return false;
+            }
+        }
+    }
+}
+
+template <bool INL = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint32_t* err, uint64_t timeout_ns,
                                              volatile int* abort_flag, uint32_t who) {
     if (mbar_try_wait_ns(bar, parity, kWaitSuspendNs)) return true;
-    return wait_slow(bar, parity, err, timeout_ns, abort_flag, who);
+    if constexpr (INL) return wait_slow_inl(bar, parity, err, timeout_ns, abort_flag, who);
+    else return wait_slow(bar, parity, err, timeout_ns, abort_flag, who);
 }
 
 __device__ __forceinline__ void spin_ns(uint64_t ns) {
@@ -254,12 +302,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
 
 // SK: compiled with the stream-K phase (partial slots, arrival counters,
 // fixups); without it the kernel is purely data-parallel.
-template <int BN, int PAIR, int STAGES, int EPI, bool SK>
-__global__ void __launch_bounds__(TileCfg<BN, PAIR, STAGES, EPI>::THREADS, 1)
+template <int BN, int PAIR, int STAGES, int EPIX, bool SK>
+__global__ void __launch_bounds__(TileCfg<BN, PAIR, STAGES, EPIX>::THREADS, 1)
 gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmD,
                   const KParams p) {
-    using Cfg = TileCfg<BN, PAIR, STAGES, EPI>;
+    using Cfg = TileCfg<BN, PAIR, STAGES, EPIX>;
+    constexpr int EPI = Cfg::EPI;
     constexpr int EB = epi_base(EPI);       // epilogue mode without the accumulator precision
     constexpr bool ACC16 = epi_acc16(EPI);  // fp16 accumulator in tensor memory
     extern __shared__ uint8_t smem_raw[];
@@ -287,8 +336,14 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int64_t ngroups = gridDim.x / PAIR;
 
     if (threadIdx.x == 0) {
+        // A stage is full once the leader's producer has armed it (and TMA has brought its
+        // bytes) and, with the row loader, every loader warp of both CTAs that writes an
+        // operand has arrived.
+        uint32_t full_count = 1;
+        if constexpr (Cfg::RL)
+            full_count += static_cast<uint32_t>(((p.rl_on[0] ? Cfg::BM : 0) + (p.rl_on[1] ? Cfg::BN_LOCAL : 0)) / 32 * PAIR);
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
+            mbar_init(full_bar(s), full_count);
             mbar_init(empty_bar(s), 1);
         }
         for (int a = 0; a < 2; ++a) {
@@ -301,8 +356,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
+        if (!(Cfg::RL && p.rl_on[0])) prefetch_tensormap(&tmA);
+        if (!(Cfg::RL && p.rl_on[1])) prefetch_tensormap(&tmB);
         if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG || EPI == EPI_PARTIAL)
             prefetch_tensormap(&tmD);
         if constexpr (EPI == EPI_TMA_C) prefetch_tensormap(&tmC);
@@ -313,6 +368,10 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
+    // Each role's register share is set at the top of its branch (row-loader variants), so
+    // that the compiler allocates every role's code within its own share.
+    if (warp < Cfg::EPI_W0) {
+    if constexpr (Cfg::RL) setmaxnreg_dec<Cfg::REGS_CTRL>();
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -327,8 +386,9 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const int32_t rowA = w.tm * (Cfg::BM * PAIR) + Cfg::BM * static_cast<int32_t>(rank);
                 // B box nb holds tile columns nb*MMA_N + [0, MMA_N), split between the pair
                 const int32_t rowB = w.tn * BN + Cfg::B_BOX_ROWS * static_cast<int32_t>(rank);
-                for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
-                    if (!wait_bounded(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 1)) {
+                for (int32_t i = 0; i < w.kb1 - w.kb0; ++i) {
+                    const int32_t kb = w.rev ? w.kb1 - 1 - i : w.kb0 + i;
+                    if (!wait_bounded<Cfg::RL>(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 1)) {
                         ok = false;
                         break;
                     }
@@ -336,7 +396,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     first = false;
                     if (!skip) {
                         const uint32_t fb = full_bar(stage);
-                        if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::STAGE_TX);
+                        if (rank == 0) mbar_arrive_expect_tx(fb, Cfg::RL ? p.tma_tx : Cfg::STAGE_TX);
                         const uint32_t dA = sA + stage * Cfg::A_BYTES;
                         const uint32_t dB = sB + stage * Cfg::B_BYTES;
                         // K-major operand: one box of 64 K x rows.  MN-major operand: boxes of
@@ -346,7 +406,9 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             if constexpr (PAIR == 1) tma_load_3d(dst, map, fl, x, y, z);
                             else tma_load_3d_pair(dst, map, fl, x, y, z);
                         };
-                        if (!p.a_mn) {
+                        if (Cfg::RL && p.rl_on[0]) {
+                            // A rows come from the loader warps
+                        } else if (!p.a_mn) {
                             load(dA, &tmA, kb * Cfg::BK, rowA, w.b * p.zA);
                         } else {
 #pragma unroll
@@ -357,7 +419,9 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         for (int nb = 0; nb < Cfg::N_MMAS; ++nb) {
                             const uint32_t dBn = dB + static_cast<uint32_t>(nb * Cfg::B_BOX_BYTES);
                             const int32_t rowBn = rowB + nb * Cfg::MMA_N;
-                            if (!p.b_mn) {
+                            if (Cfg::RL && p.rl_on[1]) {
+                                // B rows come from the loader warps
+                            } else if (!p.b_mn) {
                                 load(dBn, &tmB, kb * Cfg::BK, rowBn, w.b * p.zB);
                             } else {
                                 if constexpr (Cfg::B_BOX_ROWS % 64 == 0) {
@@ -374,7 +438,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // Drain: wait until the MMA has released every slot, so that no
             // tcgen05.commit arrives on this CTA's barriers after it exits.
             for (int i = 0; i < STAGES && ok; ++i) {
-                if (!wait_bounded(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 2)) break;
+                if (!wait_bounded<Cfg::RL>(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 2)) break;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
@@ -401,7 +465,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 // One accumulator of 512 columns: wait here for its first half only; the
                 // second half is waited for just before its first MMA, so that the tile's
                 // first k-block of MMAs runs while the epilogue still drains that half.
-                if (!wait_bounded(tempty_bar(Cfg::ACC_BUFS == 1 ? 0 : acc), acc_phase ^ 1u, p.err, p.timeout_ns,
+                if (!wait_bounded<Cfg::RL>(tempty_bar(Cfg::ACC_BUFS == 1 ? 0 : acc), acc_phase ^ 1u, p.err, p.timeout_ns,
                                   abort_flag, 3))
                     break;
                 tc_fence_after();
@@ -410,16 +474,18 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     // The stage was written by TMA (async proxy) and completed through the
                     // mbarrier's transaction count: the wait alone orders the MMA's reads.
-                    if (!wait_bounded(full_bar(stage), phase, p.err, p.timeout_ns, abort_flag, 4)) {
+                    if (!wait_bounded<Cfg::RL>(full_bar(stage), phase, p.err, p.timeout_ns, abort_flag, 4)) {
                         ok = false;
                         break;
                     }
+                    // Loader warps of the other CTA arrive with cluster-scope release.
+                    if constexpr (Cfg::RL && PAIR == 2) fence_acq_rel_cluster();
                     const uint64_t adesc = adesc0 + static_cast<uint64_t>(stage * (Cfg::A_BYTES >> 4));
                     const uint64_t bdesc = bdesc0 + static_cast<uint64_t>(stage * (Cfg::B_BYTES >> 4));
 #pragma unroll
                     for (int nb = 0; nb < Cfg::N_MMAS; ++nb) {
                         if (nb == 1 && !hi_ready) {
-                            if (!wait_bounded(tempty_bar(1), acc_phase ^ 1u, p.err, p.timeout_ns, abort_flag, 3)) {
+                            if (!wait_bounded<Cfg::RL>(tempty_bar(1), acc_phase ^ 1u, p.err, p.timeout_ns, abort_flag, 3)) {
                                 ok = false;
                                 break;
                             }
@@ -439,16 +505,140 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (ok && !hi_ready)  // (a segment always has k-blocks; keeps the phases in step regardless)
-                    ok = wait_bounded(tempty_bar(1), acc_phase ^ 1u, p.err, p.timeout_ns, abort_flag, 3);
+                    ok = wait_bounded<Cfg::RL>(tempty_bar(1), acc_phase ^ 1u, p.err, p.timeout_ns, abort_flag, 3);
                 if (!ok) break;
                 if constexpr (PAIR == 1) mma_commit(tfull_bar(acc));
                 else mma_commit_pair(tfull_bar(acc), 0x3);
                 if (++acc == Cfg::ACC_BUFS) { acc = 0; acc_phase ^= 1u; }
             }
         }
+    }  // (warps 2-3 of the row-loader variants' first warpgroup are idle)
+    } else if (warp >= Cfg::RL_W0) {
+        if constexpr (Cfg::RL) setmaxnreg_inc<Cfg::REGS_RL>();
+        // ------------------------------------------------------------ row loader (EPI_RL variants)
+        // Loader thread lt owns one row of this CTA's part of a stage: A row lt for lt < BM,
+        // else B row lt - BM.  Per k-block it loads the aligned 16-byte words covering the
+        // row's 64 halves, shifts them into place, zeroes the halves past K, and writes the
+        // eight 16-byte chunks of the row where TMA's 128-byte swizzle would put them.
+        // Loads run two k-blocks ahead of the stores (register double buffer).
+        if constexpr (Cfg::RL) {
+            const int lt = static_cast<int>(threadIdx.x) - 32 * Cfg::RL_W0;
+            const bool isA = lt < Cfg::BM;
+            const int j = isA ? lt : lt - Cfg::BM;  // row within this CTA's block of the operand
+            const int op = isA ? 0 : 1;
+            if (j < (isA ? Cfg::BM : Cfg::BN_LOCAL) && p.rl_on[op]) {  // warp-uniform
+                if (p.pdl) griddep_wait();  // (the other operand is being repacked by the kernel before)
+                const uint16_t* const base = static_cast<const uint16_t*>(p.rl_ptr[op]);
+                const int64_t ld = p.rl_ld[op], bstride = p.rl_stride[op];
+                const int64_t nrows = isA ? p.rows_a : p.rows_b;
+                const int32_t kb_total = p.kb_total;
+                // Cursor over this CTA group's data-parallel tiles and their k-blocks.
+                struct Cur {
+                    int64_t u;             // work unit
+                    int32_t i;             // k-block index within the tile, in load order
+                    int32_t rev;           // serpentine: k-blocks in reverse order
+                    const uint16_t* row;   // this thread's row at k = 0, or null past the operand
+                };
+                auto cur_tile = [&](Cur& c, int32_t wave) {
+                    c.i = 0;
+                    c.row = nullptr;
+                    c.rev = p.serp & wave;
+                    if (c.u >= p.num_units) return;
+                    Seg t;
+                    tile_coords(p, c.u, t);
+                    const int64_t r = isA ? static_cast<int64_t>(t.tm) * (Cfg::BM * PAIR) + Cfg::BM * rank + j
+                                          : static_cast<int64_t>(t.tn) * BN + Cfg::B_BOX_ROWS * rank + j;
+                    if (r < nrows) c.row = base + static_cast<int64_t>(t.b) * bstride + r * ld;
+                };
+                Cur cl, cs;  // load cursor (two k-blocks ahead) and store cursor
+                int32_t wl = 0, ws = 0;  // wave parities of the two cursors
+                cl.u = cs.u = group;
+                cur_tile(cl, wl);
+                cur_tile(cs, ws);
+                auto step = [&](Cur& c, int32_t& wave) {
+                    if (++c.i >= kb_total) {
+                        c.u += ngroups;
+                        wave ^= 1;
+                        cur_tile(c, wave);
+                    }
+                };
+                // Issues the loads of the cursor's k-block; returns the shift of the row start
+                // within its first word and the number of real halves in `valid`.
+                auto issue = [&](const Cur& c, uint32_t (&v)[36], int& valid) -> uint32_t {
+                    valid = 0;
+                    const uint16_t* src = nullptr;
+                    if (c.u < p.num_units && c.row != nullptr) {
+                        const int32_t kb = c.rev ? kb_total - 1 - c.i : c.i;
+                        const int64_t k0 = static_cast<int64_t>(kb) * Cfg::BK;
+                        valid = static_cast<int>(p.K - k0 < Cfg::BK ? p.K - k0 : Cfg::BK);
+                        src = c.row + k0;
+                    }
+                    return load_cover64(src, valid, v);
+                };
+                const uint32_t sbase_op = isA ? sA : sB;
+                const uint32_t stage_bytes = isA ? Cfg::A_BYTES : Cfg::B_BYTES;
+                const uint32_t row_off = static_cast<uint32_t>(j) * 128u;
+                const uint32_t sw = static_cast<uint32_t>(j) & 7u;
+                int stage = 0;
+                uint32_t phase = 0;
+                bool ok = true;
+                // Writes one k-block's row into the ring slot and signals the stage.
+                auto put = [&](const uint32_t (&v)[36], uint32_t sh, int valid) {
+                    int go = 1;
+                    if (lane == 0)
+                        go = wait_bounded<Cfg::RL>(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 7) ? 1 : 0;
+                    go = __shfl_sync(0xffffffffu, go, 0);
+                    if (!go) {
+                        ok = false;
+                        return;
+                    }
+                    uint32_t w[32];
+                    align_cover64(v, sh, w);
+                    if (valid < Cfg::BK) {
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) {
+                            const int e = 2 * q;
+                            w[q] = e >= valid ? 0u : (e + 1 >= valid ? (w[q] & 0xffffu) : w[q]);
+                        }
+                    }
+                    const uint32_t dst = sbase_op + static_cast<uint32_t>(stage) * stage_bytes + row_off;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c)
+                        st_shared_v4(dst + ((static_cast<uint32_t>(c) ^ sw) << 4), w[4 * c], w[4 * c + 1], w[4 * c + 2],
+                                     w[4 * c + 3]);
+                    fence_proxy_async_smem();  // the tensor core reads the slot through the async proxy
+                    __syncwarp();
+                    if (lane == 0) {
+                        if constexpr (PAIR == 1) mbar_arrive(full_bar(stage));
+                        else mbar_arrive_cluster(map_to_cta(full_bar(stage), 0));
+                    }
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                };
+                uint32_t va[36], vb[36];
+                int na = 0, nb = 0;
+                uint32_t sa = issue(cl, va, na);
+                step(cl, wl);
+                uint32_t sb = issue(cl, vb, nb);
+                step(cl, wl);
+                while (ok && cs.u < p.num_units) {
+                    put(va, sa, na);
+                    if (!ok) break;
+                    step(cs, ws);
+                    sa = issue(cl, va, na);
+                    step(cl, wl);
+                    if (cs.u >= p.num_units) break;
+                    put(vb, sb, nb);
+                    if (!ok) break;
+                    step(cs, ws);
+                    sb = issue(cl, vb, nb);
+                    step(cl, wl);
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------------ epilogue warps
-        const int ew = warp - 2;
+        if constexpr (Cfg::RL) setmaxnreg_inc<Cfg::REGS_EPI>();
+        const int ew = warp - Cfg::EPI_W0;
         const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31 are this warp's
         uint8_t* ebuf = smem + Cfg::OFF_EPI + ew * Cfg::EPI_WARP_BYTES;
         int acc = 0;
@@ -525,7 +715,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (!partial && p.beta != 0.0f) prefetch_cg(0);
             }
             int ok = 1;
-            if (lane == 0) ok = wait_bounded(tfull_bar(acc), acc_phase, p.err, p.timeout_ns, abort_flag, 5) ? 1 : 0;
+            if (lane == 0) ok = wait_bounded<Cfg::RL>(tfull_bar(acc), acc_phase, p.err, p.timeout_ns, abort_flag, 5) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
@@ -762,7 +952,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                 // before the next chunk's C lands there
                                 bulk_wait_group_read<0>();
                                 if (c + 1 < BN / 64) issue_c(c + 1, buf ^ 1u);
-                                wait_bounded(cload_bar(ew, static_cast<int>(buf)), (cphase >> buf) & 1u, p.err,
+                                wait_bounded<Cfg::RL>(cload_bar(ew, static_cast<int>(buf)), (cphase >> buf) & 1u, p.err,
                                              p.timeout_ns, abort_flag, 6);
                             }
                             cphase ^= 1u << buf;

@@ -26,6 +26,15 @@ struct TcLauncher {
         e = cudaFuncSetAttribute(gemm_tn_tc_kernel<BN, PAIR, STAGES, EPI, SK>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
+        if constexpr (Cfg::RL) {
+            // The warpgroups' register shares (setmaxnreg) add up to exactly MAX_REGS per
+            // thread; a kernel built with any other count could leave an increase waiting
+            // for registers that never come free, so it is refused.
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, gemm_tn_tc_kernel<BN, PAIR, STAGES, EPI, SK>);
+            if (e != cudaSuccess) return e;
+            if (fa.numRegs != Cfg::MAX_REGS || fa.maxThreadsPerBlock < Cfg::THREADS) return cudaErrorInvalidConfiguration;
+        }
         if (dev >= 0 && dev < 64) done[dev] = true;
         return cudaSuccess;
     }

@@ -12,7 +12,10 @@ bool launch_family_swap(const TcVariant&, const CUtensorMap&, const CUtensorMap&
                         int64_t, cudaStream_t, int64_t*, cudaError_t*);
 bool launch_family_wide(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                         const KParams&, int64_t, cudaStream_t, int64_t*, cudaError_t*);
+bool launch_family_rowload(const TcVariant&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                           const CUtensorMap&, const KParams&, int64_t, cudaStream_t, int64_t*, cudaError_t*);
 bool capacity_family_tma(const TcVariant&, int, int64_t*);
+bool capacity_family_rowload(const TcVariant&, int, int64_t*);
 bool capacity_family_wide(const TcVariant&, int, int64_t*);
 bool capacity_family_generic(const TcVariant&, int, int64_t*);
 bool capacity_family_swap(const TcVariant&, int, int64_t*);
@@ -78,6 +81,14 @@ static const TcVariant kVariants[] = {
     {16, 1, 12, EPI_PARTIAL_SWAP, 0, 0},
     {32, 1, 11, EPI_PARTIAL_SWAP, 0, 0},
     {64, 1, 9, EPI_PARTIAL_SWAP, 0, 0},
+    {256, 2, 6, EPI_VEC | EPI_RL, 0, 0},
+    {256, 2, 6, EPI_TMA | EPI_RL, 0, 0},
+    {256, 2, 6, EPI_TMA_C | EPI_RL, 0, 0},
+    {256, 2, 6, EPI_TMA_CG | EPI_RL, 0, 0},
+    {128, 1, 6, EPI_VEC | EPI_RL, 0, 0},
+    {128, 1, 6, EPI_TMA | EPI_RL, 0, 0},
+    {128, 1, 6, EPI_TMA_C | EPI_RL, 0, 0},
+    {128, 1, 6, EPI_TMA_CG | EPI_RL, 0, 0},
 };
 
 static_assert(sizeof(kVariants) / sizeof(kVariants[0]) <= kMaxVariants, "variant table too large");
@@ -105,13 +116,14 @@ cudaError_t launch_tc_variant(const TcVariant& v, const CUtensorMap& tmA, const 
     if (launch_family_wide(v, tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out, &e)) return e;
     if (launch_family_generic(v, tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out, &e)) return e;
     if (launch_family_swap(v, tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out, &e)) return e;
+    if (launch_family_rowload(v, tmA, tmB, tmC, tmD, p, max_ctas, stream, grid_out, &e)) return e;
     return cudaErrorInvalidValue;
 }
 
 int64_t tc_variant_capacity(const TcVariant& v, int sms) {
     int64_t cap = 0;
     if (capacity_family_tma(v, sms, &cap) || capacity_family_wide(v, sms, &cap) || capacity_family_generic(v, sms, &cap) ||
-        capacity_family_swap(v, sms, &cap))
+        capacity_family_swap(v, sms, &cap) || capacity_family_rowload(v, sms, &cap))
         return cap;
     return 0;
 }

@@ -272,7 +272,9 @@ typedef struct {
     int64_t sk_tiles;        /* tiles shared out by k-block */
     int32_t stage_cd;        /* always 0: no scratch copies of C or D are made (the epilogue reads
                                 C and writes D in place at any alignment) */
-    int32_t reserved;
+    int32_t row_load;        /* bit 0 (A) / bit 1 (B): the operand's rows, which tensor copies cannot
+                                address, are read by the kernel's own loader warps instead of
+                                being repacked (GEMM_TN_OPT_ROW_LOADER; pack_a / pack_b stay 0) */
 } gemm_tn_plan_t;
 
 GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int64_t batch,
@@ -308,6 +310,18 @@ GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int6
  *                                 the last wave idle and at most 8 contributors per split
  *                                 tile); 1: whenever the tiles do not divide evenly;
  *                                 -1: never.
+ *   GEMM_TN_OPT_GROUP_M           rasterisation group: consecutive work units walk this many
+ *                                 tile rows column by column (1-64), 0 = automatic.
+ *   GEMM_TN_OPT_SERPENTINE        1: every other wave of whole tiles walks K backwards, so it
+ *                                 starts on the k-blocks the wave before it loaded last;
+ *                                 -1: never; 0 (default): when the tiles span two or more
+ *                                 waves and A and B together hold 128 MB or more.
+ *   GEMM_TN_OPT_ROW_LOADER        1: K-major operands whose rows tensor copies cannot address
+ *                                 are read by the kernel's own loader warps (CTA-pair 256x256
+ *                                 and single-CTA 128x128 tiles, unswapped, no K slices)
+ *                                 instead of being repacked, so the call needs no scratch
+ *                                 for them; several times slower than the repack.  0 (default):
+ *                                 repack.
  * A forced setting that no compiled kernel supports for a problem is ignored.
  * Returns GEMM_ERR_INVALID_VALUE for an unknown option or an out-of-range value.
  */
@@ -320,7 +334,10 @@ enum {
     GEMM_TN_OPT_FORCE_SWAP = 6,
     GEMM_TN_OPT_FORCE_GENERIC_EPI = 7,
     GEMM_TN_OPT_FORCE_PACK = 8,
-    GEMM_TN_OPT_STREAM_K = 9
+    GEMM_TN_OPT_STREAM_K = 9,
+    GEMM_TN_OPT_GROUP_M = 10,
+    GEMM_TN_OPT_SERPENTINE = 11,
+    GEMM_TN_OPT_ROW_LOADER = 12
 };
 GEMM_TN_API gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value);
 GEMM_TN_API int64_t gemm_tn_f16_get_option(int32_t option);

@@ -87,7 +87,9 @@ def options(**kw):
              "force_splits": G.GEMM_TN_OPT_FORCE_SPLITS, "force_swap": G.GEMM_TN_OPT_FORCE_SWAP,
              "force_generic": G.GEMM_TN_OPT_FORCE_GENERIC_EPI, "force_pack": G.GEMM_TN_OPT_FORCE_PACK,
              "skip_first_load": G.GEMM_TN_OPT_SKIP_FIRST_LOAD, "timeout_ns": G.GEMM_TN_OPT_WAIT_TIMEOUT_NS,
-             "stream_k": G.GEMM_TN_OPT_STREAM_K}
+             "stream_k": G.GEMM_TN_OPT_STREAM_K, "group_m": G.GEMM_TN_OPT_GROUP_M,
+             "serpentine": G.GEMM_TN_OPT_SERPENTINE,
+             "row_loader": G.GEMM_TN_OPT_ROW_LOADER}
     old = {k: G.gemm_tn_f16_get_option(names[k]) for k in kw}
     try:
         for k, v in kw.items():

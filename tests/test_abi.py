@@ -240,7 +240,8 @@ def test_plan_forced_splits_use_the_reduction_kernel():
 def test_plan_ragged_packed_ld_repacks_operands_only():
     # A, B repacked; C read and D written where they are by the epilogue
     p = plan(4095, 3073, 2047, lda=2047, ldb=2047, ldc=3073, ldd=3073, beta=1.5)
-    assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["epi_tma"] == 0 and p["stage_cd"] == 0
+    assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["row_load"] == 0
+    assert p["epi_tma"] == 0 and p["stage_cd"] == 0
     assert p["workspace_bytes"] >= 2 * (4095 + 3073) * 2048
     G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_GENERIC_EPI, 1)
     try:
@@ -248,6 +249,31 @@ def test_plan_ragged_packed_ld_repacks_operands_only():
     finally:
         G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_GENERIC_EPI, 0)
     assert p["epi_tma"] == 0 and p["stage_cd"] == 0
+
+
+def test_plan_row_loader_option_reads_operand_rows_in_kernel():
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_ROW_LOADER, 1)
+    try:
+        # A, B read row by row by the loader warps (nothing repacked, no scratch)
+        p = plan(4095, 3073, 2047, lda=2047, ldb=2047, ldc=3073, ldd=3073, beta=1.5)
+        assert p["row_load"] == 3 and p["pack_a"] == 0 and p["pack_b"] == 0
+        assert p["epi_tma"] == 0 and p["stage_cd"] == 0 and p["workspace_bytes"] == 0
+        # only B misaligned: A still comes by TMA
+        p = plan(4096, 3072, 2047, lda=2048, ldb=2047, ldc=3072, ldd=3072, beta=1.5)
+        assert p["row_load"] == 2 and p["pack_a"] == 0 and p["pack_b"] == 0 and p["epi_tma"] == 1
+        # forced repack, or an epilogue with no row-loader variant: repacked to scratch
+        for opt in (G.GEMM_TN_OPT_FORCE_PACK, G.GEMM_TN_OPT_FORCE_GENERIC_EPI):
+            G.gemm_tn_f16_set_option(opt, 1)
+            try:
+                p = plan(4095, 3073, 2047, lda=2047, ldb=2047, ldc=3073, ldd=3073, beta=1.5)
+            finally:
+                G.gemm_tn_f16_set_option(opt, 0)
+            assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["row_load"] == 0
+        # swapped small-M problems have no row-loader variant either
+        p = plan(16, 3073, 2047, lda=2047, ldb=2047, ldc=3073, ldd=3073)
+        assert p["swap_ab"] == 1 and p["pack_a"] == 1 and p["pack_b"] == 1 and p["row_load"] == 0
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_ROW_LOADER, 0)
 
 
 def test_plan_score_batched_short_k():
@@ -259,7 +285,8 @@ def test_plan_score_batched_short_k():
 def test_plan_misaligned_pointer_forces_pack_only():
     # A, B repacked; C and D accessed in place by the epilogue's row words
     p = plan(1024, 1024, 1024, align=0)
-    assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["epi_tma"] == 0 and p["stage_cd"] == 0
+    assert p["pack_a"] == 1 and p["pack_b"] == 1 and p["row_load"] == 0
+    assert p["epi_tma"] == 0 and p["stage_cd"] == 0
     p = plan(1024, 1024, 1024, align=0, beta=1.0)
     assert p["epi_tma"] == 0 and p["stage_cd"] == 0
     # aligned D, misaligned C: the TMA epilogue at any size, nothing staged

@@ -1,6 +1,7 @@
-"""The GEMM launched as a programmatic dependent of the operand repack (operands whose
-rows TMA cannot address): its set-up overlaps the repack, and its loads must still see
-the repacked copies of operands that kernels earlier on the stream have just written.
+"""Operands whose rows TMA cannot address, rewritten by kernels earlier on the stream:
+either repacked, with the GEMM launched as a programmatic dependent of the repack (its
+set-up overlaps the repack, and its loads must still see the repacked copies), or read
+row by row by the GEMM's own loader warps, which must see the fresh rows.
 Several rounds of (overwrite A and B on the device, GEMM) are queued without any
 synchronisation in between; every round's D must match the oracle on that round's
 operands."""
@@ -15,9 +16,12 @@ from gpu_util import assert_close, assert_device_ok, options, to_dev, to_host, t
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("opts", [{}, {"force_bn": 512, "force_pair": 2}, {"stream_k": 1}],
-                         ids=["auto", "wide", "stream_k"])
-def test_rounds_of_fresh_operands_through_the_repack(opts):
+@pytest.mark.parametrize("opts,row_load", [({}, False), ({"force_pack": 1}, False), ({"force_bn": 512, "force_pair": 2}, False),
+                                           ({"stream_k": 1, "force_pack": 1}, False),
+                                           ({"force_bn": 128, "force_pair": 1, "row_loader": 1}, True),
+                                           ({"force_bn": 256, "force_pair": 2, "row_loader": 1}, True)],
+                         ids=["auto", "repack", "wide_repack", "stream_k_repack", "row_loader", "row_loader_pair"])
+def test_rounds_of_fresh_operands_through_the_repack(opts, row_load):
     t = torch()
     M, N, K, lda, ldb = 700, 1032, 520, 523, 521  # odd leading dimensions: A and B are repacked
     rounds = 4
@@ -30,7 +34,10 @@ def test_rounds_of_fresh_operands_through_the_repack(opts):
     outs = [t.empty(M * N, dtype=t.float16, device="cuda") for _ in range(rounds)]
     with options(**opts):
         plan = G.gemm_tn_f16_plan(M, N, K, 1, lda, ldb, N, N, 0, 0, 0, 0, 0.0, 15, 152)
-        assert plan["pack_a"] == 1 and plan["pack_b"] == 1
+        if not row_load:  # repacked copies, the GEMM a programmatic dependent of the repack
+            assert plan["pack_a"] == 1 and plan["pack_b"] == 1 and plan["row_load"] == 0
+        else:  # the GEMM's loader warps read the freshly written rows themselves
+            assert plan["pack_a"] == 0 and plan["pack_b"] == 0 and plan["row_load"] == 3
         t.cuda.synchronize()
         for r in range(rounds):
             dA.copy_(srcA[r])  # a kernel on the stream writes the operands ...

@@ -71,12 +71,26 @@ CASES = [
     ("streamk_swap_skinny", dict(M=16, N=1024, K=4096)),
     ("streamk_swap_beta", dict(M=40, N=2000, K=1000, alpha=0.5, beta=1.5, opts=dict(stream_k=1))),
     ("streamk_batched", dict(M=600, N=600, K=640, batch=3, opts=dict(stream_k=1))),
+    # serpentine K order: odd waves of whole tiles walk K backwards
+    ("serpentine_pair_waves", dict(M=3000, N=2900, K=700, alpha=0.5, beta=1.5,
+                                   opts=dict(serpentine=1, stream_k=-1, force_pair=2, force_bn=256))),
+    ("serpentine_single_waves", dict(M=2600, N=2000, K=330, opts=dict(serpentine=1, stream_k=-1, force_pair=1))),
+    ("serpentine_wide_streamk", dict(M=4608, N=4608, K=640, opts=dict(serpentine=1, stream_k=1, force_bn=512))),
+    ("serpentine_splitk", dict(M=300, N=1300, K=3000, opts=dict(serpentine=1, force_splits=3, force_pair=1))),
 ]
 
 
 @pytest.mark.parametrize("name,kw", CASES, ids=[c[0] for c in CASES])
 def test_parity(name, kw):
     run_problem(seed=zlib.crc32(name.encode()) % 1000, **kw)
+
+
+@pytest.mark.parametrize("serp", [1, -1])
+def test_serpentine_small_integers_bit_exact(serp):
+    """Reversed K order must not change an exact sum: several waves of pair tiles with
+    small-integer operands, bit for bit against the oracle."""
+    run_problem(2600, 2400, 512, dist="int", compare="exact", seed=31,
+                opts=dict(serpentine=serp, stream_k=-1, force_pair=2, force_bn=256))
 
 
 EXACT = [
