@@ -23,6 +23,7 @@ GEMM_ERR_UNSUPPORTED = 3
 GEMM_ERR_CUDA = 4
 GEMM_ERR_TIMEOUT = 5
 GEMM_ERR_WORKSPACE = 6
+GEMM_ERR_BOUNDS = 7
 
 GEMM_TN_OPT_WAIT_TIMEOUT_NS = 1
 GEMM_TN_OPT_SKIP_FIRST_LOAD = 2
@@ -36,11 +37,12 @@ GEMM_TN_OPT_STREAM_K = 9
 GEMM_TN_OPT_GROUP_M = 10
 GEMM_TN_OPT_SERPENTINE = 11
 GEMM_TN_OPT_ROW_LOADER = 12
+GEMM_TN_OPT_CHECK_TRIM_D = 13
 
 EXPORTED = ["gemm_tn_f16", "gemm_tn_f16_batched", "gemm_status_string", "gemm_tn_f16_last_device_error",
             "gemm_tn_f16_last_cuda_error", "gemm_tn_f16_shutdown", "gemm_tn_f16_version", "gemm_tn_f16_plan",
             "gemm_tn_f16_set_option", "gemm_tn_f16_get_option", "gemm_tn_f16_splitk_static", "gemm_f16", "transpose_f32", "transpose_f16", "gemm_f16_acc16",
-            "score_softmax_stats_f16", "gemm_tn_f16_host"]
+            "score_softmax_stats_f16", "gemm_tn_f16_host", "gemm_tn_f16_is_checked"]
 
 GEMM_K_MAJOR = 0
 GEMM_MN_MAJOR = 1
@@ -74,8 +76,14 @@ _lock = threading.Lock()
 _lib = None
 
 
+def checked_requested() -> bool:
+    """True when GEMM_TN_F16_CHECKED=1: this process loads the checked build (device-side
+    bounds checks on the kernels' own loads and stores) instead of the regular library."""
+    return os.environ.get("GEMM_TN_F16_CHECKED", "") == "1"
+
+
 def library_path() -> str:
-    return _build.LIB_PATH
+    return _build.LIB_PATH_CHECKED if checked_requested() else _build.LIB_PATH
 
 
 def load_library(build_if_missing: bool = True):
@@ -84,11 +92,12 @@ def load_library(build_if_missing: bool = True):
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.LIB_PATH
-        if not os.path.exists(path) or not _build.up_to_date():
+        checked = checked_requested()
+        path = library_path()
+        if not os.path.exists(path) or not _build.up_to_date(checked=checked):
             if not build_if_missing:
                 raise RuntimeError(f"{path} is missing; run dense_fp16_gemm_tn_gb300.build.build()")
-            _build.build()
+            _build.build(checked=checked)
         lib = ctypes.CDLL(path)
         vp, i64, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
         lib.gemm_tn_f16.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, f32, f32, vp]
@@ -106,6 +115,8 @@ def load_library(build_if_missing: bool = True):
         lib.gemm_tn_f16_shutdown.restype = None
         lib.gemm_tn_f16_version.argtypes = []
         lib.gemm_tn_f16_version.restype = ctypes.c_int
+        lib.gemm_tn_f16_is_checked.argtypes = []
+        lib.gemm_tn_f16_is_checked.restype = ctypes.c_int
         lib.gemm_tn_f16_plan.argtypes = [i64] * 12 + [f32, ctypes.c_uint32, ctypes.c_int32,
                                                        ctypes.POINTER(gemm_tn_plan_t)]
         lib.gemm_tn_f16_plan.restype = ctypes.c_int
@@ -238,6 +249,10 @@ def gemm_tn_f16_shutdown() -> None:
 
 def gemm_tn_f16_version() -> int:
     return load_library().gemm_tn_f16_version()
+
+
+def gemm_tn_f16_is_checked() -> int:
+    return load_library().gemm_tn_f16_is_checked()
 
 
 def gemm_tn_f16_plan(M, N, K, batch, lda, ldb, ldc, ldd, strideA, strideB, strideC, strideD,

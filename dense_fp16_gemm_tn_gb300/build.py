@@ -23,6 +23,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "gemm_tn_f16")
 LIB_PATH = os.path.join(PKG, "libgemm_tn_f16.so")
+# The checked build: the same sources with device-side bounds checks (-DGTN_CHECKED).
+BUILD_DIR_CHECKED = os.path.join(ROOT, "_build", "gemm_tn_f16_checked")
+LIB_PATH_CHECKED = os.path.join(PKG, "libgemm_tn_f16_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
@@ -45,24 +48,29 @@ def _deps():
         [os.path.join(INCLUDE, "gemm_tn_f16.h"), os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(checked: bool = False) -> bool:
+    lib = LIB_PATH_CHECKED if checked else LIB_PATH
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link the library; returns its path.  Raises on failure."""
-    if not force and up_to_date():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, checked: bool = False) -> str:
+    """Compile and link the library (or, with checked=True, its checked build); returns
+    its path.  Raises on failure."""
+    lib_path = LIB_PATH_CHECKED if checked else LIB_PATH
+    build_dir = BUILD_DIR_CHECKED if checked else BUILD_DIR
+    if not force and up_to_date(checked):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
     srcs = _sources()
+    extra = ["-DGTN_CHECKED"] if checked else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -74,14 +82,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for obj, log in results:
             sys.stderr.write(f"== {os.path.basename(obj)}\n{log}")
     objs = [o for o, _ in results]
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked="--checked" in sys.argv))

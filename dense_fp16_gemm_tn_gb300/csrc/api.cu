@@ -52,6 +52,7 @@ std::atomic<int64_t> g_opt_stream_k{0};
 std::atomic<int64_t> g_opt_group_m{0};
 std::atomic<int64_t> g_opt_serpentine{0};
 std::atomic<int64_t> g_opt_row_loader{0};
+std::atomic<int64_t> g_opt_check_trim_d{0};
 
 gemm_status_t cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -537,6 +538,12 @@ int64_t extent_bytes(int64_t rows, int64_t cols, int64_t ld, int64_t stride, int
     return 2 * ((batch - 1) * stride + (rows - 1) * ld + cols);
 }
 
+// Byte range of a matrix for the checked build's device-side bounds checks.
+Extent extent_of(const void* base, int64_t bytes) {
+    const uint64_t lo = static_cast<uint64_t>(reinterpret_cast<uintptr_t>(base));
+    return Extent{lo, lo + static_cast<uint64_t>(bytes > 0 ? bytes : 0)};
+}
+
 gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Problem& pr, float alpha,
                   cudaStream_t stream) {
     gemm_status_t st = validate(pr);
@@ -568,7 +575,11 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
 
     cudaError_t e;
     if (pr.K == 0) {
-        e = launch_scale(pr.M, pr.N, pr.batch, pr.beta, C, pr.ldc, pr.sC, D, pr.ldd, pr.sD, dev->sms, stream);
+        ReduceChecks chk = {};
+        chk.c = pr.beta != 0.0f ? extent_of(C, extent_bytes(pr.M, pr.N, pr.ldc, pr.sC, pr.batch)) : Extent{};
+        chk.d = extent_of(D, d_bytes - g_opt_check_trim_d.load());
+        chk.err = dev->err;
+        e = launch_scale(pr.M, pr.N, pr.batch, pr.beta, C, pr.ldc, pr.sC, D, pr.ldd, pr.sD, dev->sms, stream, chk);
         return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
     }
 
@@ -658,7 +669,9 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     int njobs = 0;
     if (pl.pub.pack_a) {
         void* dst = ws;
-        jobs[njobs++] = {A, p.lda, p.sA, dst, pl.ldo_a, a_rows(p), a_len(p), a_batched ? p.batch : 1};
+        jobs[njobs++] = {A, p.lda, p.sA, dst, pl.ldo_a, a_rows(p), a_len(p), a_batched ? p.batch : 1,
+                         extent_of(A, extent_bytes(a_rows(p), a_len(p), p.lda, p.sA, a_batched ? p.batch : 1)),
+                         extent_of(dst, pl.pack_a_bytes)};
         if (!encode_map(&mapPA, dst, a_len(p), a_rows(p), p.batch, pl.ldo_a, a_rows(p) * pl.ldo_a, a_batched, 64,
                         boxA)) {
             release();
@@ -667,7 +680,9 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     }
     if (pl.pub.pack_b) {
         void* dst = ws + pl.pack_a_bytes;
-        jobs[njobs++] = {B, p.ldb, p.sB, dst, pl.ldo_b, b_rows(p), b_len(p), b_batched ? p.batch : 1};
+        jobs[njobs++] = {B, p.ldb, p.sB, dst, pl.ldo_b, b_rows(p), b_len(p), b_batched ? p.batch : 1,
+                         extent_of(B, extent_bytes(b_rows(p), b_len(p), p.ldb, p.sB, b_batched ? p.batch : 1)),
+                         extent_of(dst, pl.pack_b_bytes)};
         if (!encode_map(&mapPB, dst, b_len(p), b_rows(p), p.batch, pl.ldo_b, b_rows(p) * pl.ldo_b, b_batched, 64,
                         boxB)) {
             release();
@@ -675,7 +690,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
         }
     }
     if (njobs > 0) {
-        e = launch_repack(jobs, njobs, dev->sms, stream);
+        e = launch_repack(jobs, njobs, dev->sms, stream, dev->err);
         if (e != cudaSuccess) { release(); return cuda_fail(e); }
     }
     mapA_op = swap ? mapPB : mapPA;
@@ -727,6 +742,12 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     kp.err = dev->err;
     kp.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
     kp.debug_skip_first_load = g_opt_skip_first_load.load() != 0 ? 1 : 0;
+    kp.ext_a = extent_of(A, extent_bytes(a_rows(p), a_len(p), p.lda, p.sA, a_batched ? p.batch : 1));
+    kp.ext_b = extent_of(B, extent_bytes(b_rows(p), b_len(p), p.ldb, p.sB, b_batched ? p.batch : 1));
+    kp.ext_c = p.beta != 0.0f ? extent_of(C, extent_bytes(p.M, p.N, p.ldc, p.sC, (p.batch > 1 && p.sC != 0) ? p.batch : 1))
+                              : Extent{};
+    kp.ext_d = extent_of(D, d_bytes - g_opt_check_trim_d.load());
+    kp.ext_w = extent_of(kp.W, pl.partial_bytes);
     kp.pdl = njobs > 0 ? 1 : 0;  // directly behind the repack launch
     if (pl.rl) {
         // row loader: the MMA's operands are the problem's A and B (never swapped)
@@ -755,8 +776,9 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
     e = launch_tc_variant(pl.var, mapA_op, mapB_op, mapC, mapD, kp, pl.pub.grid, stream, &grid);
     if (e != cudaSuccess) { release(); return cuda_fail(e); }
     if (pl.pub.splits > 1) {
+        const ReduceChecks chk = {kp.ext_w, kp.ext_c, kp.ext_d, dev->err};
         e = launch_splitk_reduce(kp.W, pl.pub.splits, p.M, p.N, p.batch, alpha, p.beta, C, p.ldc, p.sC, D, p.ldd,
-                                 p.sD, dev->sms, stream);
+                                 p.sD, dev->sms, stream, chk);
         if (e != cudaSuccess) { release(); return cuda_fail(e); }
     }
     release();
@@ -949,21 +971,25 @@ gemm_status_t run_softmax(const void* Q, int64_t ldq, int64_t strideQ, const voi
     RepackArgs jobs[2];
     int njobs = 0;
     if (pack_q) {
-        jobs[njobs++] = {Q, ldq, strideQ, ws, ldo, M, d, q_batched ? batch : 1};
+        jobs[njobs++] = {Q, ldq, strideQ, ws, ldo, M, d, q_batched ? batch : 1,
+                         extent_of(Q, extent_bytes(M, d, ldq, strideQ, q_batched ? batch : 1)),
+                         extent_of(ws, q_pack_bytes)};
         if (!encode_map(&mapQ, ws, d, M, batch, ldo, M * ldo, q_batched, 64, kSoftmaxTileM)) {
             release();
             return GEMM_ERR_UNSUPPORTED;
         }
     }
     if (pack_k) {
-        jobs[njobs++] = {K, ldk, strideK, ws + q_pack_bytes, ldo, N, d, k_batched ? batch : 1};
+        jobs[njobs++] = {K, ldk, strideK, ws + q_pack_bytes, ldo, N, d, k_batched ? batch : 1,
+                         extent_of(K, extent_bytes(N, d, ldk, strideK, k_batched ? batch : 1)),
+                         extent_of(ws + q_pack_bytes, k_pack_bytes)};
         if (!encode_map(&mapK, ws + q_pack_bytes, d, N, batch, ldo, N * ldo, k_batched, 64, key_box)) {
             release();
             return GEMM_ERR_UNSUPPORTED;
         }
     }
     if (njobs > 0) {
-        e = launch_repack(jobs, njobs, dev->sms, stream);
+        e = launch_repack(jobs, njobs, dev->sms, stream, dev->err);
         if (e != cudaSuccess) { release(); return cuda_fail(e); }
     }
 
@@ -1056,6 +1082,7 @@ const char* gemm_status_string(gemm_status_t s) {
         case GEMM_ERR_CUDA: return "CUDA runtime or driver error";
         case GEMM_ERR_TIMEOUT: return "device-side wait timed out";
         case GEMM_ERR_WORKSPACE: return "scratch memory unavailable";
+        case GEMM_ERR_BOUNDS: return "device-side bounds check failed (checked build)";
     }
     return "unknown status";
 }
@@ -1071,7 +1098,7 @@ gemm_status_t gemm_tn_f16_last_device_error(void) {
     if (word != 0) {
         const uint32_t zero = 0;
         if ((e = cudaMemcpy(dev->err, &zero, sizeof(zero), cudaMemcpyHostToDevice)) != cudaSuccess) return cuda_fail(e);
-        return (word >> 8) == 5u ? GEMM_ERR_TIMEOUT : GEMM_ERR_CUDA;
+        return (word >> 8) == 5u ? GEMM_ERR_TIMEOUT : (word >> 8) == 6u ? GEMM_ERR_BOUNDS : GEMM_ERR_CUDA;
     }
     return GEMM_OK;
 }
@@ -1099,6 +1126,8 @@ void gemm_tn_f16_shutdown(void) {
 }
 
 int gemm_tn_f16_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+int gemm_tn_f16_is_checked(void) { return kChecked ? 1 : 0; }
 
 gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int64_t batch, int64_t lda, int64_t ldb, int64_t ldc,
                                int64_t ldd, int64_t strideA, int64_t strideB, int64_t strideC, int64_t strideD,
@@ -1151,6 +1180,10 @@ gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value) {
             g_opt_serpentine = value;
             return GEMM_OK;
         case GEMM_TN_OPT_ROW_LOADER: g_opt_row_loader = value ? 1 : 0; return GEMM_OK;
+        case GEMM_TN_OPT_CHECK_TRIM_D:
+            if (value < 0 || value > 4096) return GEMM_ERR_INVALID_VALUE;
+            g_opt_check_trim_d = value;
+            return GEMM_OK;
 
     }
     return GEMM_ERR_INVALID_VALUE;
@@ -1170,6 +1203,7 @@ int64_t gemm_tn_f16_get_option(int32_t option) {
         case GEMM_TN_OPT_GROUP_M: return g_opt_group_m.load();
         case GEMM_TN_OPT_SERPENTINE: return g_opt_serpentine.load();
         case GEMM_TN_OPT_ROW_LOADER: return g_opt_row_loader.load();
+        case GEMM_TN_OPT_CHECK_TRIM_D: return g_opt_check_trim_d.load();
 
     }
     return -1;

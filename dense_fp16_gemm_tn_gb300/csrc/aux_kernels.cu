@@ -23,6 +23,7 @@ struct RepackJob {
     int64_t ld_src, stride_src;
     __half* dst;
     int64_t ldo, rows, K, batch;
+    Extent src_ext, dst_ext;
 };
 
 // The 16 bytes starting `shift` bytes (even, 0..14) into the 32-byte window w0..w7.
@@ -54,6 +55,7 @@ constexpr int kMaxRepackJobs = 2;
 struct RepackJobs {
     RepackJob j[kMaxRepackJobs];
     int64_t first_item[kMaxRepackJobs + 1];  // job i owns items [first_item[i], first_item[i + 1])
+    uint32_t* err;                           // device error word (checked build)
 };
 
 __global__ void __launch_bounds__(256, 4) repack_rows_kernel(const RepackJobs jobs) {
@@ -92,7 +94,16 @@ __global__ void __launch_bounds__(256, 4) repack_rows_kernel(const RepackJobs jo
                 const int32_t k0 = g * 8;
 #pragma unroll
                 for (int t = 0; t < 8; ++t) w[u][t] = 0;
-                if (g < groups && k0 < K) {
+                bool load_ok = g < groups && k0 < K;
+                if constexpr (kChecked) {
+                    // the halves of the row this group uses must lie inside the source matrix
+                    if (load_ok) {
+                        const uint64_t a = reinterpret_cast<uintptr_t>(src_row + k0);
+                        const uint64_t b = reinterpret_cast<uintptr_t>(src_row + (k0 + 8 < K ? k0 + 8 : K));
+                        load_ok = in_extent(a, b, jb.src_ext, jobs.err, CHK_REPACK_SRC);
+                    }
+                }
+                if (load_ok) {
                     const uint4 v0 = __ldg(row_blk + g);
                     w[u][0] = v0.x; w[u][1] = v0.y; w[u][2] = v0.z; w[u][3] = v0.w;
                     if (shift != 0 && k0 + reach < K) {
@@ -121,7 +132,8 @@ __global__ void __launch_bounds__(256, 4) repack_rows_kernel(const RepackJobs jo
                         out = make_uint4(o[0], o[1], o[2], o[3]);
                     }
                 }
-                *reinterpret_cast<uint4*>(dst_row + k0) = out;
+                if (chk_elem(reinterpret_cast<const uint4*>(dst_row + k0), jb.dst_ext, jobs.err, CHK_REPACK_DST))
+                    *reinterpret_cast<uint4*>(dst_row + k0) = out;
             }
         }
     }
@@ -132,7 +144,8 @@ __global__ void __launch_bounds__(256, 4) repack_rows_kernel(const RepackJobs jo
 // added in slice order.
 __global__ void splitk_reduce4_kernel(const float* __restrict__ W, int32_t splits, int64_t M, int64_t N,
                                       int64_t batch, float alpha, float beta, const __half* C, int64_t ldc,
-                                      int64_t strideC, __half* D, int64_t ldd, int64_t strideD) {
+                                      int64_t strideC, __half* D, int64_t ldd, int64_t strideD,
+                                      const ReduceChecks chk) {
     griddep_wait();  // launched as a dependent of the GEMM that writes W: its partials are visible
     const int64_t mn = M * N;
     const int64_t total = batch * mn / 4;
@@ -149,8 +162,11 @@ __global__ void splitk_reduce4_kernel(const float* __restrict__ W, int32_t split
         for (int32_t s0 = 0; s0 < splits; s0 += 8) {
             float4 v[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (s0 + u < splits) v[u] = __ldcs(w + (s0 + u) * step);
+            for (int u = 0; u < 8; ++u) {
+                v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (s0 + u < splits && chk_elem(w + (s0 + u) * step, chk.w, chk.err, CHK_REDUCE_W))
+                    v[u] = __ldcs(w + (s0 + u) * step);
+            }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 if (s0 + u < splits) {
@@ -164,8 +180,10 @@ __global__ void splitk_reduce4_kernel(const float* __restrict__ W, int32_t split
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             float x = alpha * acc[q];
-            if (beta != 0.0f) x = fmaf(beta, __half2float(C[b * strideC + m * ldc + n + q]), x);
-            D[b * strideD + m * ldd + n + q] = __float2half_rn(x);
+            const __half* ca = C + b * strideC + m * ldc + n + q;
+            if (beta != 0.0f && chk_elem(ca, chk.c, chk.err, CHK_REDUCE_C)) x = fmaf(beta, __half2float(*ca), x);
+            __half* da = D + b * strideD + m * ldd + n + q;
+            if (chk_elem(da, chk.d, chk.err, CHK_REDUCE_D)) *da = __float2half_rn(x);
         }
     }
 }
@@ -173,7 +191,8 @@ __global__ void splitk_reduce4_kernel(const float* __restrict__ W, int32_t split
 // D[b][m][n] = alpha * sum_{s<S} W[b][s][m][n] + beta * C[b][m][n]
 __global__ void splitk_reduce_kernel(const float* __restrict__ W, int32_t splits, int64_t M, int64_t N,
                                      int64_t batch, float alpha, float beta, const __half* C, int64_t ldc,
-                                     int64_t strideC, __half* D, int64_t ldd, int64_t strideD) {
+                                     int64_t strideC, __half* D, int64_t ldd, int64_t strideD,
+                                     const ReduceChecks chk) {
     griddep_wait();  // launched as a dependent of the GEMM that writes W: its partials are visible
     const int64_t mn = M * N;
     const int64_t total = batch * mn;
@@ -185,16 +204,19 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ W, int32_t splits
         const int64_t n = e % N;
         const float* w = W + b * splits * mn + e;
         float acc = 0.0f;
-        for (int32_t s = 0; s < splits; ++s) acc += w[s * mn];
+        for (int32_t s = 0; s < splits; ++s)
+            if (chk_elem(w + s * mn, chk.w, chk.err, CHK_REDUCE_W)) acc += w[s * mn];
         float x = alpha * acc;
-        if (beta != 0.0f) x = fmaf(beta, __half2float(C[b * strideC + m * ldc + n]), x);
-        D[b * strideD + m * ldd + n] = __float2half_rn(x);
+        const __half* ca = C + b * strideC + m * ldc + n;
+        if (beta != 0.0f && chk_elem(ca, chk.c, chk.err, CHK_REDUCE_C)) x = fmaf(beta, __half2float(*ca), x);
+        __half* da = D + b * strideD + m * ldd + n;
+        if (chk_elem(da, chk.d, chk.err, CHK_REDUCE_D)) *da = __float2half_rn(x);
     }
 }
 
 // D = beta * C (beta != 0) or D = 0.
 __global__ void scale_kernel(int64_t M, int64_t N, int64_t batch, float beta, const __half* C, int64_t ldc,
-                             int64_t strideC, __half* D, int64_t ldd, int64_t strideD) {
+                             int64_t strideC, __half* D, int64_t ldd, int64_t strideD, const ReduceChecks chk) {
     const int64_t mn = M * N;
     const int64_t total = batch * mn;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
@@ -204,8 +226,10 @@ __global__ void scale_kernel(int64_t M, int64_t N, int64_t batch, float beta, co
         const int64_t m = e / N;
         const int64_t n = e % N;
         float x = 0.0f;
-        if (beta != 0.0f) x = beta * __half2float(C[b * strideC + m * ldc + n]);
-        D[b * strideD + m * ldd + n] = __float2half_rn(x);
+        const __half* ca = C + b * strideC + m * ldc + n;
+        if (beta != 0.0f && chk_elem(ca, chk.c, chk.err, CHK_REDUCE_C)) x = beta * __half2float(*ca);
+        __half* da = D + b * strideD + m * ldd + n;
+        if (chk_elem(da, chk.d, chk.err, CHK_REDUCE_D)) *da = __float2half_rn(x);
     }
 }
 
@@ -217,9 +241,10 @@ static int grid_for(int64_t total, int threads, int sms) {
     return static_cast<int>(blocks);
 }
 
-cudaError_t launch_repack(const RepackArgs* ops, int count, int sms, cudaStream_t stream) {
+cudaError_t launch_repack(const RepackArgs* ops, int count, int sms, cudaStream_t stream, uint32_t* err) {
     if (count > kMaxRepackJobs) return cudaErrorInvalidValue;
     RepackJobs jobs = {};
+    jobs.err = err;
     constexpr int64_t kSpan = 32 * kRepackGroups;
     int64_t items = 0;
     for (int i = 0; i < kMaxRepackJobs; ++i) {
@@ -227,7 +252,7 @@ cudaError_t launch_repack(const RepackArgs* ops, int count, int sms, cudaStream_
         if (i < count) {
             const RepackArgs& o = ops[i];
             jobs.j[i] = {static_cast<const __half*>(o.src), o.ld_src, o.stride_src, static_cast<__half*>(o.dst),
-                         o.ldo, o.rows, o.K, o.batch};
+                         o.ldo, o.rows, o.K, o.batch, o.src_ext, o.dst_ext};
             items += o.batch * o.rows * ((o.ldo / 8 + kSpan - 1) / kSpan);
         }
     }
@@ -242,7 +267,7 @@ cudaError_t launch_repack(const RepackArgs* ops, int count, int sms, cudaStream_
 
 cudaError_t launch_splitk_reduce(const float* W, int32_t splits, int64_t M, int64_t N, int64_t batch, float alpha,
                                  float beta, const void* C, int64_t ldc, int64_t strideC, void* D, int64_t ldd,
-                                 int64_t strideD, int sms, cudaStream_t stream) {
+                                 int64_t strideD, int sms, cudaStream_t stream, const ReduceChecks& chk) {
     // A programmatic dependent of the GEMM before it on the stream: scheduled while that
     // GEMM runs, it waits for the GEMM's completion before reading the partials.
     cudaLaunchConfig_t cfg = {};
@@ -256,17 +281,19 @@ cudaError_t launch_splitk_reduce(const float* W, int32_t splits, int64_t M, int6
     if (N % 4 == 0) {
         cfg.gridDim = dim3(static_cast<unsigned>(grid_for(batch * M * N / 4, 256, sms)), 1, 1);
         return cudaLaunchKernelEx(&cfg, splitk_reduce4_kernel, W, splits, M, N, batch, alpha, beta,
-                                  static_cast<const __half*>(C), ldc, strideC, static_cast<__half*>(D), ldd, strideD);
+                                  static_cast<const __half*>(C), ldc, strideC, static_cast<__half*>(D), ldd, strideD,
+                                  chk);
     }
     cfg.gridDim = dim3(static_cast<unsigned>(grid_for(batch * M * N, 256, sms)), 1, 1);
     return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, W, splits, M, N, batch, alpha, beta,
-                              static_cast<const __half*>(C), ldc, strideC, static_cast<__half*>(D), ldd, strideD);
+                              static_cast<const __half*>(C), ldc, strideC, static_cast<__half*>(D), ldd, strideD, chk);
 }
 
 cudaError_t launch_scale(int64_t M, int64_t N, int64_t batch, float beta, const void* C, int64_t ldc,
-                         int64_t strideC, void* D, int64_t ldd, int64_t strideD, int sms, cudaStream_t stream) {
+                         int64_t strideC, void* D, int64_t ldd, int64_t strideD, int sms, cudaStream_t stream,
+                         const ReduceChecks& chk) {
     scale_kernel<<<grid_for(batch * M * N, 256, sms), 256, 0, stream>>>(
-        M, N, batch, beta, static_cast<const __half*>(C), ldc, strideC, static_cast<__half*>(D), ldd, strideD);
+        M, N, batch, beta, static_cast<const __half*>(C), ldc, strideC, static_cast<__half*>(D), ldd, strideD, chk);
     return cudaGetLastError();
 }
 

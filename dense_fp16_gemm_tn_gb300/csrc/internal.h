@@ -43,14 +43,21 @@ struct RepackArgs {
     int64_t ld_src, stride_src;
     void* dst;
     int64_t ldo, rows, K, batch;
+    Extent src_ext, dst_ext;  // byte ranges of source and copy (checked build)
 };
-// Repacks up to two operands in one launch.
-cudaError_t launch_repack(const RepackArgs* ops, int count, int sms, cudaStream_t stream);
+// Repacks up to two operands in one launch; `err` is the device error word (checked build).
+cudaError_t launch_repack(const RepackArgs* ops, int count, int sms, cudaStream_t stream, uint32_t* err);
+// Byte ranges of the partial sums, C and D for the checked build's bounds checks.
+struct ReduceChecks {
+    Extent w, c, d;
+    uint32_t* err;
+};
 cudaError_t launch_splitk_reduce(const float* W, int32_t splits, int64_t M, int64_t N, int64_t batch, float alpha,
                                  float beta, const void* C, int64_t ldc, int64_t strideC, void* D, int64_t ldd,
-                                 int64_t strideD, int sms, cudaStream_t stream);
+                                 int64_t strideD, int sms, cudaStream_t stream, const ReduceChecks& chk);
 cudaError_t launch_scale(int64_t M, int64_t N, int64_t batch, float beta, const void* C, int64_t ldc,
-                         int64_t strideC, void* D, int64_t ldd, int64_t strideD, int sms, cudaStream_t stream);
+                         int64_t strideC, void* D, int64_t ldd, int64_t strideD, int sms, cudaStream_t stream,
+                         const ReduceChecks& chk);
 
 // Fused score + softmax statistics kernel (score_softmax.cu).
 constexpr int kSoftmaxTileM = 128;  // query rows per work unit

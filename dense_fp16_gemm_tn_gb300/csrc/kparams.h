@@ -3,6 +3,8 @@
 
 #include <cstdint>
 
+#include "checked.h"
+
 namespace gtn {
 
 enum EpiMode : int {
@@ -85,6 +87,9 @@ struct KParams {
     int64_t rl_stride[2];
     int32_t rl_on[2];
     uint32_t tma_tx;  // bytes TMA brings per stage (both CTAs of a pair), for EPI_RL variants
+    // Byte ranges of the problem's A, B, C, D and of the split-K partial sums W, for the
+    // checked build's device-side bounds checks (checked.h); unused otherwise.
+    Extent ext_a, ext_b, ext_c, ext_d, ext_w;
     // EPI_PARTIAL: 1 when the tmD slot holds a tensor map of W (fp32, [batch * splits][M][N],
     // boxes of 32 rows x 32 columns, 128-byte swizzle), so partials are stored by TMA.
     int32_t w_tma;

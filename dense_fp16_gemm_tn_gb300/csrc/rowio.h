@@ -18,6 +18,13 @@
 
 namespace gtn {
 
+// Checker of a row segment [a, b) (byte addresses) before it is read or written: the
+// default accepts everything; the checked build passes one that tests the range against
+// the matrix's extent (checked.h).  A rejected segment is neither read nor written.
+struct NoCheck {
+    GTN_ROWIO bool operator()(uintptr_t, uintptr_t) const { return true; }
+};
+
 // (lo >> 16) | (hi << 16): the upper half of lo followed by the lower half of hi.
 GTN_ROWIO uint32_t join_halves(uint32_t lo, uint32_t hi) { return (lo >> 16) | (hi << 16); }
 
@@ -87,10 +94,13 @@ GTN_ROWIO void store_part16(uintptr_t wa, uint32_t lo, uint32_t hi, uint32_t w0,
 // The nine aligned words that cover halves src[0..63].  Only words holding at least one
 // of the first `valid` halves are read (so no read leaves the pages those elements live
 // on); the others are zero.  Returns the offset of src in its first word, in halves.
-GTN_ROWIO uint32_t load_cover64(const uint16_t* src, int valid, uint32_t (&v)[36]) {
+// The segment [src, src + valid) goes through `chk` first; if it is rejected nothing is
+// read and all nine words are zero.
+template <class Chk = NoCheck>
+GTN_ROWIO uint32_t load_cover64(const uint16_t* src, int valid, uint32_t (&v)[36], const Chk& chk = Chk()) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(src);
     const uintptr_t base = a & ~uintptr_t(15);
-    const bool any = valid > 0;
+    const bool any = valid > 0 && chk(a, a + 2u * static_cast<uint32_t>(valid));
     const uintptr_t end = a + 2u * static_cast<uint32_t>(any ? valid : 0);
 #pragma unroll
     for (int q = 0; q < 9; ++q) {
@@ -140,11 +150,15 @@ GTN_ROWIO void place_row64(uint32_t sh, const uint32_t (&o)[32], uint32_t (&z)[3
 // Writes the first `valid` (0..64) of the 64 halves in o (32 words, low half first) to
 // dst: place_row64 puts them in the covering words; whole words go out as 16-byte
 // stores, the two edge words in aligned pieces (store_part16).
-GTN_ROWIO void store_row64(uint16_t* dst, int valid, const uint32_t (&o)[32]) {
+// The segment [dst, dst + valid) goes through `chk` first; if it is rejected nothing is
+// written.
+template <class Chk = NoCheck>
+GTN_ROWIO void store_row64(uint16_t* dst, int valid, const uint32_t (&o)[32], const Chk& chk = Chk()) {
     if (valid <= 0) return;
     const uintptr_t a = reinterpret_cast<uintptr_t>(dst);
     const uintptr_t base = a & ~uintptr_t(15);
     const uintptr_t end = a + 2u * static_cast<uint32_t>(valid);
+    if (!chk(a, end)) return;
     uint32_t z[36];
     place_row64(static_cast<uint32_t>(a - base) >> 1, o, z);
 #pragma unroll

@@ -139,9 +139,19 @@ extern "C" GEMM_TN_API gemm_status_t gemm_tn_f16_splitk_static(const void* A, in
     StaticDevice* dev = nullptr;
     gemm_status_t st = static_device(&dev);
     if (st != GEMM_OK) return st;
+    // byte ranges for the checked build's device-side bounds checks
+    auto ext = [](const void* b, int64_t bytes) {
+        const uint64_t lo = static_cast<uint64_t>(reinterpret_cast<uintptr_t>(b));
+        return Extent{lo, lo + static_cast<uint64_t>(bytes)};
+    };
+    ReduceChecks chk = {};
+    chk.c = beta != 0.0f ? ext(C, 2 * ((M - 1) * ldc + N)) : Extent{};
+    chk.d = ext(D, d_bytes);
+    chk.err = dev->err;
     if (K == 0) {
-        return launch_scale(M, N, 1, beta, C, ldc, 0, D, ldd, 0, dev->sms, stream) == cudaSuccess ? GEMM_OK
-                                                                                                  : GEMM_ERR_CUDA;
+        return launch_scale(M, N, 1, beta, C, ldc, 0, D, ldd, 0, dev->sms, stream, chk) == cudaSuccess
+                   ? GEMM_OK
+                   : GEMM_ERR_CUDA;
     }
 
     // ---- plan: split-K over 128-row tiles; operands swapped when M is small
@@ -198,11 +208,17 @@ extern "C" GEMM_TN_API gemm_status_t gemm_tn_f16_splitk_static(const void* A, in
     kp.W = dev->scratch;
     kp.err = dev->err;
     kp.timeout_ns = 2000000000ull;
+    kp.ext_a = ext(swap ? B : A, 2 * ((rows_a - 1) * (swap ? ldb : lda) + K));
+    kp.ext_b = ext(swap ? A : B, 2 * ((rows_b - 1) * (swap ? lda : ldb) + K));
+    kp.ext_c = chk.c;
+    kp.ext_d = chk.d;
+    kp.ext_w = ext(dev->scratch, s * M * N * 4);
+    chk.w = kp.ext_w;
 
     int64_t grid = 0;
     if (launch_tc_variant(v, mapA, mapB, mapA, mapA, kp, dev->sms, stream, &grid) != cudaSuccess) return GEMM_ERR_CUDA;
     if (launch_splitk_reduce(dev->scratch, static_cast<int32_t>(s), M, N, 1, alpha, beta, C, ldc, 0, D, ldd, 0,
-                             dev->sms, stream) != cudaSuccess)
+                             dev->sms, stream, chk) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return GEMM_OK;
 }

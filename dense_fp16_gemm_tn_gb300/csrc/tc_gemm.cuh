@@ -573,7 +573,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         valid = static_cast<int>(p.K - k0 < Cfg::BK ? p.K - k0 : Cfg::BK);
                         src = c.row + k0;
                     }
-                    return load_cover64(src, valid, v);
+                    if (isA) return load_cover64(src, valid, v, GTN_ROW_CHECK(p.ext_a, p.err, CHK_RL_A));
+                    return load_cover64(src, valid, v, GTN_ROW_CHECK(p.ext_b, p.err, CHK_RL_B));
                 };
                 const uint32_t sbase_op = isA ? sA : sB;
                 const uint32_t stage_bytes = isA ? Cfg::A_BYTES : Cfg::B_BYTES;
@@ -671,7 +672,10 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const __half* src = static_cast<const __half*>(p.C) + static_cast<int64_t>(w.b) * p.strideC + col;
 #pragma unroll
                 for (int r = 0; r < 32; ++r)
-                    dst[r] = (col_ok && arow0 + r < p.M) ? src[(arow0 + r) * p.ldc] : __ushort_as_half(0);
+                    dst[r] = (col_ok && arow0 + r < p.M &&
+                              chk_elem(src + (arow0 + r) * p.ldc, p.ext_c, p.err, CHK_EPI_C_ELEM))
+                                 ? src[(arow0 + r) * p.ldc]
+                                 : __ushort_as_half(0);
             };
             if constexpr (EB == EPI_GENERIC) {
                 if (use_c && !partial) load_c_chunk(0, cnext);
@@ -709,7 +713,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     valid = static_cast<int>(p.N - col0 < 64 ? p.N - col0 : 64);
                     src += static_cast<int64_t>(w.b) * p.strideC + row * p.ldc + col0;
                 }
-                c_sh = load_cover64(reinterpret_cast<const uint16_t*>(src), valid, ccover);
+                c_sh = load_cover64(reinterpret_cast<const uint16_t*>(src), valid, ccover,
+                                    GTN_ROW_CHECK(p.ext_c, p.err, CHK_EPI_C_ROW));
             };
             if constexpr (EPI == EPI_TMA_CG || EPI == EPI_VEC) {
                 if (!partial && p.beta != 0.0f) prefetch_cg(0);
@@ -842,7 +847,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         const int64_t col0 = acol0 + c * 64;
                         const int valid =
                             (row < p.M && col0 < p.N) ? static_cast<int>(p.N - col0 < 64 ? p.N - col0 : 64) : 0;
-                        store_row64(reinterpret_cast<uint16_t*>(drow + col0), valid, o);
+                        store_row64(reinterpret_cast<uint16_t*>(drow + col0), valid, o,
+                                    GTN_ROW_CHECK(p.ext_d, p.err, CHK_EPI_D_ROW));
                     }
                 } else if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) {
                     auto fetch64 = [&](int c, uint32_t (&v0)[32], uint32_t (&v1)[32]) {
@@ -1057,7 +1063,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                     if (row < p.M) {
                                         float x = p.alpha * T[r * 33 + lane];
                                         if (use_c) x = fmaf(p.beta, __half2float(ccur[r]), x);
-                                        dst[row * p.ldd] = __float2half_rn(x);
+                                        if (chk_elem(dst + row * p.ldd, p.ext_d, p.err, CHK_EPI_D_ELEM))
+                                            dst[row * p.ldd] = __float2half_rn(x);
                                     }
                                 }
                             } else {
@@ -1065,7 +1072,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll 8
                                 for (int r = 0; r < 32; ++r) {
                                     const int64_t row = arow0 + r;
-                                    if (row < p.M) Wp[row * p.N] = T[r * 33 + lane];
+                                    if (row < p.M && chk_elem(Wp + row * p.N, p.ext_w, p.err, CHK_EPI_W))
+                                        Wp[row * p.N] = T[r * 33 + lane];
                                 }
                             }
                         }
@@ -1092,26 +1100,27 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                                 for (int j = 0; j < 16; ++j) {
                                     const int64_t m = acol0 + c * 16 + j;
-                                    cv[j] = (use_c && m < p.M)
-                                                ? Cp[static_cast<int64_t>(w.b) * p.strideC + m * p.ldc + n]
+                                    const __half* ca = Cp + static_cast<int64_t>(w.b) * p.strideC + m * p.ldc + n;
+                                    cv[j] = (use_c && m < p.M && chk_elem(ca, p.ext_c, p.err, CHK_EPI_C_ELEM))
+                                                ? *ca
                                                 : __ushort_as_half(0);
                                 }
 #pragma unroll
                                 for (int j = 0; j < 16; ++j) {
                                     const int64_t m = acol0 + c * 16 + j;
-                                    if (m < p.M) {
+                                    __half* da = Dp + static_cast<int64_t>(w.b) * p.strideD + m * p.ldd + n;
+                                    if (m < p.M && chk_elem(da, p.ext_d, p.err, CHK_EPI_D_ELEM)) {
                                         float x = p.alpha * __uint_as_float(v[j]);
                                         if (use_c) x = fmaf(p.beta, __half2float(cv[j]), x);
-                                        Dp[static_cast<int64_t>(w.b) * p.strideD + m * p.ldd + n] = __float2half_rn(x);
+                                        *da = __float2half_rn(x);
                                     }
                                 }
                             } else {
 #pragma unroll
                                 for (int j = 0; j < 16; ++j) {
                                     const int64_t m = acol0 + c * 16 + j;
-                                    if (m < p.M)
-                                        p.W[((static_cast<int64_t>(w.b) * p.splits + w.split) * p.M + m) * p.N + n] =
-                                            __uint_as_float(v[j]);
+                                    float* wa = p.W + ((static_cast<int64_t>(w.b) * p.splits + w.split) * p.M + m) * p.N + n;
+                                    if (m < p.M && chk_elem(wa, p.ext_w, p.err, CHK_EPI_W)) *wa = __uint_as_float(v[j]);
                                 }
                             }
                         }

@@ -80,7 +80,9 @@ typedef enum {
     GEMM_ERR_UNSUPPORTED = 3,   /* device is not sm_103 / sm_100 class, or sizes beyond limits */
     GEMM_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed (see gemm_tn_f16_last_cuda_error) */
     GEMM_ERR_TIMEOUT = 5,       /* a device-side wait ran past its limit (device error word) */
-    GEMM_ERR_WORKSPACE = 6      /* scratch memory could not be obtained */
+    GEMM_ERR_WORKSPACE = 6,     /* scratch memory could not be obtained */
+    GEMM_ERR_BOUNDS = 7         /* checked build only: a kernel's own load or store fell outside the
+                                   matrix it belongs to and was skipped (device error word) */
 } gemm_status_t;
 
 /*
@@ -241,6 +243,18 @@ GEMM_TN_API void gemm_tn_f16_shutdown(void);
 GEMM_TN_API int gemm_tn_f16_version(void);
 
 /*
+ * 1 for the checked build (libgemm_tn_f16_checked.so, compiled with device-side bounds
+ * checks), 0 for the regular one.  In the checked build every load and store the
+ * kernels issue themselves -- C and D rows or elements in the epilogues, rows read by
+ * the row loader, the repack of misaligned operands, the split-K sum, the K == 0
+ * scale -- is tested against the byte range of its matrix (derived from the pointer,
+ * sizes, leading dimension and batch stride of the call); one outside is skipped and
+ * reported by gemm_tn_f16_last_device_error() as GEMM_ERR_BOUNDS.  Tensor copies are
+ * bounded by their tensor maps.  A debugging aid: the checks cost time.
+ */
+GEMM_TN_API int gemm_tn_f16_is_checked(void);
+
+/*
  * Host-only planning (no CUDA call; safe without a GPU).  Describes the
  * kernel the library would launch for a problem on a device with `num_sms`
  * streaming multiprocessors.  `align_flags` bit i set means operand i
@@ -316,6 +330,10 @@ GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int6
  *                                 starts on the k-blocks the wave before it loaded last;
  *                                 -1: never; 0 (default): when the tiles span two or more
  *                                 waves and A and B together hold 128 MB or more.
+ *   GEMM_TN_OPT_CHECK_TRIM_D      checked build, testing only: bytes (0-4096) taken off the end
+ *                                 of D's range in the device-side checks, so that the last
+ *                                 stores of a call are reported (GEMM_ERR_BOUNDS) and skipped.
+ *                                 No effect in the regular build.
  *   GEMM_TN_OPT_ROW_LOADER        1: K-major operands whose rows tensor copies cannot address
  *                                 are read by the kernel's own loader warps (CTA-pair 256x256
  *                                 and single-CTA 128x128 tiles, unswapped, no K slices)
@@ -337,7 +355,8 @@ enum {
     GEMM_TN_OPT_STREAM_K = 9,
     GEMM_TN_OPT_GROUP_M = 10,
     GEMM_TN_OPT_SERPENTINE = 11,
-    GEMM_TN_OPT_ROW_LOADER = 12
+    GEMM_TN_OPT_ROW_LOADER = 12,
+    GEMM_TN_OPT_CHECK_TRIM_D = 13
 };
 GEMM_TN_API gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value);
 GEMM_TN_API int64_t gemm_tn_f16_get_option(int32_t option);

@@ -36,12 +36,27 @@ def test_every_declared_symbol_is_exported():
     assert exported == set(names), exported ^ set(names)
 
 
+def test_checked_build_exports_the_same_symbols():
+    """The checked build (device-side bounds checks) is the same library: same exports,
+    and it says it is the checked one; the regular build says it is not."""
+    path = B.build(checked=True)
+    assert path == B.LIB_PATH_CHECKED and path != B.LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported == set(declared_functions())
+    lib = ctypes.CDLL(path)
+    lib.gemm_tn_f16_is_checked.restype = ctypes.c_int
+    assert lib.gemm_tn_f16_is_checked() == 1
+    assert G.gemm_tn_f16_is_checked() == (1 if G.checked_requested() else 0)
+    assert G.gemm_status_string(G.GEMM_ERR_BOUNDS).startswith("device-side bounds check")
+
+
 def test_built_for_sm103a_only():
     assert B.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
 def test_status_strings_and_version():
-    for s in range(7):
+    for s in range(8):
         assert G.gemm_status_string(s)
     assert "unknown" in G.gemm_status_string(99)
     assert G.gemm_tn_f16_version() >= 10000

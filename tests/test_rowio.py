@@ -3,7 +3,8 @@ compiled for the host with g++: for every offset of the row in its 16-byte word 
 every length 0..64, stores write exactly the row's elements (guard bytes around them
 untouched), loads read only whole aligned words that hold at least one of the row's
 elements, and the realigned values are the row's values; a load at one alignment and a
-store at another move a row unchanged."""
+store at another move a row unchanged; the checker hook of the checked build sees the
+row segment and, when it rejects it, nothing is read or written."""
 import os
 import shutil
 import subprocess
@@ -71,6 +72,40 @@ int main() {
                 const bool in = i >= off2 && i < off2 + valid;
                 const uint16_t want = in ? src[off + (i - off2)] : 0x5555;
                 CHECK(buf[i] == want, "round trip off %d -> %d valid %d: buf[%d]", off, off2, valid, i);
+            }
+        }
+    }
+    // the checker hook of the checked build: it sees exactly the row segment, and a
+    // rejected segment is neither read nor written
+    struct Rec {
+        bool accept;
+        mutable uintptr_t lo = 0, hi = 0;
+        bool operator()(uintptr_t a, uintptr_t b) const { lo = a; hi = b; return accept; }
+    };
+    for (int off = 64; off < 64 + 16; ++off) {
+        for (int valid = 1; valid <= 64; valid += 9) {
+            for (int acc = 0; acc < 2; ++acc) {
+                ++cases;
+                Rec chk{acc != 0};
+                g_reads.clear();
+                uint32_t v[36];
+                load_cover64(src + off, valid, v, chk);
+                const uintptr_t a = reinterpret_cast<uintptr_t>(src + off);
+                CHECK(chk.lo == a && chk.hi == a + 2u * valid, "checker saw the wrong load segment");
+                if (!acc) {
+                    CHECK(g_reads.empty(), "rejected load off %d valid %d still read memory", off, valid);
+                    bool zero = true;
+                    for (int q = 0; q < 36; ++q) zero = zero && v[q] == 0;
+                    CHECK(zero, "rejected load returned data");
+                }
+                for (int i = 0; i < 1024; ++i) buf[i] = 0xAAAA;
+                Rec chk2{acc != 0};
+                store_row64(buf + off, valid, o, chk2);
+                const uintptr_t d = reinterpret_cast<uintptr_t>(buf + off);
+                CHECK(chk2.lo == d && chk2.hi == d + 2u * valid, "checker saw the wrong store segment");
+                int changed = 0;
+                for (int i = 0; i < 1024; ++i) changed += buf[i] != 0xAAAA;
+                CHECK(changed == (acc ? valid : 0), "store off %d valid %d accept %d changed %d", off, valid, acc, changed);
             }
         }
     }
