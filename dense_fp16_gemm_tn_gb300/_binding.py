@@ -38,6 +38,7 @@ GEMM_TN_OPT_GROUP_M = 10
 GEMM_TN_OPT_SERPENTINE = 11
 GEMM_TN_OPT_ROW_LOADER = 12
 GEMM_TN_OPT_CHECK_TRIM_D = 13
+GEMM_TN_OPT_K_CLUSTER = 14
 
 EXPORTED = ["gemm_tn_f16", "gemm_tn_f16_batched", "gemm_status_string", "gemm_tn_f16_last_device_error",
             "gemm_tn_f16_last_cuda_error", "gemm_tn_f16_shutdown", "gemm_tn_f16_version", "gemm_tn_f16_plan",
@@ -66,7 +67,7 @@ class gemm_tn_plan_t(ctypes.Structure):
                 ("pack_b", ctypes.c_int32), ("units", ctypes.c_int64), ("grid", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("stream_k", ctypes.c_int32), ("sk_maxc", ctypes.c_int32),
                 ("dp_tiles", ctypes.c_int64), ("sk_tiles", ctypes.c_int64), ("stage_cd", ctypes.c_int32),
-                ("row_load", ctypes.c_int32)]
+                ("row_load", ctypes.c_int32), ("k_cluster", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

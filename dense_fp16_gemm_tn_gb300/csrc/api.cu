@@ -53,6 +53,7 @@ std::atomic<int64_t> g_opt_group_m{0};
 std::atomic<int64_t> g_opt_serpentine{0};
 std::atomic<int64_t> g_opt_row_loader{0};
 std::atomic<int64_t> g_opt_check_trim_d{0};
+std::atomic<int64_t> g_opt_k_cluster{0};
 
 gemm_status_t cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -240,6 +241,7 @@ struct Plan {
     int64_t sk_iters;
     int group_m;
     int32_t rl, rl_a, rl_b;  // row-loader variant; A / B read by its loader warps (not repacked)
+    int32_t ck;              // cluster K split: the two CTAs of a cluster take the two halves of K
 };
 
 bool operand_tma_ok(bool aligned16, int64_t ld, int64_t stride, int64_t batch) {
@@ -316,7 +318,8 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
         const int64_t sk = tiles - dp;
         const int64_t I = sk * kb;
         TcVariant skv;
-        if (I >= Gs && find_tc_variant(pl.var.bn, pl.var.pair, pl.epi | (pl.rl ? EPI_RL : 0), 1, &skv)) {
+        if (I >= Gs && find_tc_variant(pl.var.bn, pl.var.pair, pl.epi | (pl.rl ? EPI_RL : 0) | (pl.ck ? EPI_CK : 0), 1,
+                                       &skv)) {
             auto owner = [&](int64_t i) { return ((i + 1) * Gs - 1) / I; };
             int64_t maxc = 1;
             for (int64_t t = 0; t < sk; ++t) maxc = std::max(maxc, owner((t + 1) * kb - 1) - owner(t * kb) + 1);
@@ -336,9 +339,11 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
             }
         }
     }
-    find_tc_variant(pl.var.bn, pl.var.pair, pl.epi | (pl.rl ? EPI_RL : 0), pub.stream_k, &pl.var);
+    find_tc_variant(pl.var.bn, pl.var.pair, pl.epi | (pl.rl ? EPI_RL : 0) | (pl.ck ? EPI_CK : 0), pub.stream_k,
+                    &pl.var);
+    const int cl = pl.ck ? 2 : pair;  // CTAs per cluster
     pub.units = pub.stream_k ? pub.dp_tiles : tiles * pub.splits;
-    pub.grid = pub.stream_k ? sk_groups * pair : std::min<int64_t>(pub.units, G) * pair;
+    pub.grid = pub.stream_k ? sk_groups * cl : std::min<int64_t>(pub.units, G) * cl;
     pub.workspace_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes;
 }
 
@@ -451,6 +456,15 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
                 splits = static_cast<int>(std::min<int64_t>({32, kb / 8, slots / tsw}));
         }
     }
+    // Two K halves of a swapped tile on the two CTAs of a cluster, the second half's partial
+    // sum added by the first CTA through distributed shared memory: one launch and no scratch
+    // where two K slices and a separate sum kernel would run (the 16 x 8192 x 8192 workload).
+    const int64_t fck = g_opt_k_cluster.load();
+    if (swap && fsplit == 0 && (fck > 0 || (fck == 0 && splits == 2)) && kb >= 2 &&
+        find_tc_variant(bn, 1, EPI_SWAP | EPI_CK, 0, nullptr)) {
+        splits = 1;
+        pl.ck = 1;
+    }
 
     // D rows TMA cannot address are written by the epilogue itself, each thread its row,
     // through the aligned 16-byte words that cover each row segment (EPI_VEC); C of any
@@ -471,7 +485,9 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
 
     TcVariant v;
     if (bn == 512 && !find_tc_variant(bn, pair, epi, 0, nullptr)) bn = 256;  // 512 columns: CTA pairs, TMA epilogues
-    if (!find_tc_variant(bn, pair, epi, 0, &v)) {
+    if (pl.ck) {
+        find_tc_variant(bn, 1, EPI_SWAP | EPI_CK, 0, &v);
+    } else if (!find_tc_variant(bn, pair, epi, 0, &v)) {
         // Fall back to the single-CTA variant of the same epilogue.
         pair = 1;
         if (!find_tc_variant(bn, pair, epi, 0, &v)) {
@@ -497,6 +513,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
         }
     }
     pub.row_load = (pl.rl_a ? 1 : 0) | (pl.rl_b ? 2 : 0);
+    pub.k_cluster = pl.ck;
     pl.var = v;
     pl.epi = epi;
     pl.rows_a = rows_a;
@@ -524,7 +541,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     pl.pack_a_bytes = pub.pack_a ? round_up(nba * a_rows(pr) * pl.ldo_a * 2, 256) : 0;
     pl.pack_b_bytes = pub.pack_b ? round_up(nbb * b_rows(pr) * pl.ldo_b * 2, 256) : 0;
     pl.partial_bytes = splits > 1 ? round_up(pr.batch * splits * pr.M * pr.N * 4, 256) : 0;
-    plan_stream_k(pr, pl, slots / pair);
+    plan_stream_k(pr, pl, slots / (pl.ck ? 2 : pair));
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -648,7 +665,7 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
         if (cap <= 0) cap = dev->sms;
         dev->capacity[pl.var.index] = cap;
     }
-    plan_stream_k(p, pl, cap / pl.var.pair);
+    plan_stream_k(p, pl, cap / (pl.ck ? 2 : pl.var.pair));
 
     const int64_t ws_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes;
     uint8_t* ws = nullptr;
@@ -1184,6 +1201,10 @@ gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value) {
             if (value < 0 || value > 4096) return GEMM_ERR_INVALID_VALUE;
             g_opt_check_trim_d = value;
             return GEMM_OK;
+        case GEMM_TN_OPT_K_CLUSTER:
+            if (value < -1 || value > 1) return GEMM_ERR_INVALID_VALUE;
+            g_opt_k_cluster = value;
+            return GEMM_OK;
 
     }
     return GEMM_ERR_INVALID_VALUE;
@@ -1204,6 +1225,7 @@ int64_t gemm_tn_f16_get_option(int32_t option) {
         case GEMM_TN_OPT_SERPENTINE: return g_opt_serpentine.load();
         case GEMM_TN_OPT_ROW_LOADER: return g_opt_row_loader.load();
         case GEMM_TN_OPT_CHECK_TRIM_D: return g_opt_check_trim_d.load();
+        case GEMM_TN_OPT_K_CLUSTER: return g_opt_k_cluster.load();
 
     }
     return -1;

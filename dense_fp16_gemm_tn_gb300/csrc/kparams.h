@@ -24,6 +24,11 @@ enum EpiMode : int {
 // rows of operands TMA cannot address (K-major, any 2-byte alignment) through the aligned
 // 16-byte words that cover them and write the swizzled shared-memory image themselves.
 constexpr int EPI_RL = 0x100;
+// Variant flag: the two CTAs of a cluster take the two halves of K of the same swapped
+// tile; the second CTA's fp32 partial sum goes into the first CTA's shared memory
+// (distributed shared memory), which adds it and writes D -- split-K in one launch,
+// with no scratch in global memory.
+constexpr int EPI_CK = 0x200;
 
 #ifdef __CUDACC__
 #define GTN_HD __host__ __device__
@@ -39,6 +44,7 @@ GTN_HD constexpr int epi_base(int epi) {
 }
 GTN_HD constexpr bool epi_acc16(int epi) { return epi_mode(epi) == EPI_TMA_A16 || epi_mode(epi) == EPI_GENERIC_A16; }
 GTN_HD constexpr bool epi_rl(int epi) { return (epi & EPI_RL) != 0; }
+GTN_HD constexpr bool epi_ck(int epi) { return (epi & EPI_CK) != 0; }
 
 struct KParams {
     // Tensor-core view: the MMA's A operand has rows_a rows, its B operand rows_b rows.

@@ -68,6 +68,8 @@ template <int BN, int PAIR, int STAGES, int EPIX>
 struct TileCfg {
     static constexpr int EPI = epi_mode(EPIX);   // epilogue mode
     static constexpr bool RL = epi_rl(EPIX);     // row-loader warps for operands TMA cannot address
+    static constexpr bool CK = epi_ck(EPIX);     // K halves on the two CTAs of a cluster (swapped tiles)
+    static constexpr int CLUSTER = (PAIR == 2 || CK) ? 2 : 1;
     static constexpr int BM = 128;               // accumulator rows per CTA (tensor-memory lanes)
     static constexpr int BK = 64;                // halves per 128-byte swizzled row
     static constexpr int BN_LOCAL = BN / PAIR;   // B rows each CTA of a pair loads
@@ -105,8 +107,12 @@ struct TileCfg {
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
     static constexpr int OFF_EPI = OFF_B + STAGES * B_BYTES;
-    static constexpr int OFF_BAR = OFF_EPI + ((EPI_WARPS * EPI_WARP_BYTES + 1023) / 1024) * 1024;
-    static constexpr int NUM_BARS = 2 * STAGES + 4 + (EPI == EPI_TMA_C ? 2 * EPI_WARPS : 0);  // + C-load barriers
+    // cluster K split: the second CTA's partial accumulator, [128 rows][BN] fp32, lands here
+    static constexpr int OFF_X = OFF_EPI + ((EPI_WARPS * EPI_WARP_BYTES + 1023) / 1024) * 1024;
+    static constexpr int X_BYTES = CK ? 128 * BN * 4 : 0;
+    static constexpr int OFF_BAR = OFF_X + X_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 4 + (EPI == EPI_TMA_C ? 2 * EPI_WARPS : 0)  // + C-load barriers
+                                    + (CK ? 2 : 0);                                           // + partial full / empty
     static constexpr int OFF_TMEM_SLOT = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
     static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;  // + slack to align the base to 1024
@@ -127,6 +133,7 @@ struct TileCfg {
                   "row loader: one row of A or B per loader thread, whole warps per operand");
     static_assert(!RL || EPI == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG || EPI == EPI_VEC,
                   "row loader: unswapped whole-tile epilogues only");
+    static_assert(!CK || (PAIR == 1 && EPI == EPI_SWAP && !RL), "cluster K split: swapped single-CTA tiles");
     static_assert(!RL || (THREADS == 512 && MAX_REGS == 128 &&
                           REGS_CTRL + REGS_EPI + 2 * REGS_RL == 4 * MAX_REGS),
                   "the warpgroups' register shares must add up to the block's launch allocation");
@@ -323,17 +330,28 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
     // C tile loads of the TMA epilogue: buffer b of epilogue warp ew.
     auto cload_bar = [&](int ew, int b) { return bar0 + 8u * (2 * STAGES + 4 + 2 * ew + b); };
+    // cluster K split: partial buffer full (in CTA 0) / empty (in CTA 1)
+    const uint32_t xfull_bar = bar0 + 8u * (Cfg::NUM_BARS - 2), xempty_bar = bar0 + 8u * (Cfg::NUM_BARS - 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_TMEM_SLOT);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_ABORT);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t rank = (PAIR == 2) ? cluster_cta_rank() : 0u;
+    const uint32_t krank = Cfg::CK ? cluster_cta_rank() : 0u;  // K half of a cluster K split
     // A kernel launched as this one's programmatic dependent (the split-K reduction) may
     // be scheduled now; it waits for this grid's completion before it reads anything.
     griddep_launch_dependents();
-    const int64_t group = blockIdx.x / PAIR;
-    const int64_t ngroups = gridDim.x / PAIR;
+    const int64_t group = blockIdx.x / Cfg::CLUSTER;
+    const int64_t ngroups = gridDim.x / Cfg::CLUSTER;
+    // Cluster K split: CTA krank of the cluster takes half krank of every tile's k-blocks.
+    auto ck_half = [&](Seg& w) {
+        if constexpr (Cfg::CK) {
+            const int32_t mid = w.kb0 + (w.kb1 - w.kb0) / 2;
+            if (krank == 0) w.kb1 = mid;
+            else w.kb0 = mid;
+        }
+    };
 
     if (threadIdx.x == 0) {
         // A stage is full once the leader's producer has armed it (and TMA has brought its
@@ -352,6 +370,10 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
         if constexpr (EPI == EPI_TMA_C)
             for (int e = 0; e < 2 * Cfg::EPI_WARPS; ++e) mbar_init(cload_bar(e / 2, e % 2), 1);
+        if constexpr (Cfg::CK) {
+            mbar_init(xfull_bar, Cfg::EPI_WARPS);
+            mbar_init(xempty_bar, Cfg::EPI_WARPS);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -364,7 +386,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
     if (warp == 1) tmem_alloc<PAIR>(smem_u32(tmem_slot), Cfg::TMEM_COLS);
     tc_fence_before();
-    if constexpr (PAIR == 2) cluster_sync(); else __syncthreads();
+    if constexpr (Cfg::CLUSTER == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
@@ -383,6 +405,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             SegIter it = seg_begin<SK>(p, group, ngroups);
             Seg w;
             while (ok && seg_next<SK>(p, it, w)) {
+                ck_half(w);
                 const int32_t rowA = w.tm * (Cfg::BM * PAIR) + Cfg::BM * static_cast<int32_t>(rank);
                 // B box nb holds tile columns nb*MMA_N + [0, MMA_N), split between the pair
                 const int32_t rowB = w.tn * BN + Cfg::B_BOX_ROWS * static_cast<int32_t>(rank);
@@ -462,6 +485,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             SegIter it = seg_begin<SK>(p, group, ngroups);
             Seg w;
             while (ok && seg_next<SK>(p, it, w)) {
+                ck_half(w);
                 // One accumulator of 512 columns: wait here for its first half only; the
                 // second half is waited for just before its first MMA, so that the tile's
                 // first k-block of MMAs runs while the epilogue still drains that half.
@@ -645,6 +669,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t chunk_count = 0;
+        uint32_t xphase = 0;  // cluster K split: parity of the next partial-buffer wait
         const bool use_c = (EB == EPI_GENERIC || EB == EPI_SWAP) && p.beta != 0.0f;
         // TMA epilogue with beta != 0: C boxes are fetched by TMA into the staging buffers.
         constexpr bool tma_c = EPI == EPI_TMA_C;
@@ -1084,6 +1109,21 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const int64_t n = arow0 + lane;
                     __half* Dp = static_cast<__half*>(p.D);
                     const __half* Cp = static_cast<const __half*>(p.C);
+                    // Cluster K split: this thread's row of the partial buffer (in CTA 0).
+                    const uint32_t xrow = smem_u32(smem + Cfg::OFF_X) + static_cast<uint32_t>((quarter * 32 + lane) * BN * 4);
+                    if constexpr (Cfg::CK) {
+                        // CTA 1 waits until CTA 0 has read the previous tile's partial; CTA 0 waits
+                        // for this tile's partial
+                        int got = 1;
+                        if (lane == 0)
+                            got = wait_bounded<Cfg::RL>(krank == 0 ? xfull_bar : xempty_bar,
+                                                        krank == 0 ? xphase : xphase ^ 1u, p.err, p.timeout_ns,
+                                                        abort_flag, 8) ? 1 : 0;
+                        got = __shfl_sync(0xffffffffu, got, 0);
+                        if (!got) return;
+                        fence_acq_rel_cluster();  // the peer's release (remote arrive) happens-before what follows
+                        xphase ^= 1u;
+                    }
 #pragma unroll 1
                     for (int c = 0; c < BN / 16; ++c) {
                         uint32_t v[16];
@@ -1092,6 +1132,27 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             tmem_ld_wait();
                         } else {
                             sum_parts(c * 16, v);
+                        }
+                        if constexpr (Cfg::CK) {
+                            const uint32_t xa = xrow + static_cast<uint32_t>(c * 64);
+                            if (krank == 1) {
+                                // hand the partial to CTA 0 and write nothing
+                                const uint32_t ra = map_to_cta(xa, 0);
+#pragma unroll
+                                for (int q = 0; q < 4; ++q)
+                                    st_cluster_v4(ra + 16u * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                                continue;
+                            }
+                            // CTA 0: add the partial, first half of K before the second
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                uint32_t x0, x1, x2, x3;
+                                ld_shared_v4(xa + 16u * q, x0, x1, x2, x3);
+                                v[4 * q] = __float_as_uint(__uint_as_float(v[4 * q]) + __uint_as_float(x0));
+                                v[4 * q + 1] = __float_as_uint(__uint_as_float(v[4 * q + 1]) + __uint_as_float(x1));
+                                v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + __uint_as_float(x2));
+                                v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + __uint_as_float(x3));
+                            }
                         }
                         if (n < p.N) {
                             if constexpr (EB == EPI_SWAP) {
@@ -1124,6 +1185,11 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                 }
                             }
                         }
+                    }
+                    if constexpr (Cfg::CK) {
+                        // CTA 1: the partial is in CTA 0's buffer; CTA 0: the buffer may be refilled
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(map_to_cta(krank == 1 ? xfull_bar : xempty_bar, krank ^ 1u));
                     }
                 }
             };
@@ -1193,7 +1259,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     __syncwarp();
     if (*abort_flag) spin_ns(2000000ull);  // let in-flight TMA loads and MMAs land
     tc_fence_before();
-    if constexpr (PAIR == 2) cluster_sync(); else __syncthreads();
+    if constexpr (Cfg::CLUSTER == 2) cluster_sync(); else __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc<PAIR>(tmem_base, Cfg::TMEM_COLS);
 }

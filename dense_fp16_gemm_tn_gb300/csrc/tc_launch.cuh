@@ -41,7 +41,7 @@ struct TcLauncher {
 
     static int64_t capacity(int sms) {
         if (prepare() != cudaSuccess) return 0;
-        if constexpr (PAIR == 1) {
+        if constexpr (Cfg::CLUSTER == 1) {
             return sms;  // one CTA per SM (shared memory and tensor memory both forbid two)
         } else {
             cudaLaunchConfig_t cfg = {};
@@ -73,10 +73,11 @@ struct TcLauncher {
         if (e != cudaSuccess) return e;
         // Data-parallel only: no more CTAs than units.  With a stream-K phase every
         // group takes part, so the caller's grid is used as it is.
-        const int64_t units_ctas = p.num_units * PAIR;
+        constexpr int CL = Cfg::CLUSTER;
+        const int64_t units_ctas = p.num_units * CL;
         int64_t grid = (p.sk_iters > 0 || max_ctas < units_ctas) ? max_ctas : units_ctas;
-        grid = (grid / PAIR) * PAIR;
-        if (grid < PAIR) grid = PAIR;
+        grid = (grid / CL) * CL;
+        if (grid < CL) grid = CL;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[2];
         unsigned na = 0;
@@ -84,7 +85,7 @@ struct TcLauncher {
         cfg.blockDim = dim3(Cfg::THREADS, 1, 1);
         cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
         cfg.stream = stream;
-        if constexpr (PAIR == 2) {
+        if constexpr (CL == 2) {
             attr[na].id = cudaLaunchAttributeClusterDimension;
             attr[na].val.clusterDim.x = 2;
             attr[na].val.clusterDim.y = 1;

@@ -89,6 +89,9 @@ static const TcVariant kVariants[] = {
     {128, 1, 6, EPI_TMA | EPI_RL, 0, 0},
     {128, 1, 6, EPI_TMA_C | EPI_RL, 0, 0},
     {128, 1, 6, EPI_TMA_CG | EPI_RL, 0, 0},
+    {16, 1, 12, EPI_SWAP | EPI_CK, 0, 0},
+    {32, 1, 10, EPI_SWAP | EPI_CK, 0, 0},
+    {64, 1, 8, EPI_SWAP | EPI_CK, 0, 0},
 };
 
 static_assert(sizeof(kVariants) / sizeof(kVariants[0]) <= kMaxVariants, "variant table too large");

@@ -289,6 +289,11 @@ typedef struct {
     int32_t row_load;        /* bit 0 (A) / bit 1 (B): the operand's rows, which tensor copies cannot
                                 address, are read by the kernel's own loader warps instead of
                                 being repacked (GEMM_TN_OPT_ROW_LOADER; pack_a / pack_b stay 0) */
+    int32_t k_cluster;       /* 1: each (swapped) tile's K is split between the two CTAs of a
+                                cluster; the second half's fp32 partial goes through distributed
+                                shared memory to the first CTA, which writes D (one launch, no
+                                scratch; splits stays 1) */
+    int32_t reserved;
 } gemm_tn_plan_t;
 
 GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int64_t batch,
@@ -334,6 +339,9 @@ GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int6
  *                                 of D's range in the device-side checks, so that the last
  *                                 stores of a call are reported (GEMM_ERR_BOUNDS) and skipped.
  *                                 No effect in the regular build.
+ *   GEMM_TN_OPT_K_CLUSTER         1: swapped small-M problems split K between the two CTAs
+ *                                 of a cluster; -1: never; 0 (default): where two K slices and
+ *                                 a separate sum would otherwise be planned.
  *   GEMM_TN_OPT_ROW_LOADER        1: K-major operands whose rows tensor copies cannot address
  *                                 are read by the kernel's own loader warps (CTA-pair 256x256
  *                                 and single-CTA 128x128 tiles, unswapped, no K slices)
@@ -356,7 +364,8 @@ enum {
     GEMM_TN_OPT_GROUP_M = 10,
     GEMM_TN_OPT_SERPENTINE = 11,
     GEMM_TN_OPT_ROW_LOADER = 12,
-    GEMM_TN_OPT_CHECK_TRIM_D = 13
+    GEMM_TN_OPT_CHECK_TRIM_D = 13,
+    GEMM_TN_OPT_K_CLUSTER = 14
 };
 GEMM_TN_API gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value);
 GEMM_TN_API int64_t gemm_tn_f16_get_option(int32_t option);

@@ -89,7 +89,8 @@ def options(**kw):
              "skip_first_load": G.GEMM_TN_OPT_SKIP_FIRST_LOAD, "timeout_ns": G.GEMM_TN_OPT_WAIT_TIMEOUT_NS,
              "stream_k": G.GEMM_TN_OPT_STREAM_K, "group_m": G.GEMM_TN_OPT_GROUP_M,
              "serpentine": G.GEMM_TN_OPT_SERPENTINE,
-             "row_loader": G.GEMM_TN_OPT_ROW_LOADER}
+             "row_loader": G.GEMM_TN_OPT_ROW_LOADER,
+             "k_cluster": G.GEMM_TN_OPT_K_CLUSTER}
     old = {k: G.gemm_tn_f16_get_option(names[k]) for k in kw}
     try:
         for k, v in kw.items():

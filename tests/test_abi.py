@@ -174,10 +174,19 @@ def test_plan_forced_stream_k_splits_the_partial_wave():
 
 
 def test_plan_skinny_m_swaps_and_splits_k():
-    # 64 swapped tiles of 128 rows: two K slices fill the SMs
+    # 64 swapped tiles of 128 rows: the two K halves of each tile on the two CTAs of a
+    # cluster (one launch, no scratch) ...
     p = plan(16, 8192, 8192)
+    assert p["kernel"] == 2 and p["swap_ab"] == 1 and p["tile_n"] == 16 and p["splits"] == 1
+    assert p["k_cluster"] == 1 and p["grid"] == 128 and p["units"] == 64 and p["workspace_bytes"] == 0
+    # ... or, without the cluster split, two K slices and the sum kernel
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_K_CLUSTER, -1)
+    try:
+        p = plan(16, 8192, 8192)
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_K_CLUSTER, 0)
     assert p["kernel"] == 3 and p["swap_ab"] == 1 and p["tile_n"] == 16 and p["splits"] == 2
-    assert p["workspace_bytes"] >= 2 * 16 * 8192 * 4
+    assert p["k_cluster"] == 0 and p["workspace_bytes"] >= 2 * 16 * 8192 * 4
     # stream-K when no whole slices fit (128 tiles), and when asked for
     q = plan(16, 16384, 8192, sms=152)
     assert q["kernel"] == 2 and q["swap_ab"] == 1 and q["splits"] == 1 and q["stream_k"] == 1

@@ -71,6 +71,14 @@ CASES = [
     ("streamk_swap_skinny", dict(M=16, N=1024, K=4096)),
     ("streamk_swap_beta", dict(M=40, N=2000, K=1000, alpha=0.5, beta=1.5, opts=dict(stream_k=1))),
     ("streamk_batched", dict(M=600, N=600, K=640, batch=3, opts=dict(stream_k=1))),
+    # K halves on the two CTAs of a cluster, the partial added through distributed shared memory
+    ("kcluster_m16", dict(M=16, N=1000, K=3000, opts=dict(k_cluster=1))),
+    ("kcluster_m40_beta", dict(M=40, N=2000, K=1000, alpha=0.5, beta=1.5, opts=dict(k_cluster=1))),
+    ("kcluster_m24_three_kblocks", dict(M=24, N=777, K=130, opts=dict(k_cluster=1))),
+    ("kcluster_many_tiles_per_cluster", dict(M=16, N=40000, K=512, beta=-0.75, opts=dict(k_cluster=1))),
+    ("kcluster_batched", dict(M=16, N=600, K=256, batch=3, alpha=0.25, beta=1.0, opts=dict(k_cluster=1))),
+    ("kcluster_packed", dict(M=33, N=400, K=777, lda=779, ldb=781, opts=dict(k_cluster=1))),
+    ("kcluster_auto_skinny", dict(M=16, N=8192, K=4096)),
     # serpentine K order: odd waves of whole tiles walk K backwards
     ("serpentine_pair_waves", dict(M=3000, N=2900, K=700, alpha=0.5, beta=1.5,
                                    opts=dict(serpentine=1, stream_k=-1, force_pair=2, force_bn=256))),
@@ -83,6 +91,12 @@ CASES = [
 @pytest.mark.parametrize("name,kw", CASES, ids=[c[0] for c in CASES])
 def test_parity(name, kw):
     run_problem(seed=zlib.crc32(name.encode()) % 1000, **kw)
+
+
+@pytest.mark.parametrize("bn_m", [16, 32, 64])
+def test_k_cluster_small_integers_bit_exact(bn_m):
+    """K halves summed through distributed shared memory: exact sums must match bit for bit."""
+    run_problem(bn_m, 3000, 2048, dist="int", compare="exact", seed=33, opts=dict(k_cluster=1))
 
 
 @pytest.mark.parametrize("serp", [1, -1])
