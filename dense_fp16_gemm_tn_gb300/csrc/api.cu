@@ -389,9 +389,26 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
         // waves the coarser quantisation loses (4096^3: 87.5 against 83-87 us, and their
         // 256 KB-per-CTA stream-K partials make the fix-up dearer than the idle wave: 98 us).
         const int64_t t_wide = ceil_div(pr.M, 256) * ceil_div(pr.N, 512) * pr.batch;
-        const int64_t pairs = slots / 2;
+        const int64_t pairs = std::max<int64_t>(slots / 2, 1);
         const int64_t wide_tail = t_wide % pairs;
-        if (pr.K >= 8192 && t_wide >= 6 * pairs && (wide_tail == 0 || 10 * wide_tail >= 7 * pairs)) {
+        const bool wide_ok = pr.K >= 8192 && t_wide >= 6 * pairs && (wide_tail == 0 || 10 * wide_tail >= 7 * pairs);
+        // 256x432 pair tiles (MMAs of N = 256 and 176) where the waves of 512-column tiles
+        // come out short: 6144 x 8192 x 8192 is exactly 6 waves of them (446 us against 475
+        // for 256 x 256 tiles).  Where 512-column tiles qualify, the 432-column ones must
+        // promise 5 % less MMA work on the critical path (waves x tile width): at the power
+        // cap fewer idle SMs in a last wave raise the clock less than it seems, and 8192^3
+        // measured the same either way (8 x 432 columns, 592-594 us, against 7 x 512,
+        // 592-598), the 512-column tile moving fewer operand bytes per FLOP.  D = alpha A B^T
+        // with K-major operands only.
+        const int64_t t_432 = ceil_div(pr.M, 256) * ceil_div(pr.N, 432) * pr.batch;
+        const int64_t tail_432 = t_432 % pairs;
+        const bool k_major = !pr.a_mn && !pr.b_mn;
+        if (pr.K >= 8192 && k_major && !pr.acc16 && pr.beta == 0.0f && t_432 >= 6 * pairs &&
+            (tail_432 == 0 || 10 * tail_432 >= 7 * pairs) &&
+            (!wide_ok || 20 * ceil_div(t_432, pairs) * 432 < 19 * ceil_div(t_wide, pairs) * 512)) {
+            pair = 2;
+            bn = 432;
+        } else if (wide_ok) {
             pair = 2;
             bn = 512;
         } else if (pr.K >= 512 && 2 * t_pair >= slots) {
@@ -410,7 +427,7 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
             bn = 128;
         }
         const int64_t fbn = g_opt_force_bn.load(), fpair = g_opt_force_pair.load();
-        if (fbn == 128 || fbn == 256 || fbn == 512) bn = static_cast<int>(fbn);
+        if (fbn == 128 || fbn == 256 || fbn == 432 || fbn == 512) bn = static_cast<int>(fbn);
         if (fpair == 1 || fpair == 2) pair = static_cast<int>(fpair);
     }
     const int64_t rows_a = swap ? pr.N : pr.M;
@@ -484,7 +501,9 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     else epi = EPI_GENERIC;
 
     TcVariant v;
-    if (bn == 512 && !find_tc_variant(bn, pair, epi, 0, nullptr)) bn = 256;  // 512 columns: CTA pairs, TMA epilogues
+    // 432 columns: CTA pairs, D = alpha * acc by TMA stores; 512 columns: CTA pairs, TMA epilogues
+    if (bn == 432 && (swap || pr.a_mn || pr.b_mn || !find_tc_variant(bn, pair, epi, 0, nullptr))) bn = 512;
+    if (bn == 512 && !find_tc_variant(bn, pair, epi, 0, nullptr)) bn = 256;
     if (pl.ck) {
         find_tc_variant(bn, 1, EPI_SWAP | EPI_CK, 0, &v);
     } else if (!find_tc_variant(bn, pair, epi, 0, &v)) {
@@ -1167,7 +1186,8 @@ gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value) {
             return GEMM_OK;
         case GEMM_TN_OPT_SKIP_FIRST_LOAD: g_opt_skip_first_load = value ? 1 : 0; return GEMM_OK;
         case GEMM_TN_OPT_FORCE_BN:
-            if (value != 0 && value != 128 && value != 256 && value != 512) return GEMM_ERR_INVALID_VALUE;
+            if (value != 0 && value != 128 && value != 256 && value != 432 && value != 512)
+                return GEMM_ERR_INVALID_VALUE;
             g_opt_force_bn = value;
             return GEMM_OK;
         case GEMM_TN_OPT_FORCE_PAIR:

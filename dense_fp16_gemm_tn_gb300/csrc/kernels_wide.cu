@@ -1,7 +1,8 @@
 // Variants with 256 x 512 CTA-pair tiles (two N=256 MMAs per K step, one 512-column
 // accumulator) and TMA-store epilogues.  Per k-block each CTA loads 128 rows of A and
 // 256 rows of B for twice the MMA work of a 256 x 256 pair tile, which keeps operand
-// delivery well inside the tensor pipe's time.
+// delivery well inside the tensor pipe's time.  The 256 x 432 tile (MMAs of N = 256 and
+// 176, the same boxes) is for problems whose waves of 512-column tiles come out short.
 #include "tc_launch.cuh"
 
 namespace gtn {
@@ -12,7 +13,8 @@ namespace gtn {
     X(512, 2, 4, EPI_TMA_C, 0)      \
     X(512, 2, 4, EPI_TMA_C, 1)      \
     X(512, 2, 4, EPI_TMA_CG, 0)     \
-    X(512, 2, 4, EPI_TMA_CG, 1)
+    X(512, 2, 4, EPI_TMA_CG, 1)     \
+    X(432, 2, 4, EPI_TMA, 0)
 
 bool launch_family_wide(const TcVariant& v, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const CUtensorMap& tmD, const KParams& p, int64_t max_ctas, cudaStream_t stream,

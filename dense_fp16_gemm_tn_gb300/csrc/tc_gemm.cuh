@@ -73,18 +73,25 @@ struct TileCfg {
     static constexpr int BM = 128;               // accumulator rows per CTA (tensor-memory lanes)
     static constexpr int BK = 64;                // halves per 128-byte swizzled row
     static constexpr int BN_LOCAL = BN / PAIR;   // B rows each CTA of a pair loads
-    // A 512-column pair tile is two N=256 MMAs per 16-wide K step, one per half of the
-    // tile's columns; each CTA loads one 128-row B box per MMA.
-    static constexpr int MMA_N = BN > 256 ? 256 : BN;
-    static constexpr int N_MMAS = BN / MMA_N;
+    // A wide pair tile (BN = 432 or 512) is two MMAs per 16-wide K step: N = 256 for the
+    // tile's first 256 columns and N = BN - 256 for the rest; each CTA loads one 128-row B
+    // box per MMA (of the second box's 128 rows, a 432-column tile uses the first 88).
+    static constexpr bool WIDE = BN > 256;
+    static constexpr int MMA_N = WIDE ? 256 : BN;      // N of the first MMA
+    static constexpr int MMA_N1 = WIDE ? BN - 256 : BN;  // N of the second
+    static constexpr int N_MMAS = WIDE ? 2 : 1;
     static constexpr int B_BOX_ROWS = MMA_N / PAIR;
     static constexpr int B_BOX_BYTES = B_BOX_ROWS * BK * 2;
     // Accumulators in tensor memory (512 columns): two of BN <= 256 columns, so that the
-    // epilogue of one tile overlaps the main loop of the next; one of 512 columns, whose
-    // halves are released separately.
+    // epilogue of one tile overlaps the main loop of the next; one of a wide tile's BN
+    // columns, whose two parts (the two MMAs' columns) are released separately.
     static constexpr int ACC_BUFS = (2 * BN <= 512) ? 2 : 1;
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN_LOCAL * BK * 2;
+    static constexpr int B_BYTES = N_MMAS * B_BOX_BYTES;
+    // Whole 64-column chunks of the TMA epilogue, and the columns of a wide tile's partial
+    // last chunk (48 for a 432-column tile, written from registers by 16-byte stores).
+    static constexpr int FULL_CHUNKS = BN / 64;
+    static constexpr int TAIL_COLS = WIDE ? BN % 64 : 0;
     static constexpr uint32_t STAGE_TX = uint32_t(A_BYTES + B_BYTES) * PAIR;
     static constexpr int EPI_WARPS = 4;
     static constexpr int RL_WARPS = RL ? 8 : 0;  // one operand row per loader thread and k-block
@@ -117,16 +124,20 @@ struct TileCfg {
     static constexpr int OFF_ABORT = OFF_TMEM_SLOT + 4;
     static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;  // + slack to align the base to 1024
 
-    static_assert(BN % 16 == 0 && BN >= 16 && (BN <= 256 || (BN == 512 && PAIR == 2)),
-                  "tcgen05 needs N in [16,256], N%16==0; 512 columns are two MMAs of a CTA pair");
+    static_assert(BN % 16 == 0 && BN >= 16 && (BN <= 256 || ((BN == 512 || BN == 432) && PAIR == 2)),
+                  "tcgen05 needs N in [16,256], N%16==0; 432 and 512 columns are two MMAs of a CTA pair");
     static_assert(BN <= 256 || EPI == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG,
                   "512-column tiles have the TMA epilogues only");
-    static_assert(BN_LOCAL % 8 == 0, "B tile must hold whole 8-row swizzle atoms");
+    static_assert(BN != 432 || EPI == EPI_TMA, "432-column tiles: D = alpha * acc by TMA stores only");
+    static_assert(MMA_N1 % 16 == 0 && MMA_N1 <= 256 && (MMA_N1 / PAIR) % 8 == 0,
+                  "second MMA: N%16==0, whole 8-row swizzle atoms of B per CTA");
     static_assert(B_BYTES % 1024 == 0 && A_BYTES % 1024 == 0 && B_BOX_BYTES % 1024 == 0,
                   "tiles must stay 1024-byte aligned");
     static_assert((epi_base(EPI) != EPI_TMA && EPI != EPI_TMA_C && EPI != EPI_TMA_CG && EPI != EPI_VEC) ||
-                      BN % 64 == 0,
+                      BN % 64 == 0 || (BN == 432 && EPI == EPI_TMA),
                   "the TMA and row-word epilogues work in 64-column chunks");
+    static_assert(!WIDE || MMA_N % 64 == 0, "a wide tile's first part ends on a 64-column chunk");
+    static_assert(TAIL_COLS == 0 || TAIL_COLS == 48, "a partial last chunk is 32 + 16 tensor-memory columns");
     static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory per CTA");
     static_assert(PAIR == 1 || PAIR == 2, "CTA pair or single CTA");
     static_assert(!RL || (BM + BN_LOCAL <= 32 * RL_WARPS && BN_LOCAL % 32 == 0 && N_MMAS == 1),
@@ -407,8 +418,9 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             while (ok && seg_next<SK>(p, it, w)) {
                 ck_half(w);
                 const int32_t rowA = w.tm * (Cfg::BM * PAIR) + Cfg::BM * static_cast<int32_t>(rank);
-                // B box nb holds tile columns nb*MMA_N + [0, MMA_N), split between the pair
-                const int32_t rowB = w.tn * BN + Cfg::B_BOX_ROWS * static_cast<int32_t>(rank);
+                // B box nb holds the columns of MMA nb (tile columns nb*MMA_N + [0, N of MMA nb)),
+                // split between the pair: this CTA's share starts (N of MMA nb) / 2 * rank in.
+                const int32_t rowB = w.tn * BN;
                 for (int32_t i = 0; i < w.kb1 - w.kb0; ++i) {
                     const int32_t kb = w.rev ? w.kb1 - 1 - i : w.kb0 + i;
                     if (!wait_bounded<Cfg::RL>(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 1)) {
@@ -441,7 +453,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                         for (int nb = 0; nb < Cfg::N_MMAS; ++nb) {
                             const uint32_t dBn = dB + static_cast<uint32_t>(nb * Cfg::B_BOX_BYTES);
-                            const int32_t rowBn = rowB + nb * Cfg::MMA_N;
+                            const int32_t rowBn = rowB + nb * Cfg::MMA_N +
+                                                  (nb == 0 ? Cfg::MMA_N : Cfg::MMA_N1) / PAIR * static_cast<int32_t>(rank);
                             if (Cfg::RL && p.rl_on[1]) {
                                 // B rows come from the loader warps
                             } else if (!p.b_mn) {
@@ -470,6 +483,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (rank == 0 && lane == 0) {
             const uint32_t IDESC =
                 idesc_f16_f32(Cfg::BM * PAIR, Cfg::MMA_N, p.a_mn ? 1u : 0u, p.b_mn ? 1u : 0u, ACC16 ? 0u : 1u);
+            const uint32_t IDESC1 =  // the second MMA of a wide tile
+                idesc_f16_f32(Cfg::BM * PAIR, Cfg::MMA_N1, p.a_mn ? 1u : 0u, p.b_mn ? 1u : 0u, ACC16 ? 0u : 1u);
             // Per 16-wide K step: +32 bytes inside a K-major 128-byte row, +2048 bytes
             // (16 rows of 128 bytes) in an MN-major box.
             const uint32_t a_step = p.a_mn ? 128u : 2u, b_step = p.b_mn ? 128u : 2u;
@@ -520,7 +535,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                         for (int k = 0; k < Cfg::BK / 16; ++k) {
                             mma_f16<PAIR>(d_tmem + static_cast<uint32_t>(nb * Cfg::MMA_N), adesc + a_step * k,
-                                          bdesc_n + b_step * k, IDESC, (kb > w.kb0 || k > 0) ? 1u : 0u);
+                                          bdesc_n + b_step * k, nb == 0 ? IDESC : IDESC1, (kb > w.kb0 || k > 0) ? 1u : 0u);
                         }
                     }
                     if (!ok) break;
@@ -819,7 +834,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 // first half of a 512-column accumulator goes back to the MMA early.
                 auto fetched = [&](int c) {
                     if constexpr (!PARTS && Cfg::ACC_BUFS == 1) {
-                        if (c == BN / 128 - 1) {
+                        if (c == Cfg::MMA_N / 64 - 1) {
                             arrive_tempty(0);
                             lo_released = true;
                         }
@@ -941,7 +956,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     } else if constexpr (!tma_c) {
                         // D = alpha * acc
 #pragma unroll 1
-                        for (int c = 0; c < BN / 64; ++c) {
+                        for (int c = 0; c < Cfg::FULL_CHUNKS; ++c) {
                             uint32_t v0[32], v1[32];
                             fetch64(c, v0, v1);
                             fetched(c);
@@ -968,6 +983,34 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                              pack_half2(al * __uint_as_float(v1[8 * j + 6]), al * __uint_as_float(v1[8 * j + 7])));
                             }
                             store_chunk(c, sb);
+                        }
+                        if constexpr (Cfg::TAIL_COLS == 48 && !PARTS && !ACC16) {
+                            // The last 48 columns (32 + 16 of tensor memory): this thread's row
+                            // segment goes out from registers in 16-byte stores (D is 16-byte
+                            // aligned here).
+                            uint32_t v0[32], v1[16];
+                            tmem_ld_32x32b_x32(t_row + Cfg::FULL_CHUNKS * 64, v0);
+                            tmem_ld_32x32b_x16(t_row + Cfg::FULL_CHUNKS * 64 + 32, v1);
+                            tmem_ld_wait();
+                            const float al = p.alpha;
+                            uint32_t o[32];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                o[i] = pack_half2(al * __uint_as_float(v0[2 * i]), al * __uint_as_float(v0[2 * i + 1]));
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                o[16 + i] = pack_half2(al * __uint_as_float(v1[2 * i]), al * __uint_as_float(v1[2 * i + 1]));
+#pragma unroll
+                            for (int i = 24; i < 32; ++i) o[i] = 0u;
+                            const int64_t row = arow0 + lane;
+                            const int64_t col0 = acol0 + Cfg::FULL_CHUNKS * 64;
+                            const int valid = (row < p.M && col0 < p.N)
+                                                  ? static_cast<int>(p.N - col0 < Cfg::TAIL_COLS ? p.N - col0 : Cfg::TAIL_COLS)
+                                                  : 0;
+                            __half* const drow =
+                                static_cast<__half*>(p.D) + static_cast<int64_t>(w.b) * p.strideD + row * p.ldd;
+                            store_row64(reinterpret_cast<uint16_t*>(drow + col0), valid, o,
+                                        GTN_ROW_CHECK(p.ext_d, p.err, CHK_EPI_D_ROW));
                         }
                     } else {
                         // D = alpha * acc + beta * C, C boxes loaded by TMA into the staging buffers

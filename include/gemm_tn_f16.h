@@ -264,8 +264,9 @@ typedef struct {
     int32_t kernel;          /* 0 none (empty problem), 1 scale-only (K == 0),
                                 2 tensor-core tile kernel, 3 split-K (+ reduction) */
     int32_t tile_m;          /* output rows per tile as seen by the tensor core (128 or 256) */
-    int32_t tile_n;          /* output columns per tile as seen by the tensor core (16..256, or 512:
-                                two N=256 MMAs side by side on a CTA pair) */
+    int32_t tile_n;          /* output columns per tile as seen by the tensor core (16..256, or 432
+                                or 512: two MMAs, N = 256 and N = tile_n - 256, side by side on
+                                a CTA pair) */
     int32_t cta_pair;        /* 1: one CTA per tile; 2: CTA pair sharing one 256-row tile */
     int32_t swap_ab;         /* 1: computes D^T = B . A^T (small M) */
     int32_t splits;          /* K slices (1 = no split) */
@@ -309,8 +310,10 @@ GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int6
  *                                 load, so its MMA wait runs out and the kernel reports
  *                                 GEMM_ERR_TIMEOUT -- exercises the stall path without any
  *                                 fault.  Testing only; 0 restores normal operation.
- *   GEMM_TN_OPT_FORCE_BN          force the tile width: 128, 256 or 512 (CTA pairs with a TMA
- *                                 epilogue only; else 256), 0 = automatic.
+ *   GEMM_TN_OPT_FORCE_BN          force the tile width: 128, 256, 432 or 512 (512: CTA pairs
+ *                                 with a TMA epilogue only, else 256; 432: CTA pairs, K-major
+ *                                 operands, beta == 0 and 16-byte aligned D rows only, else
+ *                                 as 512), 0 = automatic.
  *   GEMM_TN_OPT_FORCE_PAIR        force 1 (single CTA) or 2 (CTA pair), 0 = automatic.
  *   GEMM_TN_OPT_FORCE_SPLITS      force the number of K slices, 0 = automatic: K slices, summed
  *                                 by a second kernel, when 128 x 128 tiles would occupy at

@@ -133,11 +133,17 @@ def test_plan_large_square_uses_cta_pairs_and_tma_store():
 
 
 def test_plan_wide_pair_tiles_only_for_many_full_waves_of_long_tiles():
-    # 8192^3: 512 tiles of 256 x 512 over 76 pairs, 6.7 waves, data-parallel
+    # 8192^3: 512 tiles of 256 x 512 over 76 pairs, 6.7 waves, data-parallel (8 waves of
+    # 432-column tiles would save less than 5 % of the MMA work on the critical path)
     p = plan(8192, 8192, 8192, sms=152)
     assert p["cta_pair"] == 2 and p["tile_m"] == 256 and p["tile_n"] == 512 and p["epi_tma"] == 1
     assert p["stream_k"] == 0 and p["units"] == 512 and p["grid"] == 152 and p["stages"] == 4
     assert plan(16384, 16384, 8192, sms=152)["tile_n"] == 512
+    # 6144 x 8192 x 8192, D = alpha A B^T: 5.05 waves of 512-column tiles, exactly 6 of
+    # 256 x 432 tiles (24 x 19 = 456 = 6 x 76)
+    p = plan(6144, 8192, 8192, sms=152)
+    assert p["cta_pair"] == 2 and p["tile_n"] == 432 and p["units"] == 6 * 76 and p["stream_k"] == 0
+    assert plan(6144, 8192, 8192, sms=152, beta=1.0)["tile_n"] == 256
     # too few waves, short K, a mostly empty last wave, or an epilogue without TMA stores
     for M, N, K, kw in ((4096, 4096, 4096, {}), (4096, 4096, 8192, {}), (8192, 8192, 4096, {}),
                         (8192, 6144, 8192, {}), (8192, 8192, 8192, dict(ldd=8193)),
@@ -149,6 +155,15 @@ def test_plan_wide_pair_tiles_only_for_many_full_waves_of_long_tiles():
         assert plan(4096, 4096, 4096, sms=152)["tile_n"] == 512
         assert plan(4096, 4096, 4096, sms=152, beta=1.0, ldc=4097)["tile_n"] == 512
         assert plan(4096, 4096, 4096, sms=152, ldd=4097)["tile_n"] == 256
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 0)
+    # forced 432: D = alpha A B^T by TMA stores only, else 512, else 256
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 432)
+    try:
+        assert plan(4096, 4096, 4096, sms=152)["tile_n"] == 432
+        assert plan(4096, 4096, 4096, sms=152, beta=1.0)["tile_n"] == 512
+        assert plan(4096, 4096, 4096, sms=152, ldd=4097)["tile_n"] == 256
+        assert plan(16, 4096, 4096, sms=152)["tile_n"] == 16  # skinny problems stay swapped
     finally:
         G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 0)
 

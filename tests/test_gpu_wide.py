@@ -66,3 +66,44 @@ def test_wide_tile_small_integers_bit_exact(name, kw):
 def test_wide_tile_mn_major(a_mn, b_mn):
     run_layout(600, 1096, 520, a_mn, b_mn, alpha=0.5, beta=1.5, seed=5 + 2 * a_mn + b_mn, opts=WIDE)
     run_layout(1280, 1536, 1024, a_mn, b_mn, seed=9 + 2 * a_mn + b_mn, opts=dict(WIDE, stream_k=1))
+
+
+# 256 x 432 pair tiles: MMAs of N = 256 and 176 into one accumulator (the first part handed
+# back after its four 64-column chunks), six TMA-stored chunks and a 48-column tail written
+# from registers.  The last tile column ends inside the first MMA's part, inside the
+# second's, inside the tail chunk, and exactly on the tile.  (D rows 16-byte aligned: N and
+# ldd multiples of 8, which the 432-column variant needs.)
+W432 = dict(force_bn=432, force_pair=2)
+CASES_432 = [
+    ("one_tile", dict(M=256, N=432, K=128)),
+    ("end_in_first_part", dict(M=600, N=536, K=520)),
+    ("end_in_second_part", dict(M=300, N=1168, K=200)),
+    ("end_in_tail_chunk", dict(M=520, N=832, K=136)),
+    ("k_tail", dict(M=300, N=712, K=65)),
+    ("k1", dict(M=260, N=440, K=1)),
+    ("ldd_padded", dict(M=600, N=1000, K=264, ldd=1008, alpha=0.25)),
+    ("batched", dict(M=520, N=904, K=200, batch=3, alpha=-0.5)),
+    ("many_tiles_serpentine", dict(M=2100, N=2600, K=384, opts=dict(serpentine=1))),
+]
+
+
+@pytest.mark.parametrize("name,kw", CASES_432, ids=[c[0] for c in CASES_432])
+def test_432_column_tile_parity(name, kw):
+    kw = dict(kw)
+    opts = dict(W432, **kw.pop("opts", {}))
+    plan = plan_for(opts=opts, **kw)
+    assert plan["tile_n"] == 432 and plan["cta_pair"] == 2 and plan["epi_tma"] == 1, plan
+    run_problem(seed=zlib.crc32(name.encode()) % 1000, opts=opts, **kw)
+
+
+@pytest.mark.parametrize("N", [864, 1168, 832])
+def test_432_column_tile_small_integers_bit_exact(N):
+    assert plan_for(M=512, N=N, K=256, opts=W432)["tile_n"] == 432
+    run_problem(seed=13, M=512, N=N, K=256, dist="int", compare="exact", opts=W432)
+
+
+def test_432_column_tile_falls_back_where_it_has_no_variant():
+    # beta != 0 and MN-major operands take the 512-column tiles instead
+    assert plan_for(M=600, N=1096, K=520, beta=1.5, opts=W432)["tile_n"] == 512
+    run_problem(seed=17, M=600, N=1096, K=520, alpha=0.5, beta=1.5, opts=W432)
+    run_layout(600, 1096, 520, 0, 1, seed=19, opts=W432)
