@@ -341,6 +341,14 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
     }
     find_tc_variant(pl.var.bn, pl.var.pair, pl.epi | (pl.rl ? EPI_RL : 0) | (pl.ck ? EPI_CK : 0), pub.stream_k,
                     &pl.var);
+    // Wide data-parallel tiles with D = alpha*acc by TMA stores: the variant with one epilogue
+    // warpgroup per part of the accumulator, which hands both parts back to the MMA as soon
+    // as they are in registers (the next tile's MMAs otherwise wait for the stores of the
+    // first part before they get the second).
+    TcVariant h2v;
+    if (!pub.stream_k && !pl.rl && !pl.ck && pl.var.bn > 256 && pl.epi == EPI_TMA &&
+        find_tc_variant(pl.var.bn, pl.var.pair, EPI_TMA | EPI_H2, 0, &h2v))
+        pl.var = h2v;
     const int cl = pl.ck ? 2 : pair;  // CTAs per cluster
     pub.units = pub.stream_k ? pub.dp_tiles : tiles * pub.splits;
     pub.grid = pub.stream_k ? sk_groups * cl : std::min<int64_t>(pub.units, G) * cl;

@@ -14,7 +14,8 @@ namespace gtn {
     X(512, 2, 4, EPI_TMA_C, 1)      \
     X(512, 2, 4, EPI_TMA_CG, 0)     \
     X(512, 2, 4, EPI_TMA_CG, 1)     \
-    X(432, 2, 4, EPI_TMA, 0)
+    X(432, 2, 4, EPI_TMA, 0)        \
+    X(512, 2, 4, EPI_TMA | EPI_H2, 0)
 
 bool launch_family_wide(const TcVariant& v, const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                         const CUtensorMap& tmD, const KParams& p, int64_t max_ctas, cudaStream_t stream,

@@ -29,6 +29,11 @@ constexpr int EPI_RL = 0x100;
 // (distributed shared memory), which adds it and writes D -- split-K in one launch,
 // with no scratch in global memory.
 constexpr int EPI_CK = 0x200;
+// Variant flag (wide pair tiles, D = alpha*acc by TMA stores): two epilogue warpgroups, one
+// per part of the accumulator (the two MMAs' columns).  Each warp reads its whole part of
+// its 32 rows into registers as fp16 and hands the part back to the MMA before it stores
+// anything, so the next tile's MMAs wait only for tensor-memory reads, not for stores.
+constexpr int EPI_H2 = 0x400;
 
 #ifdef __CUDACC__
 #define GTN_HD __host__ __device__
@@ -45,6 +50,7 @@ GTN_HD constexpr int epi_base(int epi) {
 GTN_HD constexpr bool epi_acc16(int epi) { return epi_mode(epi) == EPI_TMA_A16 || epi_mode(epi) == EPI_GENERIC_A16; }
 GTN_HD constexpr bool epi_rl(int epi) { return (epi & EPI_RL) != 0; }
 GTN_HD constexpr bool epi_ck(int epi) { return (epi & EPI_CK) != 0; }
+GTN_HD constexpr bool epi_h2(int epi) { return (epi & EPI_H2) != 0; }
 
 struct KParams {
     // Tensor-core view: the MMA's A operand has rows_a rows, its B operand rows_b rows.

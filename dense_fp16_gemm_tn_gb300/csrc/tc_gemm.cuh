@@ -69,6 +69,7 @@ struct TileCfg {
     static constexpr int EPI = epi_mode(EPIX);   // epilogue mode
     static constexpr bool RL = epi_rl(EPIX);     // row-loader warps for operands TMA cannot address
     static constexpr bool CK = epi_ck(EPIX);     // K halves on the two CTAs of a cluster (swapped tiles)
+    static constexpr bool H2 = epi_h2(EPIX);     // one epilogue warpgroup per part of a wide accumulator
     static constexpr int CLUSTER = (PAIR == 2 || CK) ? 2 : 1;
     static constexpr int BM = 128;               // accumulator rows per CTA (tensor-memory lanes)
     static constexpr int BK = 64;                // halves per 128-byte swizzled row
@@ -93,22 +94,29 @@ struct TileCfg {
     static constexpr int FULL_CHUNKS = BN / 64;
     static constexpr int TAIL_COLS = WIDE ? BN % 64 : 0;
     static constexpr uint32_t STAGE_TX = uint32_t(A_BYTES + B_BYTES) * PAIR;
-    static constexpr int EPI_WARPS = 4;
+    static constexpr int EPI_WARPS = H2 ? 8 : 4;
     static constexpr int RL_WARPS = RL ? 8 : 0;  // one operand row per loader thread and k-block
     // Warp roles: 0 TMA producer, 1 MMA issuer, then the epilogue warps, then the loader warps.
     // With the row loader the block is four warpgroups whose register shares differ
     // (setmaxnreg): warps 0-3 (producer, MMA, two idle) give registers up, the epilogue
-    // warpgroup (4-7) and the two loader warpgroups (8-15) take them.
-    static constexpr int EPI_W0 = RL ? 4 : 2;
+    // warpgroup (4-7) and the two loader warpgroups (8-15) take them.  With two epilogue
+    // warpgroups (H2) it is three: warps 0-3 give up, the epilogue warpgroups 4-7 (first
+    // part of the accumulator) and 8-11 (second part) take.
+    static constexpr bool SETMAXNREG = RL || H2;
+    static constexpr int EPI_W0 = SETMAXNREG ? 4 : 2;
     static constexpr int RL_W0 = EPI_W0 + EPI_WARPS;
     static constexpr int THREADS = 32 * RL_W0 + 32 * RL_WARPS;
-    static constexpr int REGS_CTRL = 48, REGS_EPI = 176, REGS_RL = 144;  // per thread, after setmaxnreg
+    // per thread, after setmaxnreg
+    static constexpr int REGS_CTRL = H2 ? 104 : 48, REGS_EPI = H2 ? 200 : 176, REGS_RL = 144;
+    // epilogue warps arriving on each part's tensor-memory barrier (per CTA)
+    static constexpr int TEMPTY_WARPS = H2 ? EPI_WARPS / 2 : EPI_WARPS;
     // Registers per thread: all of the 64K register file over the block's warps, in steps of 8.
     static constexpr int MAX_REGS = ((65536 / THREADS) / 8 * 8) > 255 ? 255 : ((65536 / THREADS) / 8 * 8);
     static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
     static constexpr int EPI_WARP_BYTES =
-        (epi_base(EPI) == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) ? 2 * 32 * 128
+        H2 ? 32 * 128  // one staging buffer per warp (eight warps)
+        : (epi_base(EPI) == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) ? 2 * 32 * 128
         : (EPI == EPI_PARTIAL) ? 2 * 32 * 128  // TMA staging (or the padded transpose, 32 x 33 x 4)
         : (epi_base(EPI) == EPI_GENERIC) ? 32 * 33 * 4 : 0;
     static constexpr int OFF_A = 0;
@@ -147,6 +155,11 @@ struct TileCfg {
     static_assert(!CK || (PAIR == 1 && EPI == EPI_SWAP && !RL), "cluster K split: swapped single-CTA tiles");
     static_assert(!RL || (THREADS == 512 && MAX_REGS == 128 &&
                           REGS_CTRL + REGS_EPI + 2 * REGS_RL == 4 * MAX_REGS),
+                  "the warpgroups' register shares must add up to the block's launch allocation");
+    static_assert(!H2 || (WIDE && EPI == EPI_TMA && PAIR == 2 && !RL && !CK), "two epilogue warpgroups: wide TMA tiles");
+    // (with 104 registers the producer and MMA code of the 512-column tile compiles without
+    // spills, and 200 hold an epilogue warp's 128 packed words of its part plus a load)
+    static_assert(!H2 || (THREADS == 384 && MAX_REGS == 168 && REGS_CTRL + 2 * REGS_EPI == 3 * MAX_REGS),
                   "the warpgroups' register shares must add up to the block's launch allocation");
 };
 
@@ -377,7 +390,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), Cfg::EPI_WARPS * PAIR);
+            mbar_init(tempty_bar(a), Cfg::TEMPTY_WARPS * PAIR);
         }
         if constexpr (EPI == EPI_TMA_C)
             for (int e = 0; e < 2 * Cfg::EPI_WARPS; ++e) mbar_init(cload_bar(e / 2, e % 2), 1);
@@ -404,7 +417,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     // Each role's register share is set at the top of its branch (row-loader variants), so
     // that the compiler allocates every role's code within its own share.
     if (warp < Cfg::EPI_W0) {
-    if constexpr (Cfg::RL) setmaxnreg_dec<Cfg::REGS_CTRL>();
+    if constexpr (Cfg::SETMAXNREG) setmaxnreg_dec<Cfg::REGS_CTRL>();
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
@@ -423,7 +436,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 const int32_t rowB = w.tn * BN;
                 for (int32_t i = 0; i < w.kb1 - w.kb0; ++i) {
                     const int32_t kb = w.rev ? w.kb1 - 1 - i : w.kb0 + i;
-                    if (!wait_bounded<Cfg::RL>(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 1)) {
+                    if (!wait_bounded<Cfg::SETMAXNREG>(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 1)) {
                         ok = false;
                         break;
                     }
@@ -474,7 +487,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             // Drain: wait until the MMA has released every slot, so that no
             // tcgen05.commit arrives on this CTA's barriers after it exits.
             for (int i = 0; i < STAGES && ok; ++i) {
-                if (!wait_bounded<Cfg::RL>(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 2)) break;
+                if (!wait_bounded<Cfg::SETMAXNREG>(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 2)) break;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
@@ -504,7 +517,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 // One accumulator of 512 columns: wait here for its first half only; the
                 // second half is waited for just before its first MMA, so that the tile's
                 // first k-block of MMAs runs while the epilogue still drains that half.
-                if (!wait_bounded<Cfg::RL>(tempty_bar(Cfg::ACC_BUFS == 1 ? 0 : acc), acc_phase ^ 1u, p.err, p.timeout_ns,
+                if (!wait_bounded<Cfg::SETMAXNREG>(tempty_bar(Cfg::ACC_BUFS == 1 ? 0 : acc), acc_phase ^ 1u, p.err, p.timeout_ns,
                                   abort_flag, 3))
                     break;
                 tc_fence_after();
@@ -513,7 +526,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 for (int32_t kb = w.kb0; kb < w.kb1; ++kb) {
                     // The stage was written by TMA (async proxy) and completed through the
                     // mbarrier's transaction count: the wait alone orders the MMA's reads.
-                    if (!wait_bounded<Cfg::RL>(full_bar(stage), phase, p.err, p.timeout_ns, abort_flag, 4)) {
+                    if (!wait_bounded<Cfg::SETMAXNREG>(full_bar(stage), phase, p.err, p.timeout_ns, abort_flag, 4)) {
                         ok = false;
                         break;
                     }
@@ -524,7 +537,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 #pragma unroll
                     for (int nb = 0; nb < Cfg::N_MMAS; ++nb) {
                         if (nb == 1 && !hi_ready) {
-                            if (!wait_bounded<Cfg::RL>(tempty_bar(1), acc_phase ^ 1u, p.err, p.timeout_ns, abort_flag, 3)) {
+                            if (!wait_bounded<Cfg::SETMAXNREG>(tempty_bar(1), acc_phase ^ 1u, p.err, p.timeout_ns, abort_flag, 3)) {
                                 ok = false;
                                 break;
                             }
@@ -544,7 +557,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
                 if (ok && !hi_ready)  // (a segment always has k-blocks; keeps the phases in step regardless)
-                    ok = wait_bounded<Cfg::RL>(tempty_bar(1), acc_phase ^ 1u, p.err, p.timeout_ns, abort_flag, 3);
+                    ok = wait_bounded<Cfg::SETMAXNREG>(tempty_bar(1), acc_phase ^ 1u, p.err, p.timeout_ns, abort_flag, 3);
                 if (!ok) break;
                 if constexpr (PAIR == 1) mma_commit(tfull_bar(acc));
                 else mma_commit_pair(tfull_bar(acc), 0x3);
@@ -626,7 +639,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 auto put = [&](const uint32_t (&v)[36], uint32_t sh, int valid) {
                     int go = 1;
                     if (lane == 0)
-                        go = wait_bounded<Cfg::RL>(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 7) ? 1 : 0;
+                        go = wait_bounded<Cfg::SETMAXNREG>(empty_bar(stage), phase ^ 1u, p.err, p.timeout_ns, abort_flag, 7) ? 1 : 0;
                     go = __shfl_sync(0xffffffffu, go, 0);
                     if (!go) {
                         ok = false;
@@ -677,7 +690,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
     } else {
         // ------------------------------------------------------------ epilogue warps
-        if constexpr (Cfg::RL) setmaxnreg_inc<Cfg::REGS_EPI>();
+        if constexpr (Cfg::SETMAXNREG) setmaxnreg_inc<Cfg::REGS_EPI>();
         const int ew = warp - Cfg::EPI_W0;
         const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31 are this warp's
         uint8_t* ebuf = smem + Cfg::OFF_EPI + ew * Cfg::EPI_WARP_BYTES;
@@ -760,7 +773,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 if (!partial && p.beta != 0.0f) prefetch_cg(0);
             }
             int ok = 1;
-            if (lane == 0) ok = wait_bounded<Cfg::RL>(tfull_bar(acc), acc_phase, p.err, p.timeout_ns, abort_flag, 5) ? 1 : 0;
+            if (lane == 0) ok = wait_bounded<Cfg::SETMAXNREG>(tfull_bar(acc), acc_phase, p.err, p.timeout_ns, abort_flag, 5) ? 1 : 0;
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after();
@@ -914,7 +927,79 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         }
                         ++chunk_count;
                     };
-                    if constexpr (EPI == EPI_TMA_CG) {
+                    if constexpr (Cfg::H2 && !PARTS) {
+                        // Two epilogue warpgroups: warps EPI_W0 .. +3 take the first MMA's
+                        // columns [0, MMA_N), the next four the second's [MMA_N, BN).  Each warp
+                        // reads all of its part of its 32 rows into registers as fp16 (alpha
+                        // applied, rounded once), hands the part back to the MMA, and only then
+                        // stores it, chunk by chunk through its staging buffer.  The 48-column
+                        // tail of a 432-column tile goes first, straight from registers.
+                        constexpr int P0 = Cfg::MMA_N / 64;       // whole chunks of part 0
+                        constexpr int P1 = Cfg::FULL_CHUNKS - P0;  // whole chunks of part 1
+                        constexpr int PMAX = P0 > P1 ? P0 : P1;
+                        const int part = ew / 4;
+                        const int c0 = part == 0 ? 0 : P0;
+                        const int nch = part == 0 ? P0 : P1;
+                        const float al = p.alpha;
+                        if constexpr (Cfg::TAIL_COLS == 48) {
+                            if (part == 1) {
+                                uint32_t v0[32], v1[16];
+                                tmem_ld_32x32b_x32(t_row + Cfg::FULL_CHUNKS * 64, v0);
+                                tmem_ld_32x32b_x16(t_row + Cfg::FULL_CHUNKS * 64 + 32, v1);
+                                tmem_ld_wait();
+                                uint32_t o[32];
+#pragma unroll
+                                for (int j = 0; j < 16; ++j)
+                                    o[j] = pack_half2(al * __uint_as_float(v0[2 * j]), al * __uint_as_float(v0[2 * j + 1]));
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    o[16 + j] = pack_half2(al * __uint_as_float(v1[2 * j]), al * __uint_as_float(v1[2 * j + 1]));
+#pragma unroll
+                                for (int j = 24; j < 32; ++j) o[j] = 0u;
+                                const int64_t row = arow0 + lane;
+                                const int64_t col0 = acol0 + Cfg::FULL_CHUNKS * 64;
+                                const int valid = (row < p.M && col0 < p.N)
+                                                      ? static_cast<int>(p.N - col0 < Cfg::TAIL_COLS ? p.N - col0
+                                                                                                     : Cfg::TAIL_COLS)
+                                                      : 0;
+                                __half* const drow =
+                                    static_cast<__half*>(p.D) + static_cast<int64_t>(w.b) * p.strideD + row * p.ldd;
+                                store_row64(reinterpret_cast<uint16_t*>(drow + col0), valid, o,
+                                            GTN_ROW_CHECK(p.ext_d, p.err, CHK_EPI_D_ROW));
+                            }
+                        }
+                        uint32_t pk[PMAX][32];
+#pragma unroll
+                        for (int i = 0; i < PMAX; ++i) {
+                            if (i < nch) {
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    uint32_t v[32];
+                                    tmem_ld_32x32b_x32(t_row + (c0 + i) * 64 + h * 32, v);
+                                    tmem_ld_wait();
+#pragma unroll
+                                    for (int j = 0; j < 16; ++j)
+                                        pk[i][16 * h + j] =
+                                            pack_half2(al * __uint_as_float(v[2 * j]), al * __uint_as_float(v[2 * j + 1]));
+                                }
+                            }
+                        }
+                        arrive_tempty(part);
+#pragma unroll
+                        for (int i = 0; i < PMAX; ++i) {
+                            if (i < nch) {
+                                if (lane == 0) bulk_wait_group_read<0>();  // the staging buffer's last store has read it
+                                __syncwarp();
+                                const uint32_t sb = smem_u32(ebuf);
+                                const uint32_t row_addr = sb + lane * 128u;
+#pragma unroll
+                                for (int j = 0; j < 8; ++j)
+                                    st_shared_v4(row_addr + ((static_cast<uint32_t>(j) ^ (lane & 7u)) << 4), pk[i][4 * j],
+                                                 pk[i][4 * j + 1], pk[i][4 * j + 2], pk[i][4 * j + 3]);
+                                store_chunk(c0 + i, sb);
+                            }
+                        }
+                    } else if constexpr (EPI == EPI_TMA_CG) {
                         // D = alpha * acc + beta * C, C read from global memory at its own alignment
                         if constexpr (PARTS) prefetch_cg(0);
 #pragma unroll 1
@@ -1026,7 +1111,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                 // before the next chunk's C lands there
                                 bulk_wait_group_read<0>();
                                 if (c + 1 < BN / 64) issue_c(c + 1, buf ^ 1u);
-                                wait_bounded<Cfg::RL>(cload_bar(ew, static_cast<int>(buf)), (cphase >> buf) & 1u, p.err,
+                                wait_bounded<Cfg::SETMAXNREG>(cload_bar(ew, static_cast<int>(buf)), (cphase >> buf) & 1u, p.err,
                                              p.timeout_ns, abort_flag, 6);
                             }
                             cphase ^= 1u << buf;
@@ -1159,7 +1244,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         // for this tile's partial
                         int got = 1;
                         if (lane == 0)
-                            got = wait_bounded<Cfg::RL>(krank == 0 ? xfull_bar : xempty_bar,
+                            got = wait_bounded<Cfg::SETMAXNREG>(krank == 0 ? xfull_bar : xempty_bar,
                                                         krank == 0 ? xphase : xphase ^ 1u, p.err, p.timeout_ns,
                                                         abort_flag, 8) ? 1 : 0;
                         got = __shfl_sync(0xffffffffu, got, 0);
@@ -1239,8 +1324,10 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
             auto release_accumulator = [&]() {
                 if constexpr (Cfg::ACC_BUFS == 1) {
-                    if (!lo_released) arrive_tempty(0);
-                    arrive_tempty(1);
+                    if constexpr (!Cfg::H2) {  // (with two epilogue warpgroups each warp has handed its part back)
+                        if (!lo_released) arrive_tempty(0);
+                        arrive_tempty(1);
+                    }
                     acc_phase ^= 1u;
                 } else {
                     arrive_tempty(acc);

@@ -26,7 +26,7 @@ struct TcLauncher {
         e = cudaFuncSetAttribute(gemm_tn_tc_kernel<BN, PAIR, STAGES, EPI, SK>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        if constexpr (Cfg::RL) {
+        if constexpr (Cfg::SETMAXNREG) {
             // The warpgroups' register shares (setmaxnreg) add up to exactly MAX_REGS per
             // thread; a kernel built with any other count could leave an increase waiting
             // for registers that never come free, so it is refused.

@@ -74,6 +74,7 @@ static const TcVariant kVariants[] = {
     {64, 1, 9, EPI_SWAP, 1, 0},
     {512, 2, 4, EPI_TMA, 0, 0},
     {432, 2, 4, EPI_TMA, 0, 0},
+    {512, 2, 4, EPI_TMA | EPI_H2, 0, 0},
     {512, 2, 4, EPI_TMA, 1, 0},
     {512, 2, 4, EPI_TMA_C, 0, 0},
     {512, 2, 4, EPI_TMA_C, 1, 0},
