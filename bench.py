@@ -12,8 +12,10 @@ reduction, as the plan needs) runs inside it.  Rank 0 prints one JSON line.
   over device time measured with CUDA events on the launching stream; between
   steps L2 is flushed by writing a 256 MiB buffer outside the timed events.
 - roofline: the dominant (tensor-core GEMM) kernel's achieved TFLOP/s against
-  the measured peak in MEASURED_PEAKS.json (bf16 cuBLAS burst; fp16 has the
-  same nominal tensor rate), plus its DRAM traffic from the committed ncu
+  the measured peak in MEASURED_PEAKS.json (bf16 cuBLAS; fp16 has the same
+  nominal tensor rate): its sustained figure when the timed steps run back to
+  back for half a second or more (the part then sits at its power cap), else
+  its burst figure; plus the kernel's DRAM traffic from the committed ncu
   capture when that capture matches the current kernel sources.
 - e2e: the same metric through the same C call with the inputs copied from
   pinned host memory and D copied back inside the timed region.
@@ -48,6 +50,9 @@ METRIC = "TFLOPS and % of GB300 dense FP16 peak per config (1 GPU), vs CPU oracl
 UNIT = "TFLOP/s"
 MAIN_WORKLOAD = "gemm_8192"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# A timed region of back-to-back steps at least this long (seconds) is compared with the
+# sustained tensor peak, a shorter one with the burst peak.
+SUSTAINED_S = 0.5
 L2_FLUSH_BYTES = 256 << 20
 L2_BYTES = 129e6
 
@@ -590,12 +595,20 @@ def run_ours(args, rank, world, dist):
     roof, bound = roofline_tflops(w, peaks)
     kernel_tflops = w.flops / (statistics.median(times) * 1e-3) / 1e12
     traffic = ncu_traffic(args.workload)
+    # Steps timed back to back for half a second or more run at the part's power cap, as the
+    # sustained cuBLAS loop of the measured peaks does; shorter runs compare with its burst.
+    sustained = wall >= SUSTAINED_S and "bf16_tflops_sustained" in peaks
+    tensor_peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+    tensor_src = ("bf16 cuBLAS back to back for seconds (sustained, at the power cap)" if sustained
+                  else "bf16 cuBLAS burst") + "; fp16 nominal rate equals bf16"
     roofline = {"bound": "tensor" if bound == "tensor" else "hbm",
                 "achieved": kernel_tflops if bound == "tensor" else w.algorithmic_bytes / (statistics.median(times) * 1e-3) / 1e9,
-                "peak": peaks["bf16_tflops"] if bound == "tensor" else peaks["hbm_gbs"],
+                "peak": tensor_peak if bound == "tensor" else peaks["hbm_gbs"],
                 "unit": "TFLOP/s" if bound == "tensor" else "GB/s",
                 "traffic": traffic,
-                "peak_source": f"{peak_src} ({'bf16 cuBLAS burst; fp16 nominal rate equals bf16' if bound == 'tensor' else 'STREAM copy'})"}
+                "peak_source": f"{peak_src} ({tensor_src if bound == 'tensor' else 'STREAM copy'})"}
+    if bound == "tensor":
+        roofline["frac_of_burst_peak"] = kernel_tflops / peaks["bf16_tflops"]
     roofline["frac"] = roofline["achieved"] / roofline["peak"]
     if bound == "tensor":
         roofline["peak_at_max_clock"] = cpeaks["bf16_tflops"]
@@ -655,7 +668,8 @@ def run_ours(args, rank, world, dist):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": workload_config(w),
-        "frac_of_measured_peak": value / world / peaks["bf16_tflops"],
+        "frac_of_measured_peak": value / world / tensor_peak,
+        "measured_peak": {"tflops": tensor_peak, "kind": "sustained" if sustained else "burst"},
         "frac_of_peak_at_max_clock": value / world / cpeaks["bf16_tflops"],
         "roofline": roofline,
         "cpu_baseline": cpu,

@@ -29,7 +29,7 @@ def test_paths_with_own_loads_and_stores_pass_under_device_bounds_checks():
     env = dict(os.environ, GEMM_TN_F16_CHECKED="1")
     cmd = [sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", "-m", "gpu", *SELECTION,
            "-k", "not test_parity or packed or swap or generic or splitk or kcluster or k1 or k7 or k63 or k65 or batched"]
-    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=1500)
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     tail = (r.stdout + r.stderr)[-4000:]
     assert r.returncode == 0, tail
     assert " passed" in r.stdout and "skipped" not in r.stdout.splitlines()[-1], tail
