@@ -698,6 +698,7 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint32_t acc_phase = 0;
         uint32_t chunk_count = 0;
         uint32_t xphase = 0;  // cluster K split: parity of the next partial-buffer wait
+        bool x_first = true;  // cluster K split: no partial has gone through the buffers yet
         const bool use_c = (EB == EPI_GENERIC || EB == EPI_SWAP) && p.beta != 0.0f;
         // TMA epilogue with beta != 0: C boxes are fetched by TMA into the staging buffers.
         constexpr bool tma_c = EPI == EPI_TMA_C;
@@ -1237,19 +1238,38 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const int64_t n = arow0 + lane;
                     __half* Dp = static_cast<__half*>(p.D);
                     const __half* Cp = static_cast<const __half*>(p.C);
-                    // Cluster K split: this thread's row of the partial buffer (in CTA 0).
+                    // Cluster K split: this thread's row of the partial buffer.  CTA 1 stages its
+                    // partial in its own buffer and each warp sends its 32 rows to the same place in
+                    // CTA 0's with one bulk copy, whose bytes complete CTA 0's barrier: no
+                    // cluster-scope fence or remote arrive lies between the two main loops' end
+                    // and the sum.
                     const uint32_t xrow = smem_u32(smem + Cfg::OFF_X) + static_cast<uint32_t>((quarter * 32 + lane) * BN * 4);
+                    const uint32_t xwarp = smem_u32(smem + Cfg::OFF_X) + static_cast<uint32_t>(quarter * 32 * BN * 4);
+                    constexpr uint32_t XW_BYTES = 32u * BN * 4u;  // one warp's rows of the partial
                     if constexpr (Cfg::CK) {
-                        // CTA 1 waits until CTA 0 has read the previous tile's partial; CTA 0 waits
-                        // for this tile's partial
                         int got = 1;
-                        if (lane == 0)
-                            got = wait_bounded<Cfg::SETMAXNREG>(krank == 0 ? xfull_bar : xempty_bar,
-                                                        krank == 0 ? xphase : xphase ^ 1u, p.err, p.timeout_ns,
-                                                        abort_flag, 8) ? 1 : 0;
+                        if (krank == 0) {
+                            // arm this tile's phase with this warp's bytes, then wait for all four warps'
+                            if (lane == 0) {
+                                mbar_arrive_expect_tx(xfull_bar, XW_BYTES);
+                                got = wait_bounded<Cfg::SETMAXNREG>(xfull_bar, xphase, p.err, p.timeout_ns, abort_flag, 8)
+                                          ? 1 : 0;
+                            }
+                        } else if (!x_first) {
+                            // CTA 0 has read the previous partial out of its buffer, and this warp's
+                            // previous copy has read the staged rows
+                            if (lane == 0) {
+                                got = wait_bounded<Cfg::SETMAXNREG>(xempty_bar, xphase ^ 1u, p.err, p.timeout_ns, abort_flag, 8)
+                                          ? 1 : 0;
+                                bulk_wait_group_read<0>();
+                            }
+                        }
                         got = __shfl_sync(0xffffffffu, got, 0);
                         if (!got) return;
-                        fence_acq_rel_cluster();  // the peer's release (remote arrive) happens-before what follows
+                        // CTA 0's reads of the previous partial (released by its remote arrive)
+                        // happen before this tile's copy writes the buffer again
+                        if (krank == 1 && !x_first) fence_acq_rel_cluster();
+                        x_first = false;
                         xphase ^= 1u;
                     }
 #pragma unroll 1
@@ -1264,11 +1284,10 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         if constexpr (Cfg::CK) {
                             const uint32_t xa = xrow + static_cast<uint32_t>(c * 64);
                             if (krank == 1) {
-                                // hand the partial to CTA 0 and write nothing
-                                const uint32_t ra = map_to_cta(xa, 0);
+                                // stage the partial for CTA 0 and write nothing
 #pragma unroll
                                 for (int q = 0; q < 4; ++q)
-                                    st_cluster_v4(ra + 16u * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                                    st_shared_v4(xa + 16u * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                                 continue;
                             }
                             // CTA 0: add the partial, first half of K before the second
@@ -1315,9 +1334,19 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                         }
                     }
                     if constexpr (Cfg::CK) {
-                        // CTA 1: the partial is in CTA 0's buffer; CTA 0: the buffer may be refilled
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(map_to_cta(krank == 1 ? xfull_bar : xempty_bar, krank ^ 1u));
+                        if (krank == 1) {
+                            // the staged rows (generic proxy) are read by the bulk copy (async proxy)
+                            fence_proxy_async_smem();
+                            __syncwarp();
+                            if (lane == 0) {
+                                bulk_copy_to_cluster(map_to_cta(xwarp, 0), xwarp, XW_BYTES, map_to_cta(xfull_bar, 0));
+                                bulk_commit_group();
+                            }
+                        } else {
+                            // CTA 0: the buffer may be refilled
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive_cluster(map_to_cta(xempty_bar, 1));
+                        }
                     }
                 }
             };
@@ -1379,8 +1408,8 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 }
             }
         }
-        if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG || EPI == EPI_PARTIAL) {
-            if (lane == 0) bulk_wait_group<0>();
+        if constexpr (EB == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG || EPI == EPI_PARTIAL || Cfg::CK) {
+            if (lane == 0) bulk_wait_group<0>();  // (cluster K split: CTA 1's copies into CTA 0 have landed)
             __syncwarp();
         }
     }
