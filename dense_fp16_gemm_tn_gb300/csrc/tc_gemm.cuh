@@ -1300,6 +1300,13 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                 v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + __uint_as_float(x2));
                                 v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + __uint_as_float(x3));
                             }
+                            if (c == BN / 16 - 1) {
+                                // the whole partial is in registers: CTA 1 may send the next one (the
+                                // arrive's release then waits only for these reads, not for the D
+                                // stores that follow)
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive_cluster(map_to_cta(xempty_bar, 1));
+                            }
                         }
                         if (n < p.N) {
                             if constexpr (EB == EPI_SWAP) {
@@ -1342,10 +1349,6 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                 bulk_copy_to_cluster(map_to_cta(xwarp, 0), xwarp, XW_BYTES, map_to_cta(xfull_bar, 0));
                                 bulk_commit_group();
                             }
-                        } else {
-                            // CTA 0: the buffer may be refilled
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive_cluster(map_to_cta(xempty_bar, 1));
                         }
                     }
                 }
