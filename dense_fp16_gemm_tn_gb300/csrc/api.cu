@@ -349,6 +349,14 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
     if (!pub.stream_k && !pl.rl && !pl.ck && pl.var.bn > 256 && pl.epi == EPI_TMA &&
         find_tc_variant(pl.var.bn, pl.var.pair, EPI_TMA | EPI_H2, 0, &h2v))
         pl.var = h2v;
+    // Tiles of a single k-block (K <= 64: the attention score Q K^T) spend their time storing
+    // D: the variant with four staging buffers per epilogue warp and a three-stage ring keeps
+    // more TMA stores in flight (score 128 x 4096^2 x 64: 668 against 682 us; with two or
+    // five buffers, or a two-stage ring, it was slower).
+    if (!pub.stream_k && !pl.rl && !pl.ck && kb == 1 && pl.epi == EPI_TMA &&
+        find_tc_variant(pl.var.bn, pl.var.pair, EPI_TMA | EPI_SQ, 0, &h2v))
+        pl.var = h2v;
+    pub.stages = pl.var.stages;
     const int cl = pl.ck ? 2 : pair;  // CTAs per cluster
     pub.units = pub.stream_k ? pub.dp_tiles : tiles * pub.splits;
     pub.grid = pub.stream_k ? sk_groups * cl : std::min<int64_t>(pub.units, G) * cl;

@@ -13,6 +13,7 @@ bool launch_family_tma(const TcVariant& v, const CUtensorMap& tmA, const CUtenso
         return true;                                                                                  \
     }
     GTN_CASE(256, 1, 4, EPI_TMA, 0)
+    GTN_CASE(256, 1, 3, EPI_TMA | EPI_SQ, 0)
     GTN_CASE(256, 1, 4, EPI_TMA_C, 0)
     GTN_CASE(256, 1, 4, EPI_TMA_CG, 0)
     GTN_CASE(256, 1, 4, EPI_TMA, 1)
@@ -50,6 +51,7 @@ bool capacity_family_tma(const TcVariant& v, int sms, int64_t* cap) {
         return true;                                                        \
     }
     GTN_CASE(256, 1, 4, EPI_TMA, 0)
+    GTN_CASE(256, 1, 3, EPI_TMA | EPI_SQ, 0)
     GTN_CASE(256, 1, 4, EPI_TMA_C, 0)
     GTN_CASE(256, 1, 4, EPI_TMA_CG, 0)
     GTN_CASE(256, 1, 4, EPI_TMA, 1)

@@ -34,6 +34,9 @@ constexpr int EPI_CK = 0x200;
 // its 32 rows into registers as fp16 and hands the part back to the MMA before it stores
 // anything, so the next tile's MMAs wait only for tensor-memory reads, not for stores.
 constexpr int EPI_H2 = 0x400;
+// Variant flag (D = alpha*acc by TMA stores): four staging buffers per epilogue warp instead of
+// two, for tiles of one k-block, whose time goes to storing D (the attention score Q K^T).
+constexpr int EPI_SQ = 0x1000;
 
 #ifdef __CUDACC__
 #define GTN_HD __host__ __device__
@@ -51,6 +54,7 @@ GTN_HD constexpr bool epi_acc16(int epi) { return epi_mode(epi) == EPI_TMA_A16 |
 GTN_HD constexpr bool epi_rl(int epi) { return (epi & EPI_RL) != 0; }
 GTN_HD constexpr bool epi_ck(int epi) { return (epi & EPI_CK) != 0; }
 GTN_HD constexpr bool epi_h2(int epi) { return (epi & EPI_H2) != 0; }
+GTN_HD constexpr bool epi_sq(int epi) { return (epi & EPI_SQ) != 0; }
 
 struct KParams {
     // Tensor-core view: the MMA's A operand has rows_a rows, its B operand rows_b rows.

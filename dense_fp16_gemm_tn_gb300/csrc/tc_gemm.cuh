@@ -70,6 +70,8 @@ struct TileCfg {
     static constexpr bool RL = epi_rl(EPIX);     // row-loader warps for operands TMA cannot address
     static constexpr bool CK = epi_ck(EPIX);     // K halves on the two CTAs of a cluster (swapped tiles)
     static constexpr bool H2 = epi_h2(EPIX);     // one epilogue warpgroup per part of a wide accumulator
+    static constexpr bool SQ = epi_sq(EPIX);     // four TMA-store staging buffers per epilogue warp
+    static constexpr int NBUF = SQ ? 4 : 2;      // staging buffers of 32 x 64 halves per epilogue warp
     static constexpr int CLUSTER = (PAIR == 2 || CK) ? 2 : 1;
     static constexpr int BM = 128;               // accumulator rows per CTA (tensor-memory lanes)
     static constexpr int BK = 64;                // halves per 128-byte swizzled row
@@ -116,7 +118,7 @@ struct TileCfg {
                                    : (2 * BN <= 256) ? 256 : 512;
     static constexpr int EPI_WARP_BYTES =
         H2 ? 32 * 128  // one staging buffer per warp (eight warps)
-        : (epi_base(EPI) == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) ? 2 * 32 * 128
+        : (epi_base(EPI) == EPI_TMA || EPI == EPI_TMA_C || EPI == EPI_TMA_CG) ? NBUF * 32 * 128
         : (EPI == EPI_PARTIAL) ? 2 * 32 * 128  // TMA staging (or the padded transpose, 32 x 33 x 4)
         : (epi_base(EPI) == EPI_GENERIC) ? 32 * 33 * 4 : 0;
     static constexpr int OFF_A = 0;
@@ -157,6 +159,7 @@ struct TileCfg {
                           REGS_CTRL + REGS_EPI + 2 * REGS_RL == 4 * MAX_REGS),
                   "the warpgroups' register shares must add up to the block's launch allocation");
     static_assert(!H2 || (WIDE && EPI == EPI_TMA && PAIR == 2 && !RL && !CK), "two epilogue warpgroups: wide TMA tiles");
+    static_assert(!SQ || (EPI == EPI_TMA && !WIDE && !RL && !CK && !H2), "deep store queue: D = alpha*acc by TMA stores");
     // (with 104 registers the producer and MMA code of the 512-column tile compiles without
     // spills, and 200 hold an epilogue warp's 128 packed words of its part plus a load)
     static_assert(!H2 || (THREADS == 384 && MAX_REGS == 168 && REGS_CTRL + 2 * REGS_EPI == 3 * MAX_REGS),
@@ -1046,8 +1049,9 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                             uint32_t v0[32], v1[32];
                             fetch64(c, v0, v1);
                             fetched(c);
-                            const uint32_t buf = chunk_count & 1u;
-                            if (lane == 0) bulk_wait_group_read<1>();  // this buffer's previous store has read it
+                            const uint32_t buf = chunk_count & (Cfg::NBUF - 1);
+                            // this buffer's previous store has read it
+                            if (lane == 0) bulk_wait_group_read<Cfg::NBUF - 1>();
                             __syncwarp();
                             const uint32_t sb = smem_u32(ebuf) + buf * 4096u;
                             const uint32_t row_addr = sb + lane * 128u;

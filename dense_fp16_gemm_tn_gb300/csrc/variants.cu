@@ -22,6 +22,7 @@ bool capacity_family_swap(const TcVariant&, int, int64_t*);
 
 static const TcVariant kVariants[] = {
     {256, 1, 4, EPI_TMA, 0, 0},
+    {256, 1, 3, EPI_TMA | EPI_SQ, 0, 0},
     {256, 1, 4, EPI_TMA_C, 0, 0},
     {256, 1, 4, EPI_TMA_CG, 0, 0},
     {256, 1, 4, EPI_TMA, 1, 0},

@@ -168,6 +168,19 @@ def test_plan_wide_pair_tiles_only_for_many_full_waves_of_long_tiles():
         G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 0)
 
 
+def test_plan_single_k_block_tiles_take_the_deep_store_queue_variant():
+    # the attention score (K = 64, one k-block per tile, store-bound): 128 x 256 tiles with a
+    # three-stage ring and four staging buffers per epilogue warp
+    p = plan(4096, 4096, 64, batch=128, sA=4096 * 64, sB=4096 * 64, sD=4096 * 4096, sms=152)
+    assert p["tile_m"] == 128 and p["tile_n"] == 256 and p["cta_pair"] == 1 and p["stages"] == 3
+    assert p["epi_tma"] == 1
+    # two k-blocks: the four-stage ring
+    assert plan(4096, 4096, 128, batch=128, sA=4096 * 128, sB=4096 * 128, sD=4096 * 4096, sms=152)["stages"] == 4
+    # beta != 0 (C by TMA): no such variant
+    assert plan(4096, 4096, 64, batch=8, sA=4096 * 64, sB=4096 * 64, sC=4096 * 4096, sD=4096 * 4096, beta=1.0,
+                sms=152)["stages"] == 4
+
+
 def test_plan_forced_stream_k_splits_the_partial_wave():
     G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_STREAM_K, 1)
     G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 256)
