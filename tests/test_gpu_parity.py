@@ -48,6 +48,10 @@ CASES = [
     ("splitk_swap_beta", dict(M=24, N=700, K=1500, alpha=0.5, beta=1.5, opts=dict(force_splits=5))),
     ("splitk_normal", dict(M=256, N=256, K=4096, opts=dict(force_splits=4, force_pair=1))),
     ("splitk_normal_beta", dict(M=200, N=136, K=1000, alpha=0.5, beta=1.5, opts=dict(force_splits=3, force_pair=1))),
+    # tiles of one k-block with D = alpha A B^T by TMA stores: the four-staging-buffer variant
+    # (three-stage ring), ragged edges, a K tail inside the k-block, batches
+    ("store_queue_k40_batched", dict(M=1000, N=2104, K=40, batch=2, alpha=0.125)),
+    ("store_queue_k64_single_row_block", dict(M=100, N=1104, K=64)),
     ("k1", dict(M=130, N=136, K=1)),
     ("k7", dict(M=130, N=136, K=7)),
     ("k63", dict(M=130, N=136, K=63)),
@@ -116,6 +120,7 @@ EXACT = [
     ("exact_packed", dict(M=129, N=131, K=255)),
     ("exact_streamk_pair", dict(M=2560, N=2304, K=512, opts=dict(stream_k=1))),
     ("exact_streamk_swap", dict(M=16, N=1024, K=2048)),
+    ("exact_store_queue", dict(M=700, N=1304, K=64, batch=2)),
 ]
 
 
