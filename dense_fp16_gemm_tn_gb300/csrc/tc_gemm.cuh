@@ -1250,6 +1250,9 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                     const uint32_t xrow = smem_u32(smem + Cfg::OFF_X) + static_cast<uint32_t>((quarter * 32 + lane) * BN * 4);
                     const uint32_t xwarp = smem_u32(smem + Cfg::OFF_X) + static_cast<uint32_t>(quarter * 32 * BN * 4);
                     constexpr uint32_t XW_BYTES = 32u * BN * 4u;  // one warp's rows of the partial
+                    // Both CTAs of the cluster walk the same whole-tile units (the cluster K split
+                    // is data-parallel): another one follows this tile iff the iterator has one left.
+                    [[maybe_unused]] const bool x_more = SK || it.dp_next < p.num_units;
                     if constexpr (Cfg::CK) {
                         int got = 1;
                         if (krank == 0) {
@@ -1304,10 +1307,12 @@ gemm_tn_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                                 v[4 * q + 2] = __float_as_uint(__uint_as_float(v[4 * q + 2]) + __uint_as_float(x2));
                                 v[4 * q + 3] = __float_as_uint(__uint_as_float(v[4 * q + 3]) + __uint_as_float(x3));
                             }
-                            if (c == BN / 16 - 1) {
+                            if (c == BN / 16 - 1 && x_more) {
                                 // the whole partial is in registers: CTA 1 may send the next one (the
                                 // arrive's release then waits only for these reads, not for the D
-                                // stores that follow)
+                                // stores that follow).  After the cluster's last tile CTA 1 sends
+                                // nothing more, and the cluster-scope release would only delay the
+                                // stores.
                                 __syncwarp();
                                 if (lane == 0) mbar_arrive_cluster(map_to_cta(xempty_bar, 1));
                             }
