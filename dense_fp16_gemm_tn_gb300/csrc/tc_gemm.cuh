@@ -183,6 +183,7 @@ struct SegIter {
     int64_t dp_next;
     int32_t dp_wave;  // wave of the next data-parallel unit (dp_next / G)
     int64_t sk_i, sk_end;
+    int64_t sk_mid;   // >= 0: run [sk_mid, sk_end) before [sk_i, sk_mid) (see seg_begin)
 };
 
 __device__ __forceinline__ void tile_coords(const KParams& p, int64_t t, Seg& s) {
@@ -215,6 +216,17 @@ __device__ __forceinline__ SegIter seg_begin(const KParams& p, int64_t g, int64_
     it.dp_wave = 0;
     it.sk_i = (SK && p.sk_iters > 0) ? sk_start(p, g, G) : 0;
     it.sk_end = (SK && p.sk_iters > 0) ? sk_start(p, g + 1, G) : 0;
+    // A range that ends a tile and starts the next one is two segments on the two
+    // accumulators.  The first segment's epilogue parks its partial sums while the second
+    // runs, and the first whole tile after them needs the first accumulator back: when
+    // the first piece is the longer one, its parking outlasts the second piece's main
+    // loop and the MMA waits (2-4 us on 4096^3).  The shorter piece goes first instead.
+    it.sk_mid = -1;
+    if (SK && it.sk_i < it.sk_end) {
+        const int64_t kb = p.kb_total;
+        const int64_t b = (it.sk_i / kb + 1) * kb;  // first tile boundary after sk_i
+        if (b < it.sk_end && it.sk_end - b <= kb && it.sk_end - b < b - it.sk_i) it.sk_mid = b;
+    }
     return it;
 }
 
@@ -224,9 +236,10 @@ __device__ __forceinline__ bool seg_next(const KParams& p, SegIter& it, Seg& s) 
     // data-parallel work that follows instead of trailing the kernel.
     if (SK && it.sk_i < it.sk_end) {
         const int64_t kb = p.kb_total;
-        const int64_t tsk = it.sk_i / kb;
-        const int64_t k0 = it.sk_i - tsk * kb;
-        const int64_t k1 = min(kb, k0 + (it.sk_end - it.sk_i));
+        const int64_t lo = it.sk_mid >= 0 ? it.sk_mid : it.sk_i;  // start of this segment's iterations
+        const int64_t tsk = lo / kb;
+        const int64_t k0 = lo - tsk * kb;
+        const int64_t k1 = min(kb, k0 + (it.sk_end - lo));
         tile_coords(p, p.num_units + tsk, s);
         s.split = 0;
         s.rev = 0;
@@ -242,7 +255,12 @@ __device__ __forceinline__ bool seg_next(const KParams& p, SegIter& it, Seg& s) 
             s.sk_j = static_cast<int32_t>(it.g - first);
             s.sk_n = static_cast<int32_t>(sk_owner(p, (tsk + 1) * kb - 1, it.G) - first + 1);
         }
-        it.sk_i += k1 - k0;
+        if (it.sk_mid >= 0) {  // the later piece ran first; the earlier one follows
+            it.sk_end = it.sk_mid;
+            it.sk_mid = -1;
+        } else {
+            it.sk_i += k1 - k0;
+        }
         return true;
     }
     if (it.dp_next < p.num_units) {
