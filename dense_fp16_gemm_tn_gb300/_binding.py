@@ -39,6 +39,7 @@ GEMM_TN_OPT_SERPENTINE = 11
 GEMM_TN_OPT_ROW_LOADER = 12
 GEMM_TN_OPT_CHECK_TRIM_D = 13
 GEMM_TN_OPT_K_CLUSTER = 14
+GEMM_TN_OPT_SMALL = 15
 
 EXPORTED = ["gemm_tn_f16", "gemm_tn_f16_batched", "gemm_status_string", "gemm_tn_f16_last_device_error",
             "gemm_tn_f16_last_cuda_error", "gemm_tn_f16_shutdown", "gemm_tn_f16_version", "gemm_tn_f16_plan",

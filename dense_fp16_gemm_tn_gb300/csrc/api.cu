@@ -54,6 +54,7 @@ std::atomic<int64_t> g_opt_serpentine{0};
 std::atomic<int64_t> g_opt_row_loader{0};
 std::atomic<int64_t> g_opt_check_trim_d{0};
 std::atomic<int64_t> g_opt_k_cluster{0};
+std::atomic<int64_t> g_opt_small{0};
 
 gemm_status_t cuda_fail(cudaError_t e) {
     t_last_cuda_error = static_cast<int>(e);
@@ -242,6 +243,7 @@ struct Plan {
     int group_m;
     int32_t rl, rl_a, rl_b;  // row-loader variant; A / B read by its loader warps (not repacked)
     int32_t ck;              // cluster K split: the two CTAs of a cluster take the two halves of K
+    int32_t small_bn;        // > 0: small-problem kernel with tiles of 128 x small_bn
 };
 
 bool operand_tma_ok(bool aligned16, int64_t ld, int64_t stride, int64_t batch) {
@@ -363,8 +365,36 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
     pub.workspace_bytes = pl.pack_a_bytes + pl.pack_b_bytes + pl.partial_bytes + pl.sk_w_bytes + pl.sk_ctr_bytes;
 }
 
+// Tile width of the small-problem kernel for this problem, or 0 when the persistent
+// kernel takes it: K of at most four 64-wide blocks, K-major operands that tensor copies
+// address as they are, fp32 accumulation, and no option of the persistent kernel forced.
+int small_plan_width(const Problem& pr, int sms) {
+    const int64_t mode = g_opt_small.load();
+    if (mode < 0) return 0;
+    const int64_t kb = ceil_div(pr.K, 64);
+    if (kb < 1 || kb > kSmallMaxKb || pr.a_mn || pr.b_mn || pr.acc16 || pr.batch > 65535) return 0;
+    if (!operand_tma_ok(pr.align & 1u, pr.lda, pr.sA, pr.batch) || !operand_tma_ok(pr.align & 2u, pr.ldb, pr.sB, pr.batch))
+        return 0;
+    if (g_opt_force_pack.load() || g_opt_skip_first_load.load()) return 0;
+    const bool forced = g_opt_force_bn.load() || g_opt_force_pair.load() || g_opt_force_splits.load() ||
+                        g_opt_force_swap.load() || g_opt_force_generic.load() || g_opt_stream_k.load() ||
+                        g_opt_k_cluster.load() || g_opt_row_loader.load();
+    if (forced) return 0;
+    const int64_t tiles_m = ceil_div(pr.M, 128);
+    const int64_t t128 = tiles_m * ceil_div(pr.N, 128) * pr.batch;
+    // Automatic: 64-wide tiles when they fit one wave, where the persistent kernel's CTAs
+    // would each run one tile and pay its set-up for it (back to back, GB300: 256^3 5.3
+    // against 6.3 us, 512^2 x 128 5.3 against 5.9, 1000^2 x 96 5.2 against 6.3, 300 x 264
+    // x 256 with beta 6.1 against 7.3).  With 128-wide tiles near a full wave it lost
+    // (1536^2 x 128: 7.1 against 6.4 us), so larger problems stay on the persistent kernel.
+    if (mode == 0 && 2 * t128 > sms) return 0;
+    const int bn = (mode == 64 || mode == 128) ? static_cast<int>(mode) : (2 * t128 <= sms ? 64 : 128);
+    if (ceil_div(pr.N, bn) > 65535) return 0;
+    return bn;
+}
+
 // Tensor-core tile plan; pure host arithmetic, no CUDA calls.
-void make_plan(const Problem& pr, int sms, Plan& pl) {
+void make_plan(const Problem& pr, int sms, Plan& pl, bool allow_small = true) {
     std::memset(&pl, 0, sizeof(pl));
     gemm_tn_plan_t& pub = pl.pub;
     pub.splits = 1;
@@ -375,6 +405,17 @@ void make_plan(const Problem& pr, int sms, Plan& pl) {
     if (pr.K == 0) {
         pub.kernel = 1;
         pub.units = pr.batch;
+        return;
+    }
+    if (const int sbn = allow_small ? small_plan_width(pr, sms) : 0) {
+        pl.small_bn = sbn;
+        pub.kernel = 4;
+        pub.tile_m = 128;
+        pub.tile_n = sbn;
+        pub.cta_pair = 1;
+        pub.stages = static_cast<int32_t>(ceil_div(pr.K, 64));
+        pub.units = ceil_div(pr.M, 128) * ceil_div(pr.N, sbn) * pr.batch;
+        pub.grid = pub.units;
         return;
     }
     const bool force_pack = g_opt_force_pack.load() != 0;
@@ -640,6 +681,42 @@ gemm_status_t run(const void* A, const void* B, const void* C, void* D, const Pr
               (aligned16(D) ? 8u : 0u);
     Plan pl;
     make_plan(p, dev->sms, pl);
+
+    if (pl.small_bn > 0) {
+        // Small-problem kernel: operands read in place by tensor copies (boxes of 64 K x 128
+        // rows of A and 64 K x tile_n rows of B); should the driver refuse a map, the
+        // persistent kernel's plan takes over.
+        const bool a_b = p.batch > 1 && p.sA != 0, b_b = p.batch > 1 && p.sB != 0;
+        CUtensorMap sA_map, sB_map;
+        if (encode_map(&sA_map, A, p.K, p.M, p.batch, p.lda, p.sA, a_b, 64, 128) &&
+            encode_map(&sB_map, B, p.K, p.N, p.batch, p.ldb, p.sB, b_b, 64, static_cast<uint32_t>(pl.small_bn))) {
+            SmallParams sp;
+            std::memset(&sp, 0, sizeof(sp));
+            sp.M = static_cast<int32_t>(p.M);
+            sp.N = static_cast<int32_t>(p.N);
+            sp.kb = static_cast<int32_t>(ceil_div(p.K, 64));
+            sp.zA = a_b ? 1 : 0;
+            sp.zB = b_b ? 1 : 0;
+            sp.alpha = alpha;
+            sp.beta = p.beta;
+            sp.C = C;
+            sp.ldc = p.ldc;
+            sp.strideC = p.batch > 1 ? p.sC : 0;
+            sp.D = D;
+            sp.ldd = p.ldd;
+            sp.strideD = p.batch > 1 ? p.sD : 0;
+            sp.err = dev->err;
+            sp.timeout_ns = static_cast<uint64_t>(g_opt_timeout_ns.load());
+            sp.ext_c = p.beta != 0.0f
+                           ? extent_of(C, extent_bytes(p.M, p.N, p.ldc, p.sC, (p.batch > 1 && p.sC != 0) ? p.batch : 1))
+                           : Extent{};
+            sp.ext_d = extent_of(D, d_bytes - g_opt_check_trim_d.load());
+            e = launch_small_gemm(sA_map, sB_map, sp, pl.small_bn, ceil_div(p.M, 128), ceil_div(p.N, pl.small_bn),
+                                  p.batch, stream);
+            return e == cudaSuccess ? GEMM_OK : cuda_fail(e);
+        }
+        make_plan(p, dev->sms, pl, false);
+    }
 
     // Tensor maps first: an operand whose map the driver rejects is repacked instead.
     const bool swap = pl.pub.swap_ab != 0;
@@ -1241,6 +1318,10 @@ gemm_status_t gemm_tn_f16_set_option(int32_t option, int64_t value) {
             if (value < -1 || value > 1) return GEMM_ERR_INVALID_VALUE;
             g_opt_k_cluster = value;
             return GEMM_OK;
+        case GEMM_TN_OPT_SMALL:
+            if (value != -1 && value != 0 && value != 1 && value != 64 && value != 128) return GEMM_ERR_INVALID_VALUE;
+            g_opt_small = value;
+            return GEMM_OK;
 
     }
     return GEMM_ERR_INVALID_VALUE;
@@ -1262,6 +1343,7 @@ int64_t gemm_tn_f16_get_option(int32_t option) {
         case GEMM_TN_OPT_ROW_LOADER: return g_opt_row_loader.load();
         case GEMM_TN_OPT_CHECK_TRIM_D: return g_opt_check_trim_d.load();
         case GEMM_TN_OPT_K_CLUSTER: return g_opt_k_cluster.load();
+        case GEMM_TN_OPT_SMALL: return g_opt_small.load();
 
     }
     return -1;

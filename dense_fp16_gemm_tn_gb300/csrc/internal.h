@@ -59,6 +59,27 @@ cudaError_t launch_scale(int64_t M, int64_t N, int64_t batch, float beta, const 
                          int64_t strideC, void* D, int64_t ldd, int64_t strideD, int sms, cudaStream_t stream,
                          const ReduceChecks& chk);
 
+// Small-problem kernel (small_gemm.cu): one CTA per 128 x bn tile (bn = 64 or 128), grid
+// (tiles_m, tiles_n, batch), every k-block of K (at most kSmallMaxKb) loaded at once.
+// A and B are K-major and addressable by tensor copies (boxes of 64 K x 128 rows and
+// 64 K x bn rows); C and D of any alignment.
+constexpr int kSmallMaxKb = 4;
+struct SmallParams {
+    int32_t M, N;           // rows and columns of D per batch entry
+    int32_t kb;             // ceil(K / 64), 1..kSmallMaxKb
+    int32_t zA, zB;         // 1: operand has a batch dimension in its tensor map
+    float alpha, beta;
+    const void* C;          // read when beta != 0
+    int64_t ldc, strideC;
+    void* D;
+    int64_t ldd, strideD;
+    uint32_t* err;          // device error word
+    uint64_t timeout_ns;    // bound on every wait
+    Extent ext_c, ext_d;    // byte ranges of C and D (checked build)
+};
+cudaError_t launch_small_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const SmallParams& p, int bn,
+                              int64_t tiles_m, int64_t tiles_n, int64_t batch, cudaStream_t stream);
+
 // Fused score + softmax statistics kernel (score_softmax.cu).
 constexpr int kSoftmaxTileM = 128;  // query rows per work unit
 // Keys per score tile of the compiled kernel (the row count of its key boxes).

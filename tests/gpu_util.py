@@ -90,7 +90,8 @@ def options(**kw):
              "stream_k": G.GEMM_TN_OPT_STREAM_K, "group_m": G.GEMM_TN_OPT_GROUP_M,
              "serpentine": G.GEMM_TN_OPT_SERPENTINE,
              "row_loader": G.GEMM_TN_OPT_ROW_LOADER,
-             "k_cluster": G.GEMM_TN_OPT_K_CLUSTER}
+             "k_cluster": G.GEMM_TN_OPT_K_CLUSTER,
+             "small": G.GEMM_TN_OPT_SMALL}
     old = {k: G.gemm_tn_f16_get_option(names[k]) for k in kw}
     try:
         for k, v in kw.items():

@@ -435,3 +435,38 @@ def test_host_gemm_rejects_overlapping_buffers_without_a_gpu():
     # D overlapping A, and C overlapping D without being D
     assert f(0x1000, 8, 0x8000, 8, None, 8, 0x1010, 8, 8, 8, 8, 1.0, 0.0, check=False) == G.GEMM_ERR_INVALID_VALUE
     assert f(0x1000, 8, 0x8000, 8, 0x20010, 8, 0x20000, 8, 8, 8, 8, 1.0, 1.0, check=False) == G.GEMM_ERR_INVALID_VALUE
+
+
+def test_plan_small_problem_kernel_when_forced():
+    # every k-block of K <= 256 at once; tile width 64 while a wave of 128-wide tiles
+    # would fill at most half the SMs, else 128; forced widths honoured
+    G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_SMALL, 1)
+    try:
+        p = plan(128, 128, 128, sms=152)
+        q = plan(1000, 2000, 256, sms=152)  # 8 x 16 tiles of 128 x 128: more than half the SMs
+        r = plan(128, 128, 257, sms=152)  # five k-blocks: the persistent kernel
+        s = plan(128, 128, 128, lda=129, sms=152)  # rows tensor copies cannot address
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 256)
+        t = plan(128, 128, 128, sms=152)  # an option of the persistent kernel wins
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 0)
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_SMALL, 128)
+        u = plan(200, 136, 72, batch=3, sA=200 * 72, sB=136 * 72, sD=200 * 136, sms=152)
+    finally:
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 0)
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_SMALL, 0)
+    assert p["kernel"] == 4 and p["tile_m"] == 128 and p["tile_n"] == 64 and p["stages"] == 2
+    assert p["units"] == 2 and p["grid"] == 2 and p["workspace_bytes"] == 0
+    assert q["kernel"] == 4 and q["tile_n"] == 128 and q["units"] == 8 * 16 and q["stages"] == 4
+    assert r["kernel"] == 2 and s["kernel"] == 2 and t["kernel"] == 2
+    assert u["kernel"] == 4 and u["tile_n"] == 128 and u["units"] == 2 * 2 * 3
+    with pytest.raises(G.GemmError):
+        G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_SMALL, 32)
+
+
+def test_plan_small_problem_kernel_automatic_rule():
+    # 64-wide tiles while they fit one wave; larger problems stay on the persistent kernel
+    p = plan(1000, 1000, 96, sms=152)  # 8 x 16 = 128 tiles of 128 x 64
+    q = plan(1536, 1536, 128, sms=152)  # 12 x 24 = 288: more than a wave
+    r = plan(128, 128, 320, sms=152)  # five k-blocks
+    assert p["kernel"] == 4 and p["tile_n"] == 64 and p["units"] == 128
+    assert q["kernel"] == 2 and r["kernel"] == 2

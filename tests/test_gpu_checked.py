@@ -1,5 +1,5 @@
 """The checked build on the GPU: the misaligned-operand, row-word, row-loader, repack,
-split-K, swapped, wide-tile and K == 0 paths run again in a child process that loads
+split-K, swapped, wide-tile, small-problem and K == 0 paths run again in a child process that loads
 libgemm_tn_f16_checked.so (GEMM_TN_F16_CHECKED=1), where every load and store the
 kernels issue themselves is first tested against the byte range of its matrix.  Every
 result must still match the oracle and no check may fire; and in that build a trimmed
@@ -23,6 +23,7 @@ SELECTION = [
     "tests/test_gpu_dependent_launch.py",
     "tests/test_gpu_parity.py",
     "tests/test_gpu_wide.py",  # (the 432-column tile's tail chunk is stored from registers)
+    "tests/test_gpu_small.py",  # (D stored from registers)
 ]
 
 

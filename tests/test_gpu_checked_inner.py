@@ -1,7 +1,8 @@
 """Run only under the checked build (GEMM_TN_F16_CHECKED=1, from test_gpu_checked.py):
 a range for D trimmed by GEMM_TN_OPT_CHECK_TRIM_D makes the kernels' own stores past
 it fail their bounds check.  Each path that writes D itself -- the row-word epilogue,
-the predicated epilogue, the swapped epilogue, the split-K sum, the K == 0 scale --
+the predicated epilogue, the swapped epilogue, the split-K sum, the K == 0 scale, the
+small-problem kernel's 16-byte and element stores --
 must report GEMM_ERR_BOUNDS, leave the bytes past the trimmed range unwritten, and
 still write every other element correctly.  Nothing here touches memory outside the
 real buffers: the trimmed range is smaller than the allocation."""
@@ -23,6 +24,8 @@ CASES = [
     ("swapped_epilogue", 16, 1000, 300, 1000, {}),
     ("split_k_sum", 200, 136, 1000, 136, {"force_splits": 3, "force_pair": 1}),
     ("k_zero_scale", 130, 136, 0, 139, {}),
+    ("small_kernel_vector_stores", 300, 264, 128, 264, {"small": 128}),
+    ("small_kernel_element_stores", 300, 263, 128, 265, {"small": 64}),
 ]
 
 
