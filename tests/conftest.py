@@ -15,7 +15,7 @@ def pytest_configure(config):
 # Modules whose GPU tests take the library's automatic choice between the small-problem
 # kernel and the persistent kernel; every other GPU module was written for the persistent
 # kernel's paths (epilogues, swaps, K slices on small shapes too) and keeps them.
-AUTOMATIC_SMALL_KERNEL_MODULES = {"test_gpu_small", "test_gpu_workloads"}
+AUTOMATIC_SMALL_KERNEL_MODULES = {"test_gpu_small", "test_gpu_workloads", "test_gpu_random"}
 
 
 @pytest.fixture(autouse=True)

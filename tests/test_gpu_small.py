@@ -71,3 +71,33 @@ def test_small_kernel_is_the_automatic_choice(name, case):
     p = _plan_kernel(case["M"], case["N"], case["K"], case.get("batch", 1), beta=case.get("beta", 0.0))
     assert p["kernel"] == 4, p
     run_problem(**case)
+
+
+def _draw(rng):
+    """A seeded problem in the small kernel's reach: K <= 256, rows of A and B 16-byte
+    aligned, C and D at any leading dimension, batches with broadcast operands."""
+    K = int(rng.choice([1, 8, 40, 64, 100, 129, 192, 256]))
+    ld = lambda k: 8 * ((k + 7) // 8) + 8 * int(rng.choice([0, 0, 1]))
+    return dict(M=int(rng.choice([1, 5, 64, 127, 128, 200, 333, 520])), N=int(rng.choice([1, 9, 64, 65, 200, 511])),
+                K=K, batch=int(rng.choice([1, 1, 2, 3])), lda=ld(K), ldb=ld(K),
+                ldc_pad=int(rng.choice([0, 1, 7, 8])), ldd_pad=int(rng.choice([0, 1, 3, 8])),
+                alpha=float(rng.choice([1.0, -0.5, 2.0])), beta=float(rng.choice([0.0, 1.0, -0.25])),
+                bcast=int(rng.integers(0, 3)))
+
+
+RANDOM = [_draw(np.random.default_rng(2000 + i)) for i in range(16)]
+
+
+@pytest.mark.parametrize("case", RANDOM, ids=[f"r{i}" for i in range(len(RANDOM))])
+def test_small_kernel_random_problems(case):
+    c = dict(case)
+    M, N, K, batch = c["M"], c["N"], c["K"], c["batch"]
+    bc = c["bcast"] if batch > 1 else 0
+    kw = dict(batch=batch, alpha=c["alpha"], beta=c["beta"], lda=c["lda"], ldb=c["ldb"],
+              ldc=N + c["ldc_pad"], ldd=N + c["ldd_pad"], bcast_a=bc == 1, bcast_b=bc == 2, seed=M + N + K)
+    with options(small=1):
+        p = G.gemm_tn_f16_plan(M, N, K, batch, c["lda"], c["ldb"], kw["ldc"], kw["ldd"],
+                               0 if bc == 1 else M * c["lda"], 0 if bc == 2 else N * c["ldb"], M * kw["ldc"],
+                               M * kw["ldd"], c["beta"], 15, 152)
+    assert p["kernel"] == 4, (case, p)
+    run_problem(M, N, K, opts=dict(small=1), **kw)
