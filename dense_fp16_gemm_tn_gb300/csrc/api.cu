@@ -366,13 +366,14 @@ void plan_stream_k(const Problem& pr, Plan& pl, int64_t groups) {
 }
 
 // Tile width of the small-problem kernel for this problem, or 0 when the persistent
-// kernel takes it: K of at most four 64-wide blocks, K-major operands that tensor copies
-// address as they are, fp32 accumulation, and no option of the persistent kernel forced.
+// kernel takes it: every 64-wide block of K resident at once (at most 8 for 64-wide
+// tiles, 6 for 128-wide ones), K-major operands that tensor copies address as they are,
+// fp32 accumulation, and no option of the persistent kernel forced.
 int small_plan_width(const Problem& pr, int sms) {
     const int64_t mode = g_opt_small.load();
     if (mode < 0) return 0;
     const int64_t kb = ceil_div(pr.K, 64);
-    if (kb < 1 || kb > kSmallMaxKb || pr.a_mn || pr.b_mn || pr.acc16 || pr.batch > 65535) return 0;
+    if (kb < 1 || pr.a_mn || pr.b_mn || pr.acc16 || pr.batch > 65535) return 0;
     if (!operand_tma_ok(pr.align & 1u, pr.lda, pr.sA, pr.batch) || !operand_tma_ok(pr.align & 2u, pr.ldb, pr.sB, pr.batch))
         return 0;
     if (g_opt_force_pack.load() || g_opt_skip_first_load.load()) return 0;
@@ -383,13 +384,14 @@ int small_plan_width(const Problem& pr, int sms) {
     const int64_t tiles_m = ceil_div(pr.M, 128);
     const int64_t t128 = tiles_m * ceil_div(pr.N, 128) * pr.batch;
     // Automatic: 64-wide tiles when they fit one wave, where the persistent kernel's CTAs
-    // would each run one tile and pay its set-up for it (back to back, GB300: 256^3 5.3
-    // against 6.3 us, 512^2 x 128 5.3 against 5.9, 1000^2 x 96 5.2 against 6.3, 300 x 264
-    // x 256 with beta 6.1 against 7.3).  With 128-wide tiles near a full wave it lost
-    // (1536^2 x 128: 7.1 against 6.4 us), so larger problems stay on the persistent kernel.
+    // would each run one tile and pay its set-up for it (back to back, GB300: 256^3 5.1
+    // against 6.3 us, 1000^2 x 96 5.1 against 6.3, 300 x 264 x 256 with beta 6.1 against
+    // 7.3, 512^3 6.4 against 8.3, 1024^2 x 512 6.3 against 8.3, 64 x 2048 x 512 6.3 against
+    // 8.4).  With 128-wide tiles near a full wave it lost (1536^2 x 128: 7.1 against 6.4 us),
+    // so larger problems stay on the persistent kernel.
     if (mode == 0 && 2 * t128 > sms) return 0;
     const int bn = (mode == 64 || mode == 128) ? static_cast<int>(mode) : (2 * t128 <= sms ? 64 : 128);
-    if (ceil_div(pr.N, bn) > 65535) return 0;
+    if (kb > small_max_kb(bn) || ceil_div(pr.N, bn) > 65535) return 0;
     return bn;
 }
 

@@ -60,13 +60,14 @@ cudaError_t launch_scale(int64_t M, int64_t N, int64_t batch, float beta, const 
                          const ReduceChecks& chk);
 
 // Small-problem kernel (small_gemm.cu): one CTA per 128 x bn tile (bn = 64 or 128), grid
-// (tiles_m, tiles_n, batch), every k-block of K (at most kSmallMaxKb) loaded at once.
-// A and B are K-major and addressable by tensor copies (boxes of 64 K x 128 rows and
-// 64 K x bn rows); C and D of any alignment.
-constexpr int kSmallMaxKb = 4;
+// (tiles_m, tiles_n, batch), every k-block of K loaded at once: at most
+// small_max_kb(bn) of them (8 or 6, 192 KB of shared memory).  A and B are K-major and
+// addressable by tensor copies (boxes of 64 K x 128 rows and 64 K x bn rows); C and D
+// of any alignment.
+constexpr int small_max_kb(int bn) { return bn == 64 ? 8 : 6; }
 struct SmallParams {
     int32_t M, N;           // rows and columns of D per batch entry
-    int32_t kb;             // ceil(K / 64), 1..kSmallMaxKb
+    int32_t kb;             // ceil(K / 64), 1..small_max_kb(bn)
     int32_t zA, zB;         // 1: operand has a batch dimension in its tensor map
     float alpha, beta;
     const void* C;          // read when beta != 0

@@ -1,4 +1,5 @@
-// Small problems (K <= 256 and at most one wave of tiles): one CTA per 128 x BN tile of
+// Small problems (K of at most 512 / 384 for tiles 64 / 128 wide, and at most one wave of
+// tiles): one CTA per 128 x BN tile of
 // D, no persistent scheduling.  Thread 0 initialises one barrier per k-block and
 // issues every k-block's tensor copies at once, before anything else of the set-up,
 // so the loads are in flight while tensor memory is allocated; it then issues the
@@ -29,13 +30,15 @@ struct SmallCfg {
     static constexpr int A_BYTES = 128 * 128;  // 128 rows x 64 halves, 128-byte swizzle
     static constexpr int B_BYTES = BN * 128;   // BN rows x 64 halves
     static constexpr int STAGE = A_BYTES + B_BYTES;
-    static constexpr int OFF_BAR = kSmallMaxKb * STAGE;       // kSmallMaxKb full barriers + done
-    static constexpr int OFF_SLOT = OFF_BAR + 8 * (kSmallMaxKb + 1);
+    static constexpr int MAX_KB = small_max_kb(BN);           // every k-block resident at once
+    static constexpr int OFF_BAR = MAX_KB * STAGE;            // MAX_KB full barriers + done
+    static constexpr int OFF_SLOT = OFF_BAR + 8 * (MAX_KB + 1);
     static constexpr int OFF_ABORT = OFF_SLOT + 8;
     static constexpr int SMEM_BYTES = OFF_ABORT + 8 + 1024;  // + slack to align the base to 1024
     static constexpr uint32_t TMEM_COLS = BN;                 // a power of two >= 32
     static_assert(BN == 64 || BN == 128, "tile widths of the small-problem kernel");
     static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory of one CTA");
 };
 
 // Bounded wait on a barrier phase; on timeout records 0x500 | who and raises the CTA's
@@ -70,7 +73,7 @@ gemm_small_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
     const uint32_t bar0 = sbase + Cfg::OFF_BAR;
-    const uint32_t done_bar = bar0 + 8u * kSmallMaxKb;
+    const uint32_t done_bar = bar0 + 8u * Cfg::MAX_KB;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_SLOT);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_ABORT);
     const int warp = threadIdx.x >> 5;
@@ -221,7 +224,7 @@ cudaError_t launch_bn(const CUtensorMap& tmA, const CUtensorMap& tmB, const Smal
 
 cudaError_t launch_small_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const SmallParams& p, int bn,
                               int64_t tiles_m, int64_t tiles_n, int64_t batch, cudaStream_t stream) {
-    if (p.kb < 1 || p.kb > kSmallMaxKb || tiles_m < 1 || tiles_n < 1 || batch < 1 || tiles_m > 0x7fffffff ||
+    if (p.kb < 1 || p.kb > small_max_kb(bn) || tiles_m < 1 || tiles_n < 1 || batch < 1 || tiles_m > 0x7fffffff ||
         tiles_n > 65535 || batch > 65535)
         return cudaErrorInvalidValue;
     if (bn == 64) return launch_bn<64>(tmA, tmB, p, tiles_m, tiles_n, batch, stream);

@@ -264,7 +264,8 @@ typedef struct {
     int32_t kernel;          /* 0 none (empty problem), 1 scale-only (K == 0),
                                 2 tensor-core tile kernel, 3 split-K (+ reduction),
                                 4 small-problem kernel (one CTA per 128 x tile_n tile, every
-                                  k-block loaded at once: K <= 256; stages = k-blocks) */
+                                  k-block loaded at once: K <= 512 with tile_n 64, K <= 384
+                                  with tile_n 128; stages = k-blocks) */
     int32_t tile_m;          /* output rows per tile as seen by the tensor core (128 or 256) */
     int32_t tile_n;          /* output columns per tile as seen by the tensor core (16..256, or 432
                                 or 512: two MMAs, N = 256 and N = tile_n - 256, side by side on
@@ -347,14 +348,15 @@ GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int6
  *   GEMM_TN_OPT_K_CLUSTER         1: swapped small-M problems split K between the two CTAs
  *                                 of a cluster; -1: never; 0 (default): where two K slices and
  *                                 a separate sum would otherwise be planned.
- *   GEMM_TN_OPT_SMALL             small-problem kernel (K <= 256, K-major operands whose rows
+ *   GEMM_TN_OPT_SMALL             small-problem kernel (K <= 512 / 384 for tiles 64 / 128
+ *                                 wide, K-major operands whose rows
  *                                 tensor copies address as they are, fp32 accumulation):
  *                                 -1 never; 1 wherever it applies (tile width 64 when that
  *                                 keeps every tile in one wave at half the SMs, else 128);
  *                                 64 / 128 wherever it applies, with that tile width;
  *                                 0 (default): where 64-wide tiles fit one wave (batch x
- *                                 ceil(M/128) x ceil(N/64) <= SMs) and no option of the
- *                                 persistent kernel is forced.
+ *                                 ceil(M/128) x ceil(N/64) <= SMs), K <= 512, and no option
+ *                                 of the persistent kernel is forced.
  *   GEMM_TN_OPT_ROW_LOADER        1: K-major operands whose rows tensor copies cannot address
  *                                 are read by the kernel's own loader warps (CTA-pair 256x256
  *                                 and single-CTA 128x128 tiles, unswapped, no K slices)

@@ -438,13 +438,13 @@ def test_host_gemm_rejects_overlapping_buffers_without_a_gpu():
 
 
 def test_plan_small_problem_kernel_when_forced():
-    # every k-block of K <= 256 at once; tile width 64 while a wave of 128-wide tiles
+    # every k-block at once (K <= 512 / 384 for widths 64 / 128); tile width 64 while a wave of 128-wide tiles
     # would fill at most half the SMs, else 128; forced widths honoured
     G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_SMALL, 1)
     try:
         p = plan(128, 128, 128, sms=152)
         q = plan(1000, 2000, 256, sms=152)  # 8 x 16 tiles of 128 x 128: more than half the SMs
-        r = plan(128, 128, 257, sms=152)  # five k-blocks: the persistent kernel
+        r = plan(128, 128, 513, sms=152)  # nine k-blocks: the persistent kernel
         s = plan(128, 128, 128, lda=129, sms=152)  # rows tensor copies cannot address
         G.gemm_tn_f16_set_option(G.GEMM_TN_OPT_FORCE_BN, 256)
         t = plan(128, 128, 128, sms=152)  # an option of the persistent kernel wins
@@ -467,6 +467,8 @@ def test_plan_small_problem_kernel_automatic_rule():
     # 64-wide tiles while they fit one wave; larger problems stay on the persistent kernel
     p = plan(1000, 1000, 96, sms=152)  # 8 x 16 = 128 tiles of 128 x 64
     q = plan(1536, 1536, 128, sms=152)  # 12 x 24 = 288: more than a wave
-    r = plan(128, 128, 320, sms=152)  # five k-blocks
+    r = plan(128, 128, 576, sms=152)  # nine k-blocks
+    s = plan(1024, 1024, 512, sms=152)  # eight k-blocks, 128 tiles of 128 x 64
     assert p["kernel"] == 4 and p["tile_n"] == 64 and p["units"] == 128
     assert q["kernel"] == 2 and r["kernel"] == 2
+    assert s["kernel"] == 4 and s["tile_n"] == 64 and s["stages"] == 8

@@ -1,4 +1,4 @@
-"""The small-problem kernel (K <= 256, one CTA per 128 x 64 or 128 x 128 tile, every
+"""The small-problem kernel (K <= 512 / 384, one CTA per 128 x 64 or 128 x 128 tile, every
 k-block loaded at once, D written from registers) against the oracle, element by
 element: one tile and several, ragged M, N and K (tails inside a k-block, K = 1),
 beta != 0 with C and D rows 16-byte aligned and not (the element path), batches
@@ -24,7 +24,26 @@ CASES = [
     ("batched_beta", dict(M=200, N=136, K=72, batch=3, alpha=0.125, beta=1.0)),
     ("batched_bcast_b", dict(M=130, N=136, K=64, batch=4, bcast_b=True)),
     ("many_tiles", dict(M=1000, N=1000, K=96, alpha=0.5)),
+    ("six_kblocks_beta", dict(M=300, N=264, K=384, alpha=0.5, beta=-1.5)),
+    ("k_tail_in_sixth_block", dict(M=129, N=200, K=330, lda=336, ldb=344)),
 ]
+
+
+# eight k-blocks fit the 64-wide tiles only
+CASES_64 = [
+    ("eight_kblocks_beta", dict(M=260, N=136, K=512, alpha=0.25, beta=1.0)),
+    ("k_tail_in_eighth_block", dict(M=200, N=77, K=500, lda=504, ldb=512)),
+]
+
+
+@pytest.mark.parametrize("name,case", CASES_64, ids=[c[0] for c in CASES_64])
+def test_small_kernel_parity_long_k(name, case):
+    case = dict(case)
+    with options(small=64):
+        p = _plan_kernel(case["M"], case["N"], case["K"], case.get("batch", 1), case.get("lda"), case.get("ldb"),
+                         case.get("ldc"), case.get("ldd"), case.get("beta", 0.0))
+    assert p["kernel"] == 4 and p["tile_n"] == 64 and p["stages"] == (case["K"] + 63) // 64, p
+    run_problem(**case, opts=dict(small=64))
 
 
 def _plan_kernel(M, N, K, batch=1, lda=None, ldb=None, ldc=None, ldd=None, beta=0.0):
@@ -62,6 +81,7 @@ AUTO = [
     ("auto_small_m", dict(M=16, N=1024, K=128, alpha=0.5, beta=1.5)),
     ("auto_batched", dict(M=200, N=136, K=72, batch=3, alpha=0.125, beta=1.0)),
     ("auto_one_wave_of_64_wide_tiles", dict(M=1000, N=1000, K=200)),
+    ("auto_eight_kblocks", dict(M=1024, N=1024, K=512, alpha=0.5)),
 ]
 
 
@@ -74,7 +94,7 @@ def test_small_kernel_is_the_automatic_choice(name, case):
 
 
 def _draw(rng):
-    """A seeded problem in the small kernel's reach: K <= 256, rows of A and B 16-byte
+    """A seeded problem in the small kernel's reach at both widths: K <= 256, rows of A and B 16-byte
     aligned, C and D at any leading dimension, batches with broadcast operands."""
     K = int(rng.choice([1, 8, 40, 64, 100, 129, 192, 256]))
     ld = lambda k: 8 * ((k + 7) // 8) + 8 * int(rng.choice([0, 0, 1]))
