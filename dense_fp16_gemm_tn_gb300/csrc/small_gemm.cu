@@ -1,6 +1,6 @@
 // Small problems (K of at most 512 / 384 for tiles 64 / 128 wide, and at most one wave of
-// tiles): one CTA per 128 x BN tile of
-// D, no persistent scheduling.  Thread 0 initialises one barrier per k-block and
+// tiles): one CTA per 128 x BN tile of D, no persistent scheduling.  Thread 0
+// initialises one barrier per k-block and
 // issues every k-block's tensor copies at once, before anything else of the set-up,
 // so the loads are in flight while tensor memory is allocated; it then issues the
 // tile's MMAs (128 x BN x 16, fp16 in, fp32 accumulate) into tensor memory as each
