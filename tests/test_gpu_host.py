@@ -46,6 +46,12 @@ def test_host_gemm_one_block(pinned):
 
 
 @pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def test_host_gemm_one_block_with_beta_and_padding(pinned):
+    # one row block: copies and GEMM in order on the caller's stream
+    host_case(200, 136, 72, lda=80, ldb=75, ldc=140, ldd=139, alpha=-0.5, beta=1.5, pinned=pinned, seed=11)
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
 def test_host_gemm_several_row_blocks_with_beta_and_padding(pinned):
     # 2100 rows -> row blocks of 768: three blocks, the last one ragged
     host_case(2100, 777, 513, lda=520, ldb=515, ldc=780, ldd=790, alpha=0.5, beta=1.5, pinned=pinned, seed=7)
