@@ -348,15 +348,15 @@ GEMM_TN_API gemm_status_t gemm_tn_f16_plan(int64_t M, int64_t N, int64_t K, int6
  *   GEMM_TN_OPT_K_CLUSTER         1: swapped small-M problems split K between the two CTAs
  *                                 of a cluster; -1: never; 0 (default): where two K slices and
  *                                 a separate sum would otherwise be planned.
- *   GEMM_TN_OPT_SMALL             small-problem kernel (K <= 512 / 384 for tiles 64 / 128
- *                                 wide, K-major operands whose rows
- *                                 tensor copies address as they are, fp32 accumulation):
- *                                 -1 never; 1 wherever it applies (tile width 64 when that
- *                                 keeps every tile in one wave at half the SMs, else 128);
- *                                 64 / 128 wherever it applies, with that tile width;
- *                                 0 (default): where 64-wide tiles fit one wave (batch x
- *                                 ceil(M/128) x ceil(N/64) <= SMs), K <= 512, and no option
- *                                 of the persistent kernel is forced.
+ *   GEMM_TN_OPT_SMALL             small-problem kernel, which applies to K <= 512 / 384 for
+ *                                 tiles 64 / 128 wide, K-major operands whose rows tensor
+ *                                 copies address as they are and fp32 accumulation, and only
+ *                                 while no option of the persistent kernel is forced:
+ *                                 -1 never; 1 wherever it applies (tile width 64 when the
+ *                                 64-wide tiles fit one wave, else 128); 64 / 128 wherever
+ *                                 it applies, with that tile width; 0 (default): where the
+ *                                 64-wide tiles fit one wave (batch x ceil(M/128) x
+ *                                 ceil(N/64) <= SMs), with that width.
  *   GEMM_TN_OPT_ROW_LOADER        1: K-major operands whose rows tensor copies cannot address
  *                                 are read by the kernel's own loader warps (CTA-pair 256x256
  *                                 and single-CTA 128x128 tiles, unswapped, no K slices)
